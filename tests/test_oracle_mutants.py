@@ -1,0 +1,62 @@
+"""Plant mistakes in a copy of the CPU oracle and check that the pins catch them.
+
+Each mutant is the oracle's C source with one plausible slip (wrong tie rule,
+wrong block width, dropped term, wrong sign, wrong index).  It is compiled in
+a temporary directory, loaded in place of the real oracle, and every pin is
+run; the mutant must fail at least one.  Nothing here touches a GPU.
+"""
+import shutil
+
+import pytest
+
+import oracle
+import pins
+
+MUTANTS = {
+    "tie_to_higher_id": ("moe_oracle.c", "logit[e] > logit[best]", "logit[e] >= logit[best]"),
+    "logit_block_128": ("moe_oracle.h", "#define ORACLE_LOGIT_BLOCK 256", "#define ORACLE_LOGIT_BLOCK 128"),
+    "bias_dropped": ("moe_oracle.c", "logit[e] = logit[e] + bias[e];", "logit[e] = logit[e];"),
+    "softmax_sum_slot0": ("moe_oracle.c", "s = s + ex[j];", "s = s + ex[0];"),
+    "silu_sign": ("moe_oracle.c", "float silu = g / (1.0f + expf(-g));", "float silu = g / (1.0f + expf(g));"),
+    "gate_up_swapped": ("moe_oracle.c", "h[(size_t)r * I + i] = silu * u;",
+                        "h[(size_t)r * I + i] = u / (1.0f + expf(-u)) * g;"),
+    "dispatch_reverse_stable": ("moe_oracle.c", "int row = offsets[e] + fill[e];",
+                                "int row = offsets[e + 1] - 1 - fill[e];"),
+    "combine_weight_slot0": ("moe_oracle.c", "acc = acc + topk_w[(size_t)t * k + j] * y_perm[row * H + c];",
+                             "acc = acc + topk_w[(size_t)t * k] * y_perm[row * H + c];"),
+    "swiglu_bwd_sign": ("moe_oracle.c", "sg * (1.0f + g * (1.0f - sg))", "sg * (1.0f - g * (1.0f - sg))"),
+    "down_bwd_transposed": ("moe_oracle.c", "dh[i] = dh[i] + d[n] * widen_bf16(w[i]);",
+                            "dh[i] = dh[i] + d[n] * widen_bf16(Wd[((size_t)e * H + (i % H)) * I + (n % I)]);"),
+    "dWu_uses_dg": ("moe_oracle.c", "su[(size_t)i * H + c] = su[(size_t)i * H + c] + du[i] * a[c];",
+                    "su[(size_t)i * H + c] = su[(size_t)i * H + c] + dg[i] * a[c];"),
+    "router_bwd_sign": ("moe_oracle.c", "dl[(size_t)t * k + j] = w[j] * (g[j] - s);",
+                        "dl[(size_t)t * k + j] = w[j] * (g[j] + s);"),
+    "router_dx_wrong_column": ("moe_oracle.c", "Wr[(size_t)c * E + topk_idx[(size_t)t * k + j]]",
+                               "Wr[(size_t)c * E + j]"),
+    "accumulate_ignored": ("moe_oracle.c", "if (!accumulate) memset(p, 0, n * sizeof(float));",
+                           "memset(p, 0, n * sizeof(float));"),
+    "dispatch_bwd_drops_slot": ("moe_oracle.c", "for (int j = 0; j < k; ++j)\n        acc = acc + dx_perm",
+                                "for (int j = 1; j < k; ++j)\n        acc = acc + dx_perm"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(tmp_path, name):
+    fname, old, new = MUTANTS[name]
+    for f in ("moe_oracle.c", "moe_oracle.h"):
+        shutil.copy(oracle._DIR / f, tmp_path / f)
+    src = (tmp_path / fname).read_text()
+    assert src.count(old) == 1, f"mutation anchor not unique/present: {old!r}"
+    (tmp_path / fname).write_text(src.replace(old, new))
+    L = oracle.load(oracle.build(src_dir=tmp_path))
+    prev = oracle.use(L)
+    failed = []
+    try:
+        for pin in pins.ALL_PINS:
+            try:
+                pin()
+            except (AssertionError, RuntimeError):
+                failed.append(pin.__name__)
+    finally:
+        oracle.use(prev)
+    assert failed, f"mutant {name} passed every pin"
