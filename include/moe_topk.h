@@ -1,0 +1,228 @@
+/*
+ * moe_topk.h -- C ABI of the GB300 (sm_103a) MoE expert-layer library.
+ *
+ * The layer, as one GPU runs it for the tokens it holds:
+ *
+ *   forward   moe_route_topk -> moe_dispatch -> moe_grouped_gemm_swiglu
+ *             -> moe_grouped_gemm_down -> moe_combine
+ *   backward  moe_combine_bwd -> moe_grouped_gemm_down_bwd
+ *             -> moe_grouped_gemm_swiglu_bwd -> moe_dispatch_bwd
+ *             -> moe_route_topk_bwd
+ *
+ * Where the pages describe it:
+ *   - "FSDPTurbo EP/EFSDP and LlamaFactory FSDP2/CP Design", section 3, the
+ *     dispatcher table: the expert module is permute -> grouped matmul ->
+ *     unpermute with all-to-all token dispatch/combine around the grouped
+ *     matmul; the fused dispatcher must handle experts that receive no token.
+ *   - "Qwen3-MoE-30B-A3B模型EP+FSDP2并行方案", model section: 128 experts,
+ *     hidden 2048, expert intermediate 768, up [E,768,2048], down
+ *     [E,2048,768] (gate read as [E,768,2048] like up); section
+ *     "完整并行流程": experts are split over EP ranks in contiguous dim-0
+ *     blocks; section "为什么这么设计": the all-to-all moves tokens to their
+ *     experts forward and gradients back backward; section "Expert
+ *     Parallelism Details": after EP sharding the expert compute runs on
+ *     plain local tensors (hence raw pointers here).
+ *   - "TorchTitan FSDP2 完全指南", mixed-precision section: bf16 parameters,
+ *     fp32 gradient reduction (hence fp32 weight gradients).
+ * The router math, the activation and the permutation order are not written
+ * on the pages; the readings taken are stated at each function.
+ *
+ * Conventions (every function):
+ *   - Returns MOE_OK (0) or a negative MOE_ERR_* code; moe_last_error_string()
+ *     describes the last failure of the calling thread.
+ *   - Asynchronous on `stream` (a cudaStream_t passed as void*, NULL = the
+ *     legacy default stream).  Never synchronises (except
+ *     moe_read_device_status), never allocates, never aborts.
+ *   - All tensor pointers are DEVICE pointers owned by the caller, row-major,
+ *     contiguous.  "bf16" tensors are passed as void* and hold IEEE bfloat16.
+ *     Every tensor pointer must be 16-byte aligned.
+ *   - Shape limits checked on the host before any launch: H and I multiples
+ *     of 64, 1 <= E <= 1024, 1 <= k <= min(E, 32), T*k < 2^31, ep_size >= 1
+ *     dividing E, num_seg <= 1024.  Violations return MOE_ERR_INVALID_ARG /
+ *     MOE_ERR_UNSUPPORTED_SHAPE / MOE_ERR_ALIGNMENT and launch nothing.
+ *   - Scratch memory ("workspace", device, caller-owned) is sized by the
+ *     matching *_workspace_size query; a smaller ws_bytes returns
+ *     MOE_ERR_WORKSPACE.  A workspace may be reused by later calls on the
+ *     same stream; calls that overlap on the GPU need separate workspaces.
+ *   - Index data that lives on the device (topk_idx, offsets, segment
+ *     tables) cannot be checked on the host.  Kernels clamp every access
+ *     they derive from it, skip what is out of range, and record a device
+ *     status word that moe_read_device_status() returns.
+ *   - Results are deterministic: no floating-point atomics anywhere.
+ *   - Expert weights are read only.  Weight gradients are fp32 and are
+ *     overwritten, or added to when `accumulate` != 0.
+ */
+#ifndef MOE_TOPK_H
+#define MOE_TOPK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1)
+#define MOE_ERR_UNSUPPORTED_SHAPE (-2)
+#define MOE_ERR_ALIGNMENT (-3)
+#define MOE_ERR_WORKSPACE (-4)
+#define MOE_ERR_CUDA (-5)
+#define MOE_ERR_DEVICE_CHECK (-6)
+
+/* Device status bits recorded by kernels (see moe_read_device_status). */
+#define MOE_STATUS_BAD_INDEX 1      /* an expert id / row / offset was out of range */
+#define MOE_STATUS_BAD_SEGMENTS 2   /* a segment table was not monotone or exceeded R */
+#define MOE_STATUS_COUNT_MISMATCH 4 /* offsets disagree with the histogram of topk_idx */
+#define MOE_STATUS_TIMEOUT 8        /* a pipeline wait gave up (kernel returned early) */
+
+/* ABI version of this header (major * 100 + minor). */
+int moe_abi_version(void);
+
+/* Text of the last error returned to the calling host thread ("" if none). */
+const char* moe_last_error_string(void);
+
+/* Copies the device status word (OR of MOE_STATUS_* bits set by kernels
+ * since the last reset) to *status after synchronising `stream`; if reset is
+ * non-zero the word is cleared.  The only synchronising call of the library. */
+int moe_read_device_status(int* status, int reset, void* stream);
+
+/* ------------------------------------------------------------------------
+ * A1 + A2  router, top-k, expert histogram and offsets.
+ *
+ * For every token t:
+ *   logits[t,e] = sum_h x[t,h] * Wr[h,e]  (+ bias[e])
+ * in fp32 with a fixed order: h is cut into blocks of 256; each block is
+ * summed in increasing h with fused multiply-add starting from 0; block sums
+ * are added left to right; the bias is added last.  (Reading: the pages
+ * never write the router out; this order is fixed so that selection is
+ * reproducible bit for bit.)
+ *   topk_idx[t,0..k) = the k largest logits in descending order, equal
+ *                      logits to the lower expert id;
+ *   topk_w[t,j]      = softmax over the k selected logits (equivalently, a
+ *                      full softmax renormalised over the selected experts).
+ * Then over all T*k slots:
+ *   counts[e]        = number of slots routed to e;
+ *   offsets[0..E]    = exclusive prefix sum of counts (offsets[E] = T*k);
+ *   rank_offsets[r]  = offsets[r*E/ep_size], r = 0..ep_size: the row range
+ *                      of EP rank r's contiguous block of E/ep_size experts
+ *                      (the send-buffer split an all-to-all would use).
+ * x: bf16 [T,H]; Wr: fp32 [H,E]; bias: fp32 [E] or NULL (no gradient).
+ * Outputs: topk_idx int32 [T,k], topk_w fp32 [T,k], counts int32 [E],
+ * offsets int32 [E+1], rank_offsets int32 [ep_size+1].
+ * No capacity limit: every token keeps all k experts.  T == 0 is allowed.
+ * ---------------------------------------------------------------------- */
+size_t moe_route_topk_workspace_size(int T, int H, int E);
+int moe_route_topk(const void* x, const float* Wr, const float* bias, int T, int H, int E, int k,
+                   int ep_size, int32_t* topk_idx, float* topk_w, int32_t* counts,
+                   int32_t* offsets, int32_t* rank_offsets, void* ws, size_t ws_bytes,
+                   void* stream);
+
+/* ------------------------------------------------------------------------
+ * A3  dispatch (permute).
+ *
+ * Row of slot (t,j) with expert e = topk_idx[t,j]:
+ *   row(t,j) = offsets[e] + #{ t' < t : token t' routed to e }
+ * i.e. expert-contiguous, stable by token index (reading of "permute" in
+ * the dispatcher table; expert-ascending order makes each EP rank's block
+ * contiguous).  x_perm[row(t,j)] = x[t]; row_of_slot[t,j] = row(t,j);
+ * token_of_row[row(t,j)] = t.
+ * x: bf16 [T,H]; topk_idx int32 [T,k]; offsets int32 [E+1] (from
+ * moe_route_topk).  Outputs: x_perm bf16 [T*k,H], row_of_slot int32 [T,k],
+ * token_of_row int32 [T*k].  x_perm may be NULL (indices only).
+ * A histogram that disagrees with offsets sets MOE_STATUS_COUNT_MISMATCH.
+ * ---------------------------------------------------------------------- */
+size_t moe_dispatch_workspace_size(int T, int E, int k);
+int moe_dispatch(const void* x, const int32_t* topk_idx, const int32_t* offsets, int T, int H,
+                 int E, int k, void* x_perm, int32_t* row_of_slot, int32_t* token_of_row,
+                 void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Segment tables (grouped GEMMs).  Rows [seg_offsets[s], seg_offsets[s+1])
+ * of the grouped operand belong to expert seg_expert[s], or to expert s when
+ * seg_expert is NULL.  With num_seg = E and seg_offsets = offsets this is the
+ * layout moe_dispatch produces.  The general form covers the receive side of
+ * expert parallelism, where rows arrive as (source rank x local expert)
+ * blocks.  Segments may be empty; rows outside every segment are neither
+ * read for output nor written.  seg_offsets: int32 [num_seg+1], device.
+ * ---------------------------------------------------------------------- */
+
+/* A4  grouped gate/up GEMM with SwiGLU.
+ * For each row r of expert e:
+ *   g = x_perm[r] . Wg[e]^T,  u = x_perm[r] . Wu[e]^T   (fp32 accumulation)
+ *   h[r] = silu(g) * u,  silu(g) = g / (1 + exp(-g))  -> bf16
+ * x_perm bf16 [R,H]; Wg, Wu bf16 [E,I,H] ([E,out,in]); h bf16 [R,I];
+ * gu_save bf16 [R,2I] or NULL: g in columns [0,I), u in [I,2I) (kept for the
+ * backward pass).  ws may be NULL (no workspace needed). */
+int moe_grouped_gemm_swiglu(const void* x_perm, const void* Wg, const void* Wu, int num_seg,
+                            const int32_t* seg_offsets, const int32_t* seg_expert, int R, int H,
+                            int I, int E, void* h, void* gu_save, void* ws, size_t ws_bytes,
+                            void* stream);
+
+/* A5  grouped down GEMM: y_perm[r] = h[r] . Wd[e]^T (fp32 accumulation) -> bf16.
+ * h bf16 [R,I]; Wd bf16 [E,H,I]; y_perm bf16 [R,H].  ws may be NULL. */
+int moe_grouped_gemm_down(const void* h, const void* Wd, int num_seg, const int32_t* seg_offsets,
+                          const int32_t* seg_expert, int R, int H, int I, int E, void* y_perm,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/* A6  combine (unpermute): y[t] = sum_{j=0..k-1} topk_w[t,j] * y_perm[row_of_slot[t,j]],
+ * accumulated in fp32 in increasing j, rounded once to bf16.
+ * y_perm bf16 [R,H]; topk_w fp32 [T,k]; row_of_slot int32 [T,k]; y bf16 [T,H]. */
+int moe_combine(const void* y_perm, const float* topk_w, const int32_t* row_of_slot, int T, int H,
+                int k, void* y, void* stream);
+
+/* B1  combine backward.
+ *   dy_perm[row(t,j)] = topk_w[t,j] * dy[t]                  -> bf16
+ *   d_w[t,j]          = sum_h dy[t,h] * y_perm[row(t,j),h]   (fp32)
+ * dy bf16 [T,H]; y_perm bf16 [R,H]; outputs dy_perm bf16 [R,H], d_w fp32 [T,k]. */
+int moe_combine_bwd(const void* dy, const void* y_perm, const float* topk_w,
+                    const int32_t* row_of_slot, int T, int H, int k, void* dy_perm, float* d_w,
+                    void* stream);
+
+/* B2  down backward with the SwiGLU backward in its epilogue.
+ *   dh = dy_perm[r] . Wd[e]                         (fp32)
+ *   with s = sigmoid(g): dg = dh * u * s * (1 + g*(1 - s)),  du = dh * g * s
+ *   dgu[r] = [dg | du]                              -> bf16 [R,2I]
+ *   dWd[e] = sum over e's rows of dy_perm[r]^T h[r] (fp32 [E,H,I])
+ * gu_save is the [g|u] tensor written by moe_grouped_gemm_swiglu.  Experts
+ * with no rows get dWd[e] = 0 (or unchanged when accumulate != 0).  ws may be
+ * NULL. */
+int moe_grouped_gemm_down_bwd(const void* dy_perm, const void* h, const void* gu_save,
+                              const void* Wd, int num_seg, const int32_t* seg_offsets,
+                              const int32_t* seg_expert, int R, int H, int I, int E, void* dgu,
+                              float* dWd, int accumulate, void* ws, size_t ws_bytes, void* stream);
+
+/* B3  gate/up backward.
+ *   dx_perm[r] = dg[r] . Wg[e] + du[r] . Wu[e]   (one fp32 sum over 2I terms) -> bf16 [R,H]
+ *   dWg[e] = sum over e's rows of dg[r]^T x_perm[r],  dWu[e] likewise with du  (fp32 [E,I,H])
+ * dgu bf16 [R,2I] from moe_grouped_gemm_down_bwd.  ws may be NULL. */
+int moe_grouped_gemm_swiglu_bwd(const void* dgu, const void* x_perm, const void* Wg,
+                                const void* Wu, int num_seg, const int32_t* seg_offsets,
+                                const int32_t* seg_expert, int R, int H, int I, int E,
+                                void* dx_perm, float* dWg, float* dWu, int accumulate, void* ws,
+                                size_t ws_bytes, void* stream);
+
+/* B4  dispatch backward: dx_acc[t] = sum_{j=0..k-1} dx_perm[row_of_slot[t,j]] in fp32,
+ * increasing j.  dx_perm bf16 [R,H]; dx_acc fp32 [T,H]. */
+int moe_dispatch_bwd(const void* dx_perm, const int32_t* row_of_slot, int T, int H, int k,
+                     float* dx_acc, void* stream);
+
+/* B5  router backward.
+ *   dl[t,j] = topk_w[t,j] * (d_w[t,j] - sum_i topk_w[t,i] * d_w[t,i])
+ *             (gradient of the softmax over the selected logits; the
+ *             unselected logits, the indices and the bias get none)
+ *   dWr[h,e] = sum_t x[t,h] * dl[t,e]                  (fp32 [H,E])
+ *   dx[t,h]  = dx_acc[t,h] + sum_j dl[t,j] * Wr[h,topk_idx[t,j]]  -> bf16 [T,H]
+ * The two contractions run on the tensor cores with each fp32 operand split
+ * into a bf16 high part and a bf16 low part (products hi*hi + hi*lo + lo*hi,
+ * relative error about 2^-16).  dx_acc fp32 [T,H] from moe_dispatch_bwd. */
+size_t moe_route_topk_bwd_workspace_size(int T, int H, int E);
+int moe_route_topk_bwd(const float* d_w, const float* topk_w, const int32_t* topk_idx,
+                       const void* x, const float* Wr, const float* dx_acc, int T, int H, int E,
+                       int k, float* dWr, void* dx, int accumulate, void* ws, size_t ws_bytes,
+                       void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_TOPK_H */

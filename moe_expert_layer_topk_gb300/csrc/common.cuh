@@ -1,0 +1,69 @@
+// Shared host and device helpers of the MoE expert-layer library (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_topk.h"
+
+namespace moe {
+
+// ----------------------------------------------------------------- host side
+
+// Records a printf-style message for moe_last_error_string() and returns `code`.
+int fail(int code, const char* fmt, ...);
+// Clears the calling thread's last error.
+void clear_error();
+// Device address of the status word for the current device (nullptr on failure).
+int* status_word();
+// Multiprocessor count of the current device (cached; 0 on failure).
+int sm_count();
+// Current device ordinal (-1 on failure).
+int current_device();
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int check_launch(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return MOE_OK;
+}
+
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+constexpr int kMaxSegments = 1024;
+
+// Internal entry points shared between translation units (not exported).
+struct GroupedSegs {
+  int num_seg;
+  const int32_t* seg_offsets;
+  const int32_t* seg_expert;  // may be null (identity)
+};
+
+// Dense "row" GEMM with K-major A [M,K] and K-major B [N,K], both bf16, one
+// segment [0,M) and fp32 accumulation; epilogue out[m,n] = bf16(acc + add[m,n])
+// with `add` fp32 [M,N] (row stride N).  Used by the router backward.
+int launch_dense_add_bf16(const void* A, const void* B, const float* add, void* out, int M, int N,
+                          int K, cudaStream_t stream);
+// out[g] (fp32 [groups, M, N]) = sum over the K rows of segment g of A^T B,
+// with A [K_rows, M] and B [K_rows, N] bf16 row-major (both MN-major).  Used
+// by the router backward (split-K partials, overwrite).
+int launch_dw_split(const void* A, const void* B, int K_rows, int M, int N,
+                    const int32_t* seg_offsets, int num_seg, float* out, cudaStream_t stream);
+
+// ---------------------------------------------------------------- device side
+
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+__device__ __forceinline__ void set_status(int* status, int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+}  // namespace moe

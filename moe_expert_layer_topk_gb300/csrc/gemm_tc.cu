@@ -1,0 +1,1006 @@
+// Grouped GEMMs of the MoE expert layer on the 5th-generation tensor cores
+// (sm_103a): tcgen05.mma with fp32 accumulators in tensor memory (TMEM),
+// operands staged in shared memory by TMA (cp.async.bulk.tensor, 128-byte
+// swizzle), mbarrier producer/consumer pipeline, warp-specialised persistent
+// CTAs.
+//
+// "FSDPTurbo EP/EFSDP and LlamaFactory FSDP2/CP Design", section 3: the
+// expert compute between permute and unpermute is a grouped matmul over the
+// experts' row groups, and must cope with experts that receive no rows.
+// Shapes: "Qwen3-MoE-30B-A3B模型EP+FSDP2并行方案", model section (gate/up
+// [E,I,H], down [E,H,I]).  fp32 weight gradients: "TorchTitan FSDP2 完全指南",
+// mixed-precision section.
+//
+// One kernel template serves six GEMM shapes (`Kind`):
+//   GATE_UP_FWD    h = silu(A Wg^T) * (A Wu^T)  (+ save g, u)     A, B K-major
+//   DOWN_FWD       y = A Wd^T                                     A, B K-major
+//   DOWN_BWD_DX    dh = A Wd; SwiGLU backward in the epilogue     B MN-major
+//   GATE_UP_BWD_DX dx = dg Wg + du Wu (K = 2I, two B tensors)      B MN-major
+//   DW             dW[g] = sum over group g's rows of A^T B (fp32) A, B MN-major
+//   DENSE_ADD      out = bf16(A B^T + add)  (router backward)     A, B K-major
+//
+// CTA layout (192 threads, one CTA per SM, persistent over tiles):
+//   warp 0      TMA producer (one lane issues)
+//   warp 1      TMEM allocator + MMA issuer (one lane issues)
+//   warps 2..5  epilogue: TMEM -> registers -> global (warp w reads TMEM
+//               lanes 32*(w%4)..+31, i.e. accumulator rows)
+// Tile: 128 rows x BN columns (BN <= 256), k-block 64 (one 128-byte swizzle
+// row of bf16), 4-stage shared-memory ring, two 256-column accumulators in
+// TMEM so the epilogue of tile i overlaps the MMAs of tile i+1.
+//
+// Every wait on an mbarrier is bounded (globaltimer): on timeout the CTA
+// records MOE_STATUS_TIMEOUT, all roles leave their loops, outstanding MMAs
+// are drained with a bounded wait and TMEM is freed before returning.
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int THREADS = 192;
+constexpr int A_BYTES = BM * BK * 2;          // 16 KiB
+constexpr int B_BYTES_MAX = 256 * BK * 2;     // 32 KiB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES_MAX;
+constexpr int ACC_COLS = 256;
+constexpr int TMEM_COLS = 512;
+constexpr int CHUNK_BYTES = 64 * BK * 2;      // one 64(MN) x 64(K) MN-major box: 8 KiB
+constexpr unsigned long long TIMEOUT_NS = 2000000000ull;
+
+enum Kind : int { GATE_UP_FWD = 0, DOWN_FWD = 1, DOWN_BWD_DX = 2, GATE_UP_BWD_DX = 3, DW = 4, DENSE_ADD = 5 };
+
+struct Params {
+  int M;             // row kinds: rows of A (R).  DW: output rows per group.
+  int N;             // output columns
+  int K;             // row kinds: reduction length.  DW: rows of the K-indexed operands.
+  int BN;            // MMA N
+  int NH;            // GATE_UP_FWD: width of each of the g and u halves
+  int n_tiles;
+  int m_tiles;       // DW: m-tiles per group
+  int num_seg;
+  const int32_t* seg_offsets;
+  const int32_t* seg_expert;
+  int num_groups;    // experts (B row groups) / DW output groups
+  int b_group_rows;  // rows of the 2-D view of B per expert
+  int split_m;       // DW: rows m < split_m -> out0, else out1 (0: all out0)
+  int ldo;           // leading dimension of out0/out1 (elements)
+  int I;             // intermediate size (gu / dgu layouts)
+  uint32_t idesc;
+  int accumulate;
+  void* out0;
+  void* out1;
+  const void* aux;
+  int* status;
+};
+
+struct Ctl {
+  unsigned long long full[STAGES];
+  unsigned long long empty[STAGES];
+  unsigned long long tfull[2];
+  unsigned long long tempty[2];
+  unsigned long long drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int total_tiles;
+  int seg_tiles[kMaxSegments + 1];  // prefix sum of 128-row tiles per segment
+  int seg_off[kMaxSegments + 1];
+  int seg_exp[kMaxSegments];
+  int grp_rows[kMaxSegments];       // DW: rows per output group
+};
+
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Ctl);
+
+// ------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait for phase `parity` of an mbarrier.  Returns false when the
+// CTA is aborting or the wait timed out (which starts the abort).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl* ctl, int* status) {
+  unsigned long long t0 = 0;
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*reinterpret_cast<volatile int*>(&ctl->abort_flag)) return false;
+      const unsigned long long now = globaltimer();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > TIMEOUT_NS) {
+        *reinterpret_cast<volatile int*>(&ctl->abort_flag) = 1;
+        set_status(status, MOE_STATUS_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem], bf16 inputs, fp32 accumulation.
+__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive (once) on `bar` when all previously issued tcgen05 ops of this thread complete.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 layout, version 1), 128-byte swizzle.
+//   K-major operand: 8-row groups of 1024 B (SBO = 1024), k advanced by +32 B per 16 elements.
+//   MN-major operand: 64-element MN chunks LBO apart, 8-row K groups SBO = 1024 apart.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ float f32(uint32_t u) { return __uint_as_float(u); }
+
+// ----------------------------------------------------------------- the kernel
+
+template <int KIND>
+struct Traits {
+  static constexpr bool a_mn = (KIND == DW);
+  static constexpr bool b_mn = (KIND == DOWN_BWD_DX || KIND == GATE_UP_BWD_DX || KIND == DW);
+  static constexpr bool rows = (KIND != DW);
+};
+
+struct Tile {
+  int group;   // expert (row kinds) / output group (DW)
+  int m0;      // first row (row kinds: of A; DW: of the output)
+  int n0;      // first output column
+  int row_end; // row kinds: end of the segment (exclusive)
+  int seg;     // row kinds: segment index
+};
+
+template <int KIND>
+__device__ __forceinline__ Tile decode_tile(int tile, const Params& p, const Ctl* ctl) {
+  Tile t;
+  if constexpr (Traits<KIND>::rows) {
+    const int gm = tile / p.n_tiles, nt = tile % p.n_tiles;
+    int lo = 0, hi = p.num_seg - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (ctl->seg_tiles[mid] <= gm) lo = mid; else hi = mid - 1;
+    }
+    t.seg = lo;
+    t.group = ctl->seg_exp[lo];
+    t.m0 = ctl->seg_off[lo] + (gm - ctl->seg_tiles[lo]) * BM;
+    t.row_end = ctl->seg_off[lo + 1];
+    t.n0 = nt * (KIND == GATE_UP_FWD ? p.NH : p.BN);
+  } else {
+    const int per = p.m_tiles * p.n_tiles;
+    t.group = tile / per;
+    const int rem = tile % per;
+    t.m0 = (rem / p.n_tiles) * BM;
+    t.n0 = (rem % p.n_tiles) * p.BN;
+    t.row_end = 0;
+    t.seg = 0;
+  }
+  return t;
+}
+
+// Calls f(row0, valid_rows) for every k-block of a tile, in order.
+template <int KIND, class F>
+__device__ __forceinline__ void for_each_kblock(const Tile& t, const Params& p, const Ctl* ctl, F&& f) {
+  if constexpr (Traits<KIND>::rows) {
+    const int nkb = p.K / BK;
+    for (int kb = 0; kb < nkb; ++kb)
+      if (!f(kb * BK, BK)) return;
+  } else {
+    for (int s = 0; s < p.num_seg; ++s) {
+      if (ctl->seg_exp[s] != t.group) continue;
+      const int a = ctl->seg_off[s], b = ctl->seg_off[s + 1];
+      for (int r = a; r < b; r += BK)
+        if (!f(r, min(BK, b - r))) return;
+    }
+  }
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB0,
+                        const __grid_constant__ CUtensorMap tmB1, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + (size_t)STAGES * STAGE_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int limit = Traits<KIND>::rows ? p.M : p.K;  // rows addressable through the segment table
+
+  // ---- segment table -> shared memory (clamped; bad entries become empty)
+  for (int s = threadIdx.x; s <= p.num_seg; s += THREADS) {
+    // a null table means one segment covering every row
+    int o = p.seg_offsets ? p.seg_offsets[s] : (s == 0 ? 0 : limit);
+    if (o < 0 || o > limit) {
+      set_status(p.status, MOE_STATUS_BAD_SEGMENTS);
+      o = o < 0 ? 0 : limit;
+    }
+    ctl->seg_off[s] = o;
+  }
+  __syncthreads();
+  for (int s = threadIdx.x; s < p.num_seg; s += THREADS) {
+    int e = p.seg_expert ? p.seg_expert[s] : s;
+    if (e < 0 || e >= p.num_groups) {
+      set_status(p.status, MOE_STATUS_BAD_SEGMENTS);
+      e = -1;
+    }
+    if (ctl->seg_off[s + 1] < ctl->seg_off[s]) {
+      set_status(p.status, MOE_STATUS_BAD_SEGMENTS);
+      ctl->seg_off[s + 1] = ctl->seg_off[s];  // racy only for already-invalid tables
+    }
+    ctl->seg_exp[s] = e;
+  }
+  if (!Traits<KIND>::rows)
+    for (int g = threadIdx.x; g < p.num_groups; g += THREADS) ctl->grp_rows[g] = 0;
+  __syncthreads();
+  if (!Traits<KIND>::rows)
+    for (int s = threadIdx.x; s < p.num_seg; s += THREADS)
+      if (ctl->seg_exp[s] >= 0) atomicAdd(&ctl->grp_rows[ctl->seg_exp[s]], ctl->seg_off[s + 1] - ctl->seg_off[s]);
+  if (warp == 0) {
+    if constexpr (Traits<KIND>::rows) {
+      int carry = 0;
+      for (int base = 0; base < p.num_seg; base += 32) {
+        const int s = base + lane;
+        int n = 0;
+        if (s < p.num_seg && ctl->seg_exp[s] >= 0) {
+          const int len = ctl->seg_off[s + 1] - ctl->seg_off[s];
+          n = len > 0 ? (len + BM - 1) / BM : 0;
+        }
+        int incl = n;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int o = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += o;
+        }
+        if (s < p.num_seg) ctl->seg_tiles[s] = carry + incl - n;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) {
+        ctl->seg_tiles[p.num_seg] = carry;
+        ctl->total_tiles = carry * p.n_tiles;
+      }
+    } else {
+      if (lane == 0) ctl->total_tiles = p.num_groups * p.m_tiles * p.n_tiles;
+    }
+    if (lane == 0) {
+      for (int i = 0; i < STAGES; ++i) {
+        mbar_init(smem_u32(&ctl->full[i]), 1);
+        mbar_init(smem_u32(&ctl->empty[i]), 1);
+      }
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(smem_u32(&ctl->tfull[i]), 1);
+        mbar_init(smem_u32(&ctl->tempty[i]), 4);
+      }
+      mbar_init(smem_u32(&ctl->drain), 1);
+      ctl->abort_flag = 0;
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB0);
+      prefetch_tmap(&tmB1);
+    }
+  } else if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+  const int total = ctl->total_tiles;
+  const uint32_t b_bytes = (uint32_t)p.BN * BK * 2;
+
+  if (warp == 0) {
+    // ============================ TMA producer ============================
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const Tile t = decode_tile<KIND>(tile, p, ctl);
+        for_each_kblock<KIND>(t, p, ctl, [&](int row0, int) -> bool {
+          if (!wait_bar(smem_u32(&ctl->empty[stage]), phase ^ 1u, ctl, p.status)) {
+            ok = false;
+            return false;
+          }
+          const uint32_t fb = smem_u32(&ctl->full[stage]);
+          const uint32_t sA = smem_u32(smem + (size_t)stage * STAGE_BYTES);
+          const uint32_t sB = sA + A_BYTES;
+          mbar_arrive_expect_tx(fb, A_BYTES + b_bytes);
+          if constexpr (KIND == DW) {
+            tma_load_2d(sA, &tmA, fb, t.m0, row0);
+            tma_load_2d(sA + CHUNK_BYTES, &tmA, fb, t.m0 + 64, row0);
+            for (int c = 0; c < p.BN / 64; ++c)
+              tma_load_2d(sB + c * CHUNK_BYTES, &tmB0, fb, t.n0 + 64 * c, row0);
+          } else {
+            tma_load_2d(sA, &tmA, fb, row0, t.m0);
+            if constexpr (KIND == GATE_UP_FWD) {
+              const int brow = t.group * p.b_group_rows + t.n0;
+              tma_load_2d(sB, &tmB0, fb, row0, brow);
+              tma_load_2d(sB + (uint32_t)p.NH * BK * 2, &tmB1, fb, row0, brow);
+            } else if constexpr (KIND == DOWN_FWD || KIND == DENSE_ADD) {
+              tma_load_2d(sB, &tmB0, fb, row0, t.group * p.b_group_rows + t.n0);
+            } else if constexpr (KIND == DOWN_BWD_DX) {
+              for (int c = 0; c < p.BN / 64; ++c)
+                tma_load_2d(sB + c * CHUNK_BYTES, &tmB0, fb, t.n0 + 64 * c,
+                            t.group * p.b_group_rows + row0);
+            } else {  // GATE_UP_BWD_DX: k < I from Wg, k >= I from Wu
+              const bool up = row0 >= p.I;
+              const int krow = t.group * p.b_group_rows + (up ? row0 - p.I : row0);
+              for (int c = 0; c < p.BN / 64; ++c)
+                tma_load_2d(sB + c * CHUNK_BYTES, up ? &tmB1 : &tmB0, fb, t.n0 + 64 * c, krow);
+            }
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          return true;
+        });
+      }
+    }
+  } else if (warp == 1) {
+    // ============================ MMA issuer ==============================
+    int stage = 0;
+    uint32_t phase = 0;
+    int local = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++local) {
+      const Tile t = decode_tile<KIND>(tile, p, ctl);
+      const int buf = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1);
+      if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&ctl->tempty[buf]), (use & 1u) ^ 1u, ctl, p.status))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d = tmem_base + (uint32_t)(buf * ACC_COLS);
+      int nk = 0;
+      for_each_kblock<KIND>(t, p, ctl, [&](int, int valid) -> bool {
+        if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&ctl->full[stage]), phase, ctl, p.status))) {
+          ok = false;
+          return false;
+        }
+        uint8_t* sA = smem + (size_t)stage * STAGE_BYTES;
+        uint8_t* sB = sA + A_BYTES;
+        if (KIND == DW && valid < BK) {
+          // rows past the segment end belong to another group: zero them in
+          // both operands (each K row is one 128-byte line of every chunk)
+          const int a_chunks = 2, b_chunks = p.BN / 64;
+          const int nrows = BK - valid;
+          const int units = (a_chunks + b_chunks) * nrows * 8;
+          for (int u = lane; u < units; u += 32) {
+            const int chunk = u / (nrows * 8);
+            const int rem = u % (nrows * 8);
+            const int r = valid + rem / 8, c16 = rem % 8;
+            uint8_t* base = chunk < a_chunks ? sA + chunk * CHUNK_BYTES
+                                             : sB + (chunk - a_chunks) * CHUNK_BYTES;
+            *reinterpret_cast<uint4*>(base + r * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = Traits<KIND>::a_mn ? sdesc(a0 + kk * 2048, CHUNK_BYTES, 1024)
+                                                   : sdesc(a0 + kk * 32, 16, 1024);
+            const uint64_t bd = Traits<KIND>::b_mn ? sdesc(b0 + kk * 2048, CHUNK_BYTES, 1024)
+                                                   : sdesc(b0 + kk * 32, 16, 1024);
+            mma_bf16(d, ad, bd, p.idesc, (nk > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&ctl->empty[stage]));
+        }
+        __syncwarp();
+        ++nk;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        return true;
+      });
+      if (!ok) break;
+      if (lane == 0) mma_commit(smem_u32(&ctl->tfull[buf]));
+      __syncwarp();
+    }
+    if (!ok) {
+      // drain MMAs still in flight before TMEM is released
+      if (lane == 0) mma_commit(smem_u32(&ctl->drain));
+      __syncwarp();
+      const unsigned long long t0 = globaltimer();
+      while (!mbar_try_wait(smem_u32(&ctl->drain), 0) && globaltimer() - t0 < TIMEOUT_NS) {
+      }
+    }
+  } else {
+    // ============================ epilogue ================================
+    const int q = warp & 3;
+    const int row_in_tile = q * 32 + lane;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+      const Tile t = decode_tile<KIND>(tile, p, ctl);
+      const int buf = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1);
+      if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&ctl->tfull[buf]), use & 1u, ctl, p.status))) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * ACC_COLS);
+
+      if constexpr (KIND == GATE_UP_FWD) {
+        const int r = t.m0 + row_in_tile;
+        const bool valid = r < t.row_end;
+        __nv_bfloat16* h = static_cast<__nv_bfloat16*>(p.out0);
+        __nv_bfloat16* gu = static_cast<__nv_bfloat16*>(p.out1);
+        for (int c = 0; c < p.NH; c += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32(taddr + c, g);
+          tmem_ld32(taddr + p.NH + c, u);
+          tmem_wait_ld();
+          if (valid) {
+            uint32_t hp[16], gp[16], upk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float g0 = f32(g[2 * i]), g1 = f32(g[2 * i + 1]);
+              const float u0 = f32(u[2 * i]), u1 = f32(u[2 * i + 1]);
+              const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
+              const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
+              hp[i] = pack_bf16x2(h0, h1);
+              gp[i] = pack_bf16x2(g0, g1);
+              upk[i] = pack_bf16x2(u0, u1);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(h + (size_t)r * p.I + t.n0 + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(hp[4 * i], hp[4 * i + 1], hp[4 * i + 2], hp[4 * i + 3]);
+            if (gu) {
+              uint4* dg = reinterpret_cast<uint4*>(gu + (size_t)r * 2 * p.I + t.n0 + c);
+              uint4* du = reinterpret_cast<uint4*>(gu + (size_t)r * 2 * p.I + p.I + t.n0 + c);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                dg[i] = make_uint4(gp[4 * i], gp[4 * i + 1], gp[4 * i + 2], gp[4 * i + 3]);
+                du[i] = make_uint4(upk[4 * i], upk[4 * i + 1], upk[4 * i + 2], upk[4 * i + 3]);
+              }
+            }
+          }
+        }
+      } else if constexpr (KIND == DOWN_FWD || KIND == GATE_UP_BWD_DX || KIND == DENSE_ADD) {
+        const int r = t.m0 + row_in_tile;
+        const bool valid = r < t.row_end;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out0);
+        for (int c = 0; c < p.BN; c += 32) {
+          uint32_t a[32];
+          tmem_ld32(taddr + c, a);
+          tmem_wait_ld();
+          if (valid) {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = f32(a[i]);
+            if constexpr (KIND == DENSE_ADD) {
+              const float4* add = reinterpret_cast<const float4*>(
+                  static_cast<const float*>(p.aux) + (size_t)r * p.ldo + t.n0 + c);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float4 w = __ldg(add + i);
+                v[4 * i] += w.x; v[4 * i + 1] += w.y; v[4 * i + 2] += w.z; v[4 * i + 3] += w.w;
+              }
+            }
+            uint4* dst = reinterpret_cast<uint4*>(out + (size_t)r * p.ldo + t.n0 + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                  pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+          }
+        }
+      } else if constexpr (KIND == DOWN_BWD_DX) {
+        const int r = t.m0 + row_in_tile;
+        const bool valid = r < t.row_end;
+        const __nv_bfloat16* gu = static_cast<const __nv_bfloat16*>(p.aux);
+        __nv_bfloat16* dgu = static_cast<__nv_bfloat16*>(p.out0);
+        for (int c = 0; c < p.BN; c += 32) {
+          uint32_t a[32];
+          tmem_ld32(taddr + c, a);
+          tmem_wait_ld();
+          if (valid) {
+            const uint4* gsrc = reinterpret_cast<const uint4*>(gu + (size_t)r * 2 * p.I + t.n0 + c);
+            const uint4* usrc = reinterpret_cast<const uint4*>(gu + (size_t)r * 2 * p.I + p.I + t.n0 + c);
+            uint4* gdst = reinterpret_cast<uint4*>(dgu + (size_t)r * 2 * p.I + t.n0 + c);
+            uint4* udst = reinterpret_cast<uint4*>(dgu + (size_t)r * 2 * p.I + p.I + t.n0 + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint4 gv = __ldg(gsrc + i), uv = __ldg(usrc + i);
+              const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+              const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+              uint32_t og[4], ou[4];
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj) {
+                float dg2[2], du2[2];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                  const float g = hh ? bf16hi(gw[jj]) : bf16lo(gw[jj]);
+                  const float u = hh ? bf16hi(uw[jj]) : bf16lo(uw[jj]);
+                  const float dh = f32(a[8 * i + 2 * jj + hh]);
+                  const float sg = 1.0f / (1.0f + __expf(-g));
+                  dg2[hh] = dh * u * sg * (1.0f + g * (1.0f - sg));
+                  du2[hh] = dh * (g * sg);
+                }
+                og[jj] = pack_bf16x2(dg2[0], dg2[1]);
+                ou[jj] = pack_bf16x2(du2[0], du2[1]);
+              }
+              gdst[i] = make_uint4(og[0], og[1], og[2], og[3]);
+              udst[i] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+            }
+          }
+        }
+      } else {  // DW
+        const int m = t.m0 + row_in_tile;
+        const bool valid = m < p.M;
+        const bool nonempty = ctl->grp_rows[t.group] > 0;
+        float* dst_row = nullptr;
+        if (valid) {
+          if (p.split_m > 0 && m >= p.split_m)
+            dst_row = static_cast<float*>(p.out1) + ((size_t)t.group * p.split_m + (m - p.split_m)) * p.ldo;
+          else if (p.split_m > 0)
+            dst_row = static_cast<float*>(p.out0) + ((size_t)t.group * p.split_m + m) * p.ldo;
+          else
+            dst_row = static_cast<float*>(p.out0) + ((size_t)t.group * p.M + m) * p.ldo;
+        }
+        if (nonempty || !p.accumulate) {
+          for (int c = 0; c < p.BN; c += 32) {
+            uint32_t a[32];
+            if (nonempty) {
+              tmem_ld32(taddr + c, a);
+              tmem_wait_ld();
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) a[i] = 0u;
+            }
+            if (valid) {
+              float4* dst = reinterpret_cast<float4*>(dst_row + t.n0 + c);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                float4 v = make_float4(f32(a[4 * i]), f32(a[4 * i + 1]), f32(a[4 * i + 2]), f32(a[4 * i + 3]));
+                if (p.accumulate) {
+                  const float4 o = dst[i];
+                  v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+                }
+                dst[i] = v;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[buf]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// --------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor [outer, inner] row-major, box {box_inner, box_outer}, 128-byte swizzle.
+int make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+              uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {inner, outer > 0 ? outer : 1};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%llu x %llu] box %u x %u",
+                (int)r, (unsigned long long)outer, (unsigned long long)inner, box_inner, box_outer);
+  return MOE_OK;
+}
+
+uint32_t make_idesc(int n, bool a_mn, bool b_mn) {
+  return (1u << 4)                    // D fp32
+         | (1u << 7) | (1u << 10)     // A, B bf16
+         | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(n >> 3) << 17)   // N / 8
+         | ((uint32_t)(BM >> 4) << 24);  // M / 16
+}
+
+int pick_bn(int n) { return n % 256 == 0 ? 256 : (n % 128 == 0 ? 128 : 64); }
+
+bool g_attr[6][64] = {};
+
+template <int KIND>
+int launch(const Params& p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+           int upper_tiles, cudaStream_t s, const char* what) {
+  const int dev = current_device();
+  if (dev < 0) return fail(MOE_ERR_CUDA, "%s: no current CUDA device", what);
+  if (!g_attr[KIND][dev]) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<KIND>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    g_attr[KIND][dev] = true;
+  }
+  const int sms = sm_count();
+  if (sms <= 0) return fail(MOE_ERR_CUDA, "%s: cannot query the SM count", what);
+  int grid = upper_tiles < sms ? upper_tiles : sms;
+  if (grid < 1) grid = 1;
+  grouped_gemm_kernel<KIND><<<grid, THREADS, SMEM_BYTES, s>>>(a, b0, b1, p);
+  return check_launch(what);
+}
+
+int check_grouped(const char* fn, int num_seg, const int32_t* seg_offsets, int R, int H, int I, int E) {
+  if (R < 0 || H <= 0 || I <= 0 || E <= 0 || num_seg < 0)
+    return fail(MOE_ERR_INVALID_ARG, "%s: need R>=0, H>0, I>0, E>0, num_seg>=0", fn);
+  if (H % 64 || I % 64 || E > kMaxExperts || num_seg > kMaxSegments)
+    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "%s: need H%%64==0, I%%64==0, num_seg<=%d (H=%d I=%d num_seg=%d)",
+                fn, kMaxSegments, H, I, num_seg);
+  if (num_seg > 0 && !seg_offsets) return fail(MOE_ERR_INVALID_ARG, "%s: seg_offsets is NULL", fn);
+  return MOE_OK;
+}
+
+Params base_params(int num_seg, const int32_t* so, const int32_t* se, int groups) {
+  Params p{};
+  p.num_seg = num_seg;
+  p.seg_offsets = so;
+  p.seg_expert = se;
+  p.num_groups = groups;
+  p.status = status_word();
+  return p;
+}
+
+int row_tiles_upper(int R, int num_seg, int n_tiles) {
+  return (int)(((long long)(R + BM - 1) / BM + num_seg) * n_tiles);
+}
+
+}  // namespace tc
+
+// Router-backward helpers (declared in common.cuh).
+int launch_dense_add_bf16(const void* A, const void* B, const float* add, void* out, int M, int N,
+                          int K, cudaStream_t stream) {
+  using namespace tc;
+  if (M == 0) return MOE_OK;
+  // one segment [0, M): a null segment table stands for it
+  Params p = base_params(1, nullptr, nullptr, 1);
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.BN = pick_bn(N);
+  p.n_tiles = N / p.BN;
+  p.b_group_rows = 0;
+  p.ldo = N;
+  p.idesc = make_idesc(p.BN, false, false);
+  p.out0 = out;
+  p.aux = add;
+  CUtensorMap ta, tb;
+  if (int rc = make_tmap(&ta, A, K, M, 64, BM)) return rc;
+  if (int rc = make_tmap(&tb, B, K, N, 64, p.BN)) return rc;
+  return launch<DENSE_ADD>(p, ta, tb, tb, row_tiles_upper(M, 1, p.n_tiles), stream,
+                           "router backward dx GEMM");
+}
+
+int launch_dw_split(const void* A, const void* B, int K_rows, int M, int N,
+                    const int32_t* seg_offsets, int num_seg, float* out, cudaStream_t stream) {
+  using namespace tc;
+  Params p = base_params(num_seg, seg_offsets, nullptr, num_seg);
+  p.M = M;
+  p.N = N;
+  p.K = K_rows;
+  p.BN = pick_bn(N);
+  p.n_tiles = N / p.BN;
+  p.m_tiles = (M + BM - 1) / BM;
+  p.ldo = N;
+  p.idesc = make_idesc(p.BN, true, true);
+  p.out0 = out;
+  CUtensorMap ta, tb;
+  if (int rc = make_tmap(&ta, A, M, K_rows, 64, 64)) return rc;
+  if (int rc = make_tmap(&tb, B, N, K_rows, 64, 64)) return rc;
+  return launch<DW>(p, ta, tb, tb, num_seg * p.m_tiles * p.n_tiles, stream,
+                    "router backward dWr GEMM");
+}
+
+}  // namespace moe
+
+using namespace moe;
+using namespace moe::tc;
+
+extern "C" {
+
+int moe_grouped_gemm_swiglu(const void* x_perm, const void* Wg, const void* Wu, int num_seg,
+                            const int32_t* seg_offsets, const int32_t* seg_expert, int R, int H,
+                            int I, int E, void* h, void* gu_save, void* ws, size_t ws_bytes,
+                            void* stream) {
+  (void)ws; (void)ws_bytes;
+  clear_error();
+  const char* fn = "moe_grouped_gemm_swiglu";
+  if (int rc = check_grouped(fn, num_seg, seg_offsets, R, H, I, E)) return rc;
+  if (!x_perm || !Wg || !Wu || !h) return fail(MOE_ERR_INVALID_ARG, "%s: NULL pointer argument", fn);
+  if (!aligned16(x_perm) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(h) ||
+      (gu_save && !aligned16(gu_save)))
+    return fail(MOE_ERR_ALIGNMENT, "%s: tensors must be 16-byte aligned", fn);
+  if (R == 0 || num_seg == 0) return MOE_OK;
+  Params p = base_params(num_seg, seg_offsets, seg_expert, E);
+  p.M = R;
+  p.N = I;
+  p.K = H;
+  p.NH = (I % 128 == 0) ? 128 : 64;
+  p.BN = 2 * p.NH;
+  p.n_tiles = I / p.NH;
+  p.b_group_rows = I;
+  p.I = I;
+  p.idesc = make_idesc(p.BN, false, false);
+  p.out0 = h;
+  p.out1 = gu_save;
+  CUtensorMap ta, tg, tu;
+  if (int rc = make_tmap(&ta, x_perm, H, R, 64, BM)) return rc;
+  if (int rc = make_tmap(&tg, Wg, H, (uint64_t)E * I, 64, p.NH)) return rc;
+  if (int rc = make_tmap(&tu, Wu, H, (uint64_t)E * I, 64, p.NH)) return rc;
+  return launch<GATE_UP_FWD>(p, ta, tg, tu, row_tiles_upper(R, num_seg, p.n_tiles),
+                             static_cast<cudaStream_t>(stream), fn);
+}
+
+int moe_grouped_gemm_down(const void* h, const void* Wd, int num_seg, const int32_t* seg_offsets,
+                          const int32_t* seg_expert, int R, int H, int I, int E, void* y_perm,
+                          void* ws, size_t ws_bytes, void* stream) {
+  (void)ws; (void)ws_bytes;
+  clear_error();
+  const char* fn = "moe_grouped_gemm_down";
+  if (int rc = check_grouped(fn, num_seg, seg_offsets, R, H, I, E)) return rc;
+  if (!h || !Wd || !y_perm) return fail(MOE_ERR_INVALID_ARG, "%s: NULL pointer argument", fn);
+  if (!aligned16(h) || !aligned16(Wd) || !aligned16(y_perm))
+    return fail(MOE_ERR_ALIGNMENT, "%s: tensors must be 16-byte aligned", fn);
+  if (R == 0 || num_seg == 0) return MOE_OK;
+  Params p = base_params(num_seg, seg_offsets, seg_expert, E);
+  p.M = R;
+  p.N = H;
+  p.K = I;
+  p.BN = pick_bn(H);
+  p.n_tiles = H / p.BN;
+  p.b_group_rows = H;
+  p.ldo = H;
+  p.idesc = make_idesc(p.BN, false, false);
+  p.out0 = y_perm;
+  CUtensorMap ta, tb;
+  if (int rc = make_tmap(&ta, h, I, R, 64, BM)) return rc;
+  if (int rc = make_tmap(&tb, Wd, I, (uint64_t)E * H, 64, p.BN)) return rc;
+  return launch<DOWN_FWD>(p, ta, tb, tb, row_tiles_upper(R, num_seg, p.n_tiles),
+                          static_cast<cudaStream_t>(stream), fn);
+}
+
+int moe_grouped_gemm_down_bwd(const void* dy_perm, const void* h, const void* gu_save,
+                              const void* Wd, int num_seg, const int32_t* seg_offsets,
+                              const int32_t* seg_expert, int R, int H, int I, int E, void* dgu,
+                              float* dWd, int accumulate, void* ws, size_t ws_bytes, void* stream) {
+  (void)ws; (void)ws_bytes;
+  clear_error();
+  const char* fn = "moe_grouped_gemm_down_bwd";
+  if (int rc = check_grouped(fn, num_seg, seg_offsets, R, H, I, E)) return rc;
+  if (!dy_perm || !h || !gu_save || !Wd || !dgu || !dWd)
+    return fail(MOE_ERR_INVALID_ARG, "%s: NULL pointer argument", fn);
+  if (!aligned16(dy_perm) || !aligned16(h) || !aligned16(gu_save) || !aligned16(Wd) ||
+      !aligned16(dgu) || !aligned16(dWd))
+    return fail(MOE_ERR_ALIGNMENT, "%s: tensors must be 16-byte aligned", fn);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (R > 0 && num_seg > 0) {
+    // dgu = SwiGLU'(dy_perm . Wd[e])
+    Params p = base_params(num_seg, seg_offsets, seg_expert, E);
+    p.M = R;
+    p.N = I;
+    p.K = H;
+    p.BN = pick_bn(I);
+    p.n_tiles = I / p.BN;
+    p.b_group_rows = H;
+    p.I = I;
+    p.idesc = make_idesc(p.BN, false, true);
+    p.out0 = dgu;
+    p.aux = gu_save;
+    CUtensorMap ta, tb;
+    if (int rc = make_tmap(&ta, dy_perm, H, R, 64, BM)) return rc;
+    if (int rc = make_tmap(&tb, Wd, I, (uint64_t)E * H, 64, 64)) return rc;
+    if (int rc = launch<DOWN_BWD_DX>(p, ta, tb, tb, row_tiles_upper(R, num_seg, p.n_tiles), s, fn))
+      return rc;
+  }
+  // dWd[e] = dy_perm[rows of e]^T . h[rows of e]
+  if (num_seg == 0) {
+    if (accumulate) return MOE_OK;
+    cudaError_t e = cudaMemsetAsync(dWd, 0, sizeof(float) * (size_t)E * H * I, s);
+    return e == cudaSuccess ? MOE_OK : fail(MOE_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+  }
+  Params p = base_params(num_seg, seg_offsets, seg_expert, E);
+  p.M = H;
+  p.N = I;
+  p.K = R;
+  p.BN = pick_bn(I);
+  p.n_tiles = I / p.BN;
+  p.m_tiles = (H + BM - 1) / BM;
+  p.ldo = I;
+  p.idesc = make_idesc(p.BN, true, true);
+  p.accumulate = accumulate;
+  p.out0 = dWd;
+  CUtensorMap ta, tb;
+  if (int rc = make_tmap(&ta, dy_perm, H, R, 64, 64)) return rc;
+  if (int rc = make_tmap(&tb, h, I, R, 64, 64)) return rc;
+  return launch<DW>(p, ta, tb, tb, E * p.m_tiles * p.n_tiles, s, fn);
+}
+
+int moe_grouped_gemm_swiglu_bwd(const void* dgu, const void* x_perm, const void* Wg,
+                                const void* Wu, int num_seg, const int32_t* seg_offsets,
+                                const int32_t* seg_expert, int R, int H, int I, int E,
+                                void* dx_perm, float* dWg, float* dWu, int accumulate, void* ws,
+                                size_t ws_bytes, void* stream) {
+  (void)ws; (void)ws_bytes;
+  clear_error();
+  const char* fn = "moe_grouped_gemm_swiglu_bwd";
+  if (int rc = check_grouped(fn, num_seg, seg_offsets, R, H, I, E)) return rc;
+  if (!dgu || !x_perm || !Wg || !Wu || !dx_perm || !dWg || !dWu)
+    return fail(MOE_ERR_INVALID_ARG, "%s: NULL pointer argument", fn);
+  if (!aligned16(dgu) || !aligned16(x_perm) || !aligned16(Wg) || !aligned16(Wu) ||
+      !aligned16(dx_perm) || !aligned16(dWg) || !aligned16(dWu))
+    return fail(MOE_ERR_ALIGNMENT, "%s: tensors must be 16-byte aligned", fn);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (R > 0 && num_seg > 0) {
+    // dx_perm = [dg du] . [Wg[e]; Wu[e]]
+    Params p = base_params(num_seg, seg_offsets, seg_expert, E);
+    p.M = R;
+    p.N = H;
+    p.K = 2 * I;
+    p.BN = pick_bn(H);
+    p.n_tiles = H / p.BN;
+    p.b_group_rows = I;
+    p.I = I;
+    p.ldo = H;
+    p.idesc = make_idesc(p.BN, false, true);
+    p.out0 = dx_perm;
+    CUtensorMap ta, tg, tu;
+    if (int rc = make_tmap(&ta, dgu, 2 * I, R, 64, BM)) return rc;
+    if (int rc = make_tmap(&tg, Wg, H, (uint64_t)E * I, 64, 64)) return rc;
+    if (int rc = make_tmap(&tu, Wu, H, (uint64_t)E * I, 64, 64)) return rc;
+    if (int rc = launch<GATE_UP_BWD_DX>(p, ta, tg, tu, row_tiles_upper(R, num_seg, p.n_tiles), s, fn))
+      return rc;
+  }
+  if (num_seg == 0) {
+    if (accumulate) return MOE_OK;
+    cudaError_t e = cudaMemsetAsync(dWg, 0, sizeof(float) * (size_t)E * I * H, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dWu, 0, sizeof(float) * (size_t)E * I * H, s);
+    return e == cudaSuccess ? MOE_OK : fail(MOE_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+  }
+  // [dWg[e]; dWu[e]] = dgu[rows of e]^T . x_perm[rows of e]   (M = 2I split at I)
+  Params p = base_params(num_seg, seg_offsets, seg_expert, E);
+  p.M = 2 * I;
+  p.N = H;
+  p.K = R;
+  p.BN = pick_bn(H);
+  p.n_tiles = H / p.BN;
+  p.m_tiles = (2 * I + BM - 1) / BM;
+  p.split_m = I;
+  p.ldo = H;
+  p.idesc = make_idesc(p.BN, true, true);
+  p.accumulate = accumulate;
+  p.out0 = dWg;
+  p.out1 = dWu;
+  CUtensorMap ta, tb;
+  if (int rc = make_tmap(&ta, dgu, 2 * I, R, 64, 64)) return rc;
+  if (int rc = make_tmap(&tb, x_perm, H, R, 64, 64)) return rc;
+  return launch<DW>(p, ta, tb, tb, E * p.m_tiles * p.n_tiles, s, fn);
+}
+
+}  // extern "C"

@@ -1,0 +1,386 @@
+// A3 dispatch (permute), A6 combine (unpermute), B1 combine backward,
+// B4 dispatch backward.
+//
+// "FSDPTurbo EP/EFSDP and LlamaFactory FSDP2/CP Design", section 3: the
+// expert module runs permute -> grouped matmul -> unpermute.  The row order
+// (expert-contiguous, stable by token) is the reading stated in moe_topk.h;
+// with experts in ascending order every EP rank's block of experts
+// ("Qwen3-MoE-30B-A3B模型EP+FSDP2并行方案", "完整并行流程") is one contiguous
+// row range, which is the send buffer an all-to-all would consume.
+//
+// All four kernels are HBM-bound copies/reductions over 16-byte vectors
+// (8 bf16): every row is read and written with fully coalesced 16-byte
+// accesses, and each thread keeps all k of its independent loads in flight.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kChunkTok = 32;  // tokens per ranking chunk
+
+// --------------------------------------------------------------- histogram
+// blk_hist[c][e] = number of slots of chunk c routed to expert e.
+__global__ void __launch_bounds__(256) chunk_hist_kernel(const int32_t* __restrict__ topk_idx,
+                                                         int T, int E, int k, int nchunk,
+                                                         int32_t* __restrict__ chunk_base,
+                                                         int* status) {
+  extern __shared__ int hist[];  // [8 warps][E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * 8 + warp;
+  int* h = hist + (size_t)warp * E;
+  for (int e = lane; e < E; e += 32) h[e] = 0;
+  __syncwarp();
+  if (c < nchunk) {
+    const int s0 = c * kChunkTok * k;
+    const int s1 = min(T, (c + 1) * kChunkTok) * k;
+    for (int q = s0 + lane; q < s1; q += 32) {
+      const int e = topk_idx[q];
+      if (e >= 0 && e < E)
+        atomicAdd(&h[e], 1);
+      else
+        set_status(status, MOE_STATUS_BAD_INDEX);
+    }
+    __syncwarp();
+    for (int e = lane; e < E; e += 32) chunk_base[(size_t)c * E + e] = h[e];
+  }
+}
+
+// chunk_base[c][e] <- offsets[e] + sum_{c' < c} hist[c'][e]  (in place).
+__global__ void __launch_bounds__(1024) chunk_scan_kernel(int32_t* __restrict__ chunk_base,
+                                                          const int32_t* __restrict__ offsets,
+                                                          int nchunk, int E, int* status) {
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = offsets[e];
+    for (int c = 0; c < nchunk; ++c) {
+      const int v = chunk_base[(size_t)c * E + e];
+      chunk_base[(size_t)c * E + e] = run;
+      run += v;
+    }
+    if (run != offsets[e + 1]) set_status(status, MOE_STATUS_COUNT_MISMATCH);
+  }
+}
+
+// ------------------------------------------------------- rank and row copy
+// One CTA per chunk of 32 tokens.  Warp 0 hands out rows slot by slot in
+// (token, slot) order: lanes that hold the same expert in one batch of 32
+// slots get consecutive rows in lane order (= token order, since a token
+// picks an expert at most once).  Then all 8 warps copy the chunk's token
+// rows to their k destinations.
+__global__ void __launch_bounds__(256) dispatch_kernel(
+    const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ topk_idx,
+    const int32_t* __restrict__ chunk_base, int T, int H, int E, int k,
+    __nv_bfloat16* __restrict__ x_perm, int32_t* __restrict__ row_of_slot,
+    int32_t* __restrict__ token_of_row, int* status) {
+  extern __shared__ int sm[];
+  int* cnt = sm;                // [E]
+  int* rows = sm + E;           // [kChunkTok * k]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x;
+  const int t0 = c * kChunkTok;
+  const int nt = min(kChunkTok, T - t0);
+  const int nslot = nt * k;
+  const int R = T * k;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = chunk_base[(size_t)c * E + e];
+  __syncthreads();
+  if (warp == 0) {
+    for (int b = 0; b < nslot; b += 32) {
+      const int q = b + lane;
+      int e = -1;
+      if (q < nslot) {
+        e = topk_idx[(size_t)t0 * k + q];
+        if (e < 0 || e >= E) e = -1;
+      }
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      int row = -1;
+      if (e >= 0) row = cnt[e] + rank;
+      __syncwarp();
+      if (e >= 0 && rank == 0) cnt[e] += __popc(peers);
+      __syncwarp();
+      if (q < nslot) {
+        if (e < 0 || row < 0 || row >= R) {
+          set_status(status, MOE_STATUS_BAD_INDEX);
+          row = -1;
+        }
+        rows[q] = row;
+        row_of_slot[(size_t)t0 * k + q] = row;
+        if (row >= 0) token_of_row[row] = t0 + q / k;
+      }
+    }
+  }
+  __syncthreads();
+  if (!x_perm) return;
+  const int nvec = H / 8;  // 16-byte vectors per row
+  for (int i = warp; i < nt; i += 8) {
+    const int t = t0 + i;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    for (int v0 = 0; v0 < nvec; v0 += 32 * 8) {
+      uint4 buf[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v < nvec) buf[u] = __ldg(src + v);
+      }
+      for (int j = 0; j < k; ++j) {
+        const int row = rows[i * k + j];
+        if (row < 0) continue;
+        uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)row * H);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int v = v0 + u * 32 + lane;
+          if (v < nvec) dst[v] = buf[u];
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ combine
+// Thread = one 16-byte vector (8 columns) of one token; k independent row
+// loads, fp32 accumulation in slot order, one bf16 rounding.
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  f[0] = bf16lo(v.x); f[1] = bf16hi(v.x); f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+  f[4] = bf16lo(v.z); f[5] = bf16hi(v.z); f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+template <bool kWeighted, bool kF32Out>
+__global__ void __launch_bounds__(256) gather_sum_kernel(const __nv_bfloat16* __restrict__ src,
+                                                         const float* __restrict__ topk_w,
+                                                         const int32_t* __restrict__ row_of_slot,
+                                                         int T, int H, int k, int R,
+                                                         void* __restrict__ out, int* status) {
+  const int nvec = H / 8;
+  const size_t total = (size_t)T * nvec;
+  for (size_t gid = blockIdx.x * (size_t)blockDim.x + threadIdx.x; gid < total;
+       gid += (size_t)gridDim.x * blockDim.x) {
+    const int t = (int)(gid / nvec), v = (int)(gid % nvec);
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      uint4 buf[8];
+      float wv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u;
+        buf[u] = make_uint4(0, 0, 0, 0);
+        wv[u] = 0.f;
+        if (j < k) {
+          const int row = __ldg(row_of_slot + (size_t)t * k + j);
+          if (row >= 0 && row < R) {
+            buf[u] = __ldg(reinterpret_cast<const uint4*>(src + (size_t)row * H) + v);
+            wv[u] = kWeighted ? __ldg(topk_w + (size_t)t * k + j) : 1.f;
+          } else {
+            set_status(status, MOE_STATUS_BAD_INDEX);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (j0 + u < k) {
+          float f[8];
+          unpack8(buf[u], f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            acc[i] = kWeighted ? __fmaf_rn(wv[u], f[i], acc[i]) : __fadd_rn(acc[i], f[i]);
+        }
+      }
+    }
+    if (kF32Out) {
+      float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + (size_t)t * H) + 2 * v;
+      o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    } else {
+      reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + (size_t)t * H)[v] = pack8(acc);
+    }
+  }
+}
+
+// ------------------------------------------------------------ combine bwd
+// CTA per token: for every slot the CTA writes dy_perm[row] = w * dy[t] and
+// reduces the dot product dy[t] . y_perm[row] (per-thread partials, then a
+// fixed-order warp and block reduction).  Slots go in batches of 8 so that
+// eight independent row loads per thread are in flight.
+__global__ void __launch_bounds__(256) combine_bwd_kernel(
+    const __nv_bfloat16* __restrict__ dy, const __nv_bfloat16* __restrict__ y_perm,
+    const float* __restrict__ topk_w, const int32_t* __restrict__ row_of_slot, int T, int H, int k,
+    int R, __nv_bfloat16* __restrict__ dy_perm, float* __restrict__ d_w, int* status) {
+  __shared__ float red[8][kMaxTopK];
+  const int t = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nvec = H / 8;
+  for (int j0 = 0; j0 < k; j0 += 8) {
+    int rows[8];
+    float wv[8], part[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = j0 + u;
+      rows[u] = -1;
+      wv[u] = 0.f;
+      part[u] = 0.f;
+      if (j < k) {
+        const int row = __ldg(row_of_slot + (size_t)t * k + j);
+        if (row >= 0 && row < R) {
+          rows[u] = row;
+          wv[u] = __ldg(topk_w + (size_t)t * k + j);
+        } else {
+          set_status(status, MOE_STATUS_BAD_INDEX);
+        }
+      }
+    }
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+      float g[8];
+      unpack8(__ldg(reinterpret_cast<const uint4*>(dy + (size_t)t * H) + v), g);
+      uint4 yb[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        yb[u] = rows[u] >= 0 ? __ldg(reinterpret_cast<const uint4*>(y_perm + (size_t)rows[u] * H) + v)
+                             : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (rows[u] < 0) continue;
+        float yv[8], o[8];
+        unpack8(yb[u], yv);
+        float p = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          o[i] = wv[u] * g[i];
+          p = __fmaf_rn(g[i], yv[i], p);
+        }
+        reinterpret_cast<uint4*>(dy_perm + (size_t)rows[u] * H)[v] = pack8(o);
+        part[u] += p;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      float p = part[u];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+      if (lane == 0 && j0 + u < k) red[warp][j0 + u] = p;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < k) {
+    float s = 0.f;
+    for (int w = 0; w < 8; ++w) s += red[w][threadIdx.x];
+    d_w[(size_t)t * k + threadIdx.x] = s;
+  }
+}
+
+size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+int grid_for(size_t work, int per_block) {
+  const size_t b = (work + per_block - 1) / per_block;
+  const size_t cap = (size_t)(sm_count() > 0 ? sm_count() : 148) * 16;
+  return (int)(b < cap ? (b > 0 ? b : 1) : cap);
+}
+
+int check_rows_args(const char* fn, int T, int H, int k) {
+  if (T < 0 || H <= 0 || k <= 0) return fail(MOE_ERR_INVALID_ARG, "%s: need T>=0, H>0, k>0", fn);
+  if (H % 64 != 0 || k > kMaxTopK || (long long)T * k >= (1ll << 31))
+    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "%s: need H%%64==0, k<=32, T*k<2^31", fn);
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_dispatch_workspace_size(int T, int E, int k) {
+  (void)k;
+  if (T < 0 || E <= 0) return 0;
+  const size_t nchunk = (size_t)((T + kChunkTok - 1) / kChunkTok);
+  return align256(sizeof(int32_t) * (nchunk > 0 ? nchunk : 1) * E);
+}
+
+int moe_dispatch(const void* x, const int32_t* topk_idx, const int32_t* offsets, int T, int H,
+                 int E, int k, void* x_perm, int32_t* row_of_slot, int32_t* token_of_row,
+                 void* ws, size_t ws_bytes, void* stream) {
+  clear_error();
+  if (int rc = check_rows_args("moe_dispatch", T, H, k)) return rc;
+  if (E <= 0 || E > kMaxExperts || k > E)
+    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "moe_dispatch: need 1<=E<=1024, k<=E");
+  if (!topk_idx || !offsets || !row_of_slot || !token_of_row || !ws || (x_perm && !x))
+    return fail(MOE_ERR_INVALID_ARG, "moe_dispatch: NULL pointer argument");
+  if ((x && !aligned16(x)) || (x_perm && !aligned16(x_perm)) || !aligned16(ws))
+    return fail(MOE_ERR_ALIGNMENT, "moe_dispatch: x, x_perm and ws must be 16-byte aligned");
+  const size_t need = moe_dispatch_workspace_size(T, E, k);
+  if (ws_bytes < need)
+    return fail(MOE_ERR_WORKSPACE, "moe_dispatch: workspace %zu < %zu bytes", ws_bytes, need);
+  if (T == 0) return MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* status = status_word();
+  const int nchunk = (T + kChunkTok - 1) / kChunkTok;
+  int32_t* chunk_base = static_cast<int32_t*>(ws);
+  chunk_hist_kernel<<<(nchunk + 7) / 8, 256, sizeof(int) * 8 * E, s>>>(topk_idx, T, E, k, nchunk,
+                                                                       chunk_base, status);
+  if (int rc = check_launch("moe_dispatch: histogram kernel")) return rc;
+  chunk_scan_kernel<<<1, 1024, 0, s>>>(chunk_base, offsets, nchunk, E, status);
+  if (int rc = check_launch("moe_dispatch: scan kernel")) return rc;
+  dispatch_kernel<<<nchunk, 256, sizeof(int) * (E + kChunkTok * k), s>>>(
+      static_cast<const __nv_bfloat16*>(x), topk_idx, chunk_base, T, H, E, k,
+      static_cast<__nv_bfloat16*>(x_perm), row_of_slot, token_of_row, status);
+  return check_launch("moe_dispatch: row kernel");
+}
+
+int moe_combine(const void* y_perm, const float* topk_w, const int32_t* row_of_slot, int T, int H,
+                int k, void* y, void* stream) {
+  clear_error();
+  if (int rc = check_rows_args("moe_combine", T, H, k)) return rc;
+  if (!y_perm || !topk_w || !row_of_slot || !y)
+    return fail(MOE_ERR_INVALID_ARG, "moe_combine: NULL pointer argument");
+  if (!aligned16(y_perm) || !aligned16(y))
+    return fail(MOE_ERR_ALIGNMENT, "moe_combine: y_perm and y must be 16-byte aligned");
+  if (T == 0) return MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t work = (size_t)T * (H / 8);
+  gather_sum_kernel<true, false><<<grid_for(work, 256), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(y_perm), topk_w, row_of_slot, T, H, k, T * k, y,
+      status_word());
+  return check_launch("moe_combine");
+}
+
+int moe_dispatch_bwd(const void* dx_perm, const int32_t* row_of_slot, int T, int H, int k,
+                     float* dx_acc, void* stream) {
+  clear_error();
+  if (int rc = check_rows_args("moe_dispatch_bwd", T, H, k)) return rc;
+  if (!dx_perm || !row_of_slot || !dx_acc)
+    return fail(MOE_ERR_INVALID_ARG, "moe_dispatch_bwd: NULL pointer argument");
+  if (!aligned16(dx_perm) || !aligned16(dx_acc))
+    return fail(MOE_ERR_ALIGNMENT, "moe_dispatch_bwd: dx_perm and dx_acc must be 16-byte aligned");
+  if (T == 0) return MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t work = (size_t)T * (H / 8);
+  gather_sum_kernel<false, true><<<grid_for(work, 256), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(dx_perm), nullptr, row_of_slot, T, H, k, T * k, dx_acc,
+      status_word());
+  return check_launch("moe_dispatch_bwd");
+}
+
+int moe_combine_bwd(const void* dy, const void* y_perm, const float* topk_w,
+                    const int32_t* row_of_slot, int T, int H, int k, void* dy_perm, float* d_w,
+                    void* stream) {
+  clear_error();
+  if (int rc = check_rows_args("moe_combine_bwd", T, H, k)) return rc;
+  if (!dy || !y_perm || !topk_w || !row_of_slot || !dy_perm || !d_w)
+    return fail(MOE_ERR_INVALID_ARG, "moe_combine_bwd: NULL pointer argument");
+  if (!aligned16(dy) || !aligned16(y_perm) || !aligned16(dy_perm))
+    return fail(MOE_ERR_ALIGNMENT, "moe_combine_bwd: dy, y_perm and dy_perm must be 16-byte aligned");
+  if (T == 0) return MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  combine_bwd_kernel<<<T, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(dy),
+                                       static_cast<const __nv_bfloat16*>(y_perm), topk_w,
+                                       row_of_slot, T, H, k, T * k,
+                                       static_cast<__nv_bfloat16*>(dy_perm), d_w, status_word());
+  return check_launch("moe_combine_bwd");
+}
+
+}  // extern "C"

@@ -1,0 +1,101 @@
+"""Buffers and call order of one MoE expert layer over the C entry points.
+
+`MoELayer` owns the device tensors one layer needs for a fixed token count
+(outputs, activations kept for the backward pass, gradients, workspaces),
+allocated once through torch, and issues the library calls in order on one
+stream.  It adds no arithmetic of its own.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (moe_combine, moe_combine_bwd, moe_dispatch, moe_dispatch_bwd,
+               moe_dispatch_workspace_size, moe_grouped_gemm_down, moe_grouped_gemm_down_bwd,
+               moe_grouped_gemm_swiglu, moe_grouped_gemm_swiglu_bwd, moe_route_topk,
+               moe_route_topk_bwd, moe_route_topk_bwd_workspace_size,
+               moe_route_topk_workspace_size)
+
+
+def _ws(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(256, (nbytes + 255) // 256 * 256), dtype=torch.uint8, device=device)
+
+
+class MoELayer:
+    """One layer's buffers for T tokens of hidden size H, E experts of size I, top-k."""
+
+    def __init__(self, T: int, H: int, I: int, E: int, k: int, ep_size: int = 1, *,
+                 training: bool = True, device: str | torch.device = "cuda"):
+        self.T, self.H, self.I, self.E, self.k, self.ep_size = T, H, I, E, k, ep_size
+        self.R = R = T * k
+        self.training = training
+        dev = torch.device(device)
+        i32, f32, bf = torch.int32, torch.float32, torch.bfloat16
+        e = lambda *s, dt: torch.empty(*s, dtype=dt, device=dev)  # noqa: E731
+        self.topk_idx = e(T, k, dt=i32)
+        self.topk_w = e(T, k, dt=f32)
+        self.counts = e(E, dt=i32)
+        self.offsets = e(E + 1, dt=i32)
+        self.rank_offsets = e(ep_size + 1, dt=i32)
+        self.ws_route = _ws(moe_route_topk_workspace_size(T, H, E), dev)
+        self.ws_dispatch = _ws(moe_dispatch_workspace_size(T, E, k), dev)
+        self.x_perm = e(R, H, dt=bf)
+        self.row_of_slot = e(T, k, dt=i32)
+        self.token_of_row = e(R, dt=i32)
+        self.h = e(R, I, dt=bf)
+        self.gu = e(R, 2 * I, dt=bf) if training else None
+        self.y_perm = e(R, H, dt=bf)
+        self.y = e(T, H, dt=bf)
+        if training:
+            self.dy_perm = e(R, H, dt=bf)
+            self.d_w = e(T, k, dt=f32)
+            self.dgu = e(R, 2 * I, dt=bf)
+            self.dx_perm = e(R, H, dt=bf)
+            self.dx_acc = e(T, H, dt=f32)
+            self.dx = e(T, H, dt=bf)
+            self.dWg = e(E, I, H, dt=f32)
+            self.dWu = e(E, I, H, dt=f32)
+            self.dWd = e(E, H, I, dt=f32)
+            self.dWr = e(H, E, dt=f32)
+            self.ws_route_bwd = _ws(moe_route_topk_bwd_workspace_size(T, H, E), dev)
+
+    # ---------------------------------------------------------------- forward
+    def route(self, x, Wr, bias=None, stream=None):
+        moe_route_topk(x, Wr, bias, self.T, self.H, self.E, self.k, self.ep_size, self.topk_idx,
+                       self.topk_w, self.counts, self.offsets, self.rank_offsets, self.ws_route,
+                       stream)
+
+    def dispatch(self, x, stream=None):
+        moe_dispatch(x, self.topk_idx, self.offsets, self.T, self.H, self.E, self.k, self.x_perm,
+                     self.row_of_slot, self.token_of_row, self.ws_dispatch, stream)
+
+    def experts(self, Wg, Wu, Wd, stream=None):
+        moe_grouped_gemm_swiglu(self.x_perm, Wg, Wu, self.E, self.offsets, None, self.R, self.H,
+                                self.I, self.E, self.h, self.gu, None, stream)
+        moe_grouped_gemm_down(self.h, Wd, self.E, self.offsets, None, self.R, self.H, self.I,
+                              self.E, self.y_perm, None, stream)
+
+    def combine(self, stream=None):
+        moe_combine(self.y_perm, self.topk_w, self.row_of_slot, self.T, self.H, self.k, self.y,
+                    stream)
+
+    def forward(self, x, Wr, bias, Wg, Wu, Wd, stream=None):
+        self.route(x, Wr, bias, stream)
+        self.dispatch(x, stream)
+        self.experts(Wg, Wu, Wd, stream)
+        self.combine(stream)
+        return self.y
+
+    # --------------------------------------------------------------- backward
+    def backward(self, dy, x, Wr, Wg, Wu, Wd, accumulate: bool = False, stream=None):
+        assert self.training, "layer was built without backward buffers"
+        T, H, I, E, k, R = self.T, self.H, self.I, self.E, self.k, self.R
+        moe_combine_bwd(dy, self.y_perm, self.topk_w, self.row_of_slot, T, H, k, self.dy_perm,
+                        self.d_w, stream)
+        moe_grouped_gemm_down_bwd(self.dy_perm, self.h, self.gu, Wd, E, self.offsets, None, R, H, I,
+                                  E, self.dgu, self.dWd, accumulate, None, stream)
+        moe_grouped_gemm_swiglu_bwd(self.dgu, self.x_perm, Wg, Wu, E, self.offsets, None, R, H, I, E,
+                                    self.dx_perm, self.dWg, self.dWu, accumulate, None, stream)
+        moe_dispatch_bwd(self.dx_perm, self.row_of_slot, T, H, k, self.dx_acc, stream)
+        moe_route_topk_bwd(self.d_w, self.topk_w, self.topk_idx, x, Wr, self.dx_acc, T, H, E, k,
+                           self.dWr, self.dx, accumulate, self.ws_route_bwd, stream)
+        return self.dx

@@ -1,0 +1,97 @@
+"""The C-ABI library loads and exports what include/moe_topk.h declares, and
+rejects bad arguments on the host before any launch (no GPU needed)."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+import moe_expert_layer_topk_gb300 as m
+from moe_expert_layer_topk_gb300 import build as b
+
+HEADER = Path(__file__).resolve().parents[1] / "include" / "moe_topk.h"
+DECL = re.compile(r"^(?:int|size_t|const char\*)\s+(moe_\w+)\s*\(([^;]*)\);", re.M | re.S)
+
+OK, INVALID, SHAPE, ALIGN, WS = 0, -1, -2, -3, -4
+
+
+@pytest.fixture(scope="module")
+def L():
+    b.build()
+    return m.lib()
+
+
+def header_decls():
+    return {name: args for name, args in DECL.findall(HEADER.read_text())}
+
+
+def test_header_symbols_exported(L):
+    decls = header_decls()
+    assert len(decls) >= 16
+    for name in decls:
+        assert hasattr(L, name), name
+
+
+def test_binding_matches_header(L):
+    decls = header_decls()
+    assert set(decls) == set(m.ENTRY_POINTS), set(decls) ^ set(m.ENTRY_POINTS)
+    for name, args in decls.items():
+        n = 0 if args.strip() in ("", "void") else args.count(",") + 1
+        assert len(m.ENTRY_POINTS[name][0]) == n, name
+
+
+def test_workspace_queries(L):
+    assert m.moe_route_topk_workspace_size(4096, 2048, 128) >= 4096 * 128 * 4
+    assert m.moe_dispatch_workspace_size(4096, 128, 8) >= (4096 // 32) * 128 * 4
+    assert m.moe_route_topk_bwd_workspace_size(8192, 2048, 128) > 0
+    assert m.moe_route_topk_workspace_size(-1, 2048, 128) == 0
+
+
+def _err(L):
+    return L.moe_last_error_string().decode()
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails host validation first
+
+
+def test_route_rejects_bad_shapes(L):
+    P = FAKE
+    assert L.moe_route_topk(P, P, None, 16, 128, 8, 9, 1, P, P, P, P, P, P, 1 << 20, None) == SHAPE
+    assert "k<=" in _err(L)
+    assert L.moe_route_topk(P, P, None, 16, 100, 8, 2, 1, P, P, P, P, P, P, 1 << 20, None) == SHAPE
+    assert L.moe_route_topk(P, P, None, 16, 128, 8, 2, 3, P, P, P, P, P, P, 1 << 20, None) == INVALID
+    assert L.moe_route_topk(P, None, None, 16, 128, 8, 2, 1, P, P, P, P, P, P, 1 << 20, None) == INVALID
+    assert L.moe_route_topk(P + 2, P, None, 16, 128, 8, 2, 1, P, P, P, P, P, P, 1 << 20, None) == ALIGN
+    assert L.moe_route_topk(P, P, None, 4096, 128, 8, 2, 1, P, P, P, P, P, P, 64, None) == WS
+    assert "workspace" in _err(L)
+
+
+def test_grouped_gemm_rejects_bad_shapes(L):
+    P = FAKE
+    assert L.moe_grouped_gemm_swiglu(P, P, P, 8, P, None, 64, 100, 64, 8, P, None, None, 0, None) == SHAPE
+    assert L.moe_grouped_gemm_swiglu(P, P, P, 2000, P, None, 64, 128, 64, 8, P, None, None, 0, None) == SHAPE
+    assert L.moe_grouped_gemm_swiglu(P, P, P, 8, None, None, 64, 128, 64, 8, P, None, None, 0, None) == INVALID
+    assert L.moe_grouped_gemm_down(P, P + 8, 8, P, None, 64, 128, 64, 8, P, None, 0, None) == ALIGN
+    assert L.moe_grouped_gemm_down_bwd(P, P, None, P, 8, P, None, 64, 128, 64, 8, P, P, 0, None, 0,
+                                       None) == INVALID
+    assert L.moe_grouped_gemm_swiglu_bwd(P, P, P, P, 8, P, None, 64, 128, 96, 8, P, P, P, 0, None, 0,
+                                         None) == SHAPE
+
+
+def test_rows_ops_reject_bad_args(L):
+    P = FAKE
+    assert L.moe_combine(P, P, P, 16, 128, 33, P, None) == SHAPE
+    assert L.moe_combine(P, P, P, 16, 128, 2, None, None) == INVALID
+    assert L.moe_dispatch(P, P, P, 16, 128, 8, 2, P, P, P, P, 0, None) == WS
+    assert L.moe_dispatch_bwd(P + 4, P, 16, 128, 2, P, None) == ALIGN
+    assert L.moe_combine_bwd(P, P, P, P, -1, 128, 2, P, P, None) == INVALID
+    assert L.moe_route_topk_bwd(P, P, P, P, P, P, 16, 128, 8, 2, P, P, 0, P, 16, None) == WS
+
+
+def test_zero_tokens_is_a_no_op(L):
+    # T == 0: nothing to do, no launch, OK
+    P = FAKE
+    assert L.moe_combine(P, P, P, 0, 128, 2, P, None) == OK
+    assert L.moe_dispatch_bwd(P, P, 0, 128, 2, P, None) == OK
+    assert L.moe_grouped_gemm_swiglu(P, P, P, 8, P, None, 0, 128, 64, 8, P, None, None, 0, None) == OK
+    assert L.moe_grouped_gemm_down(P, P, 0, None, None, 64, 128, 64, 8, P, None, 0, None) == OK
