@@ -1,0 +1,402 @@
+"""Benchmark of the MoE expert layer on GB300 (prints one JSON line).
+
+A step is one pass of the whole hot path over one batch: router top-k,
+dispatch, grouped gate/up GEMM + SwiGLU, grouped down GEMM, combine, and the
+backward of all of them (dX, dW_gate, dW_up, dW_down, d router W), at the
+Qwen3-30B-A3B-shaped workload T=8192 tokens, hidden 2048, intermediate 768,
+128 experts, top-8 (seeded synthetic inputs, random weights).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain single-threaded C
+restatement used by the tests) on a bounded sample of the same workload;
+it is a deliberately slow baseline, not a tuned competitor.
+
+With N > 1 (torchrun, one rank per GPU) every rank runs an independent
+replica of the step (the layer has no data-path exchange on one node's
+replicas), ranks are barrier-synchronised around the timed region, and the
+slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "MoE layer tokens/s fwd & fwd+bwd on 1 GB300; grouped-GEMM TFLOP/s vs bf16 peak"
+WORKLOAD = "qwen3_30b_fwd_bwd"
+FWD_WORKLOAD = "qwen3_30b_fwd"
+
+
+def peaks():
+    try:
+        return json.loads((ROOT / "MEASURED_PEAKS.json").read_text()), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def layer_flops(T, H, I, E, k):
+    """Algorithmic flops (2 per multiply-add) of one layer pass."""
+    R = T * k
+    fwd = {"router": 2.0 * T * H * E, "gate_up": 2.0 * R * H * 2 * I, "down": 2.0 * R * I * H}
+    bwd = {"down_bwd": 2 * fwd["down"], "gate_up_bwd": 2 * fwd["gate_up"], "router_bwd": 2 * fwd["router"]}
+    return fwd, bwd
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.f = None
+
+    def __enter__(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.f is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.f.flush()
+        rows = []
+        for line in Path(self.f.name).read_text().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        try:
+            os.unlink(self.f.name)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1])]
+        mx = [num(r[2]) for r in rows if num(r[2])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+# --------------------------------------------------------------- multi-rank
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if os.environ.get("BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend=backend)
+        return dist, dist.get_rank(), world, int(os.environ.get("LOCAL_RANK", "0"))
+    return None, 0, 1, 0
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """Largest `value` over all ranks (the slowest replica defines the time)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# -------------------------------------------------------------- CPU oracle
+
+def oracle_sample_step(inp, T_s):
+    """Oracle forward+backward over the first T_s tokens of the workload."""
+    import numpy as np
+
+    import oracle
+    from moe_expert_layer_topk_gb300.synth import bf16_bits
+    x = bf16_bits(inp["x"][:T_s])
+    Wr = inp["Wr"].numpy()
+    Wg, Wu, Wd = (bf16_bits(inp[n]) for n in ("Wg", "Wu", "Wd"))
+    k, E = inp["k"], inp["E"]
+    rt = oracle.route_topk(x, Wr, None, k, inp["ep_size"])
+    dp = oracle.dispatch(x, rt["topk_idx"], rt["offsets"], E)
+    xp = oracle.widen_bf16(dp["x_perm"])
+    h, gu = oracle.grouped_gemm_swiglu(xp, Wg, Wu, rt["offsets"], save_gu=True)
+    yp = oracle.grouped_gemm_down(h, Wd, rt["offsets"])
+    oracle.combine(yp, rt["topk_w"], dp["row_of_slot"])
+    dy = oracle.widen_bf16(bf16_bits(inp["dy"][:T_s]))
+    dyp, dw = oracle.combine_bwd(dy, yp, rt["topk_w"], dp["row_of_slot"])
+    dgu, _ = oracle.grouped_gemm_down_bwd(dyp, h, gu, Wd, rt["offsets"])
+    dxp, _, _ = oracle.grouped_gemm_swiglu_bwd(dgu, xp, Wg, Wu, rt["offsets"])
+    dxa = oracle.dispatch_bwd(dxp, dp["row_of_slot"])
+    oracle.route_topk_bwd(dw, rt["topk_w"], rt["topk_idx"], x, Wr, dxa)
+    return np.int64(T_s)
+
+
+def cpu_cores_used():
+    return 1  # the oracle is single-threaded C
+
+
+def run_reference(args, shape, inp):
+    dist, rank, world, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    T_s = args.ref_tokens
+    for _ in range(args.warmup):
+        oracle_sample_step(inp, T_s)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample_step(inp, T_s)
+    dt = time.perf_counter() - t0
+    value = T_s * args.steps / dt
+    sample = f"first {T_s} tokens of {WORKLOAD} (T={shape.T}) per step, forward+backward, full weights"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded normal inputs, random-init weights)",
+            "config": {"workload": WORKLOAD, "T": shape.T, "H": shape.H, "I": shape.I, "E": shape.E,
+                       "k": shape.k, "sample_tokens_per_step": T_s},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores_used(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_ours(args, shape, inp):
+    import torch
+
+    import moe_expert_layer_topk_gb300 as m
+    dist, rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    g = {n: (v.to(dev) if isinstance(v, torch.Tensor) else v) for n, v in inp.items()}
+    layer = m.MoELayer(T, H, I, E, k, shape.ep_size, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # per-call events: (name, start, end) recorded on the launching stream
+    names = ["route", "dispatch", "gate_up", "down", "combine", "combine_bwd", "down_bwd",
+             "gate_up_bwd", "dispatch_bwd", "route_bwd"]
+
+    def step(ev=None):
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        R = layer.R
+        mark(0)
+        layer.route(g["x"], g["Wr"], g["bias"]); mark(1)
+        layer.dispatch(g["x"]); mark(2)
+        m.moe_grouped_gemm_swiglu(layer.x_perm, g["Wg"], g["Wu"], E, layer.offsets, None, R, H, I, E,
+                                  layer.h, layer.gu); mark(3)
+        m.moe_grouped_gemm_down(layer.h, g["Wd"], E, layer.offsets, None, R, H, I, E, layer.y_perm); mark(4)
+        layer.combine(); mark(5)
+        m.moe_combine_bwd(g["dy"], layer.y_perm, layer.topk_w, layer.row_of_slot, T, H, k, layer.dy_perm,
+                          layer.d_w); mark(6)
+        m.moe_grouped_gemm_down_bwd(layer.dy_perm, layer.h, layer.gu, g["Wd"], E, layer.offsets, None, R, H,
+                                    I, E, layer.dgu, layer.dWd); mark(7)
+        m.moe_grouped_gemm_swiglu_bwd(layer.dgu, layer.x_perm, g["Wg"], g["Wu"], E, layer.offsets, None, R,
+                                      H, I, E, layer.dx_perm, layer.dWg, layer.dWu); mark(8)
+        m.moe_dispatch_bwd(layer.dx_perm, layer.row_of_slot, T, H, k, layer.dx_acc); mark(9)
+        m.moe_route_topk_bwd(layer.d_w, layer.topk_w, layer.topk_idx, g["x"], g["Wr"], layer.dx_acc, T, H,
+                             E, k, layer.dWr, layer.dx, 0, layer.ws_route_bwd); mark(10)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if m.moe_read_device_status(reset=True) != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(11)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    ms_local = t_start.elapsed_time(t_end)
+    ms = max_over_ranks(ms_local, dist, dev)
+    per_call = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
+                for j, n in enumerate(names)}
+
+    # forward-only throughput at T=4096 (the forward workload)
+    from moe_expert_layer_topk_gb300.synth import CONFIGS, make_layer_inputs
+    fshape = CONFIGS[FWD_WORKLOAD]
+    fin = make_layer_inputs(fshape, 0)
+    fg = {n: (v.to(dev) if isinstance(v, torch.Tensor) else v) for n, v in fin.items()}
+    flayer = m.MoELayer(fshape.T, fshape.H, fshape.I, fshape.E, fshape.k, fshape.ep_size,
+                        training=False, device=dev)
+    for _ in range(args.warmup):
+        flayer.forward(fg["x"], fg["Wr"], fg["bias"], fg["Wg"], fg["Wu"], fg["Wd"])
+    fs, fe = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    fs.record(stream)
+    for _ in range(args.steps):
+        flayer.forward(fg["x"], fg["Wr"], fg["bias"], fg["Wg"], fg["Wu"], fg["Wd"])
+    fe.record(stream)
+    torch.cuda.synchronize(dev)
+    fwd_ms = fs.elapsed_time(fe) / args.steps
+    del flayer, fg
+
+    # end to end through the public API with host buffers: x and dY come from
+    # pinned host memory, y and dX go back, every step
+    hx = inp["x"].pin_memory()
+    hdy = inp["dy"].pin_memory()
+    hy = torch.empty_like(inp["x"]).pin_memory()
+    hdx = torch.empty_like(inp["x"]).pin_memory()
+    dx_in = torch.empty_like(g["x"])
+    ddy_in = torch.empty_like(g["dy"])
+
+    def e2e_step():
+        dx_in.copy_(hx, non_blocking=True)
+        ddy_in.copy_(hdy, non_blocking=True)
+        layer.forward(dx_in, g["Wr"], g["bias"], g["Wg"], g["Wu"], g["Wd"])
+        layer.backward(ddy_in, dx_in, g["Wr"], g["Wg"], g["Wu"], g["Wd"])
+        hy.copy_(layer.y, non_blocking=True)
+        hdx.copy_(layer.dx, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    es.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    ee.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(es.elapsed_time(ee), dist, dev) / args.steps
+    if m.moe_read_device_status(reset=True) != 0:
+        raise RuntimeError("device status word set during the timed region")
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    pk, pk_kind = peaks()
+    fwd_fl, bwd_fl = layer_flops(T, H, I, E, k)
+    gemm_fl = {"gate_up": fwd_fl["gate_up"], "down": fwd_fl["down"], "down_bwd": bwd_fl["down_bwd"],
+               "gate_up_bwd": bwd_fl["gate_up_bwd"]}
+    gemm_ms = sum(per_call[n] for n in gemm_fl)
+    gemm_tflops = sum(gemm_fl.values()) / (gemm_ms * 1e-3) / 1e12
+    # dominant single-kernel call: the forward gate/up GEMM is one launch
+    dom = "gate_up"
+    dom_tflops = gemm_fl[dom] / (per_call[dom] * 1e-3) / 1e12
+    step_ms = ms / args.steps
+    value = world * T / (step_ms * 1e-3)
+    prof = ROOT / "profiles" / "traffic.json"
+    traffic = None
+    if prof.exists():
+        try:
+            traffic = json.loads(prof.read_text()).get("grouped_gemm_gate_up_fwd_T4096x8_bytes_per_launch")
+        except Exception:
+            traffic = None
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normal inputs, random-init weights)",
+        "config": {"workload": WORKLOAD, "T": T, "H": H, "I": I, "E": E, "k": k,
+                   "step": "forward+backward (router, dispatch, gate/up+SwiGLU, down, combine and their backward)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (1.2 GB of expert weights per step)"},
+        "fwd_tokens_per_s": fshape.T / (fwd_ms * 1e-3),
+        "fwd_ms": fwd_ms, "fwd_config": {"workload": FWD_WORKLOAD, "T": fshape.T},
+        "grouped_gemm_tflops": gemm_tflops,
+        "per_call_ms": per_call,
+        "roofline": {"bound": "tensor", "kernel": "grouped_gemm gate/up + SwiGLU (forward)",
+                     "achieved": dom_tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": dom_tflops / pk["bf16_tflops"], "peak_source": f"{pk_kind} bf16 burst",
+                     "traffic": traffic},
+        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(hx.numel() * 2 + hdy.numel() * 2),
+                "d2h_bytes_per_step": int(hy.numel() * 2 + hdx.numel() * 2)},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clk.summary(),
+    }
+    if args.cpu_baseline:
+        t0 = time.perf_counter()
+        oracle_sample_step(inp, args.cpu_tokens)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": args.cpu_tokens / dt, "unit": "tokens/s", "cores": cpu_cores_used(),
+                                "kind": "oracle",
+                                "sample": f"first {args.cpu_tokens} tokens of {WORKLOAD}, forward+backward, "
+                                          f"single-threaded C oracle, {dt:.1f} s"}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# kernels launched per step by the calls in run_ours.step():
+# route 3, dispatch 3, gate/up 1, down 1, combine 1, combine_bwd 1,
+# down_bwd 2, gate/up bwd 2, dispatch_bwd 1, route_bwd 6
+KERNELS_PER_STEP = 3 + 3 + 1 + 1 + 1 + 1 + 2 + 2 + 1 + 6
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--ref-tokens", type=int, default=8, help="oracle tokens per reference step")
+    ap.add_argument("--cpu-tokens", type=int, default=48, help="oracle tokens for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from moe_expert_layer_topk_gb300.synth import CONFIGS, make_layer_inputs
+    shape = CONFIGS[WORKLOAD]
+    inp = make_layer_inputs(shape, 0)
+    if args.impl == "reference":
+        run_reference(args, shape, inp)
+    else:
+        run_ours(args, shape, inp)
+
+
+if __name__ == "__main__":
+    main()
