@@ -455,11 +455,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         uint8_t* sA = smem + (size_t)stage * STAGE_BYTES;
         uint8_t* sB = sA + A_BYTES;
+        int nkk = BK / 16;
         if (KIND == DW && valid < BK) {
-          // rows past the segment end belong to another group: zero them in
-          // both operands (each K row is one 128-byte line of every chunk)
+          // Rows past the segment end belong to another group.  Only the
+          // 16-row MMA steps that hold valid rows are issued; inside the last
+          // of them the rows [valid, 16*nkk) are zeroed in both operands
+          // (each K row is one 128-byte line of every 64-wide chunk).
+          nkk = (valid + 15) / 16;
           const int a_chunks = 2, b_chunks = p.BN / 64;
-          const int nrows = BK - valid;
+          const int nrows = nkk * 16 - valid;
           const int units = (a_chunks + b_chunks) * nrows * 8;
           for (int u = lane; u < units; u += 32) {
             const int chunk = u / (nrows * 8);
@@ -469,7 +473,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                              : sB + (chunk - a_chunks) * CHUNK_BYTES;
             *reinterpret_cast<uint4*>(base + r * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
           }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          if (nrows > 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
         }
         tc_fence_after();
@@ -477,6 +481,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
+            if (kk >= nkk) break;
             const uint64_t ad = Traits<KIND>::a_mn ? sdesc(a0 + kk * 2048, CHUNK_BYTES, 1024)
                                                    : sdesc(a0 + kk * 32, 16, 1024);
             const uint64_t bd = Traits<KIND>::b_mn ? sdesc(b0 + kk * 2048, CHUNK_BYTES, 1024)
@@ -514,6 +519,23 @@ __global__ void __launch_bounds__(THREADS, 1)
       const Tile t = decode_tile<KIND>(tile, p, ctl);
       const int buf = local & 1;
       const uint32_t use = (uint32_t)(local >> 1);
+      // SwiGLU backward: the saved g, u of this thread's row do not depend on
+      // the accumulator, so the first chunk is requested before waiting.
+      uint4 gpre[4], upre[4];
+      const int r2 = t.m0 + row_in_tile;
+      const bool valid2 = (KIND == DOWN_BWD_DX) && r2 < t.row_end;
+      const __nv_bfloat16* grow =
+          static_cast<const __nv_bfloat16*>(p.aux) + (size_t)r2 * 2 * p.I + t.n0;
+      auto prefetch_gu = [&](int c) {
+        if (valid2) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            gpre[i] = __ldg(reinterpret_cast<const uint4*>(grow + c) + i);
+            upre[i] = __ldg(reinterpret_cast<const uint4*>(grow + p.I + c) + i);
+          }
+        }
+      };
+      if constexpr (KIND == DOWN_BWD_DX) prefetch_gu(0);
       if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&ctl->tfull[buf]), use & 1u, ctl, p.status))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * ACC_COLS);
@@ -584,22 +606,26 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       } else if constexpr (KIND == DOWN_BWD_DX) {
-        const int r = t.m0 + row_in_tile;
-        const bool valid = r < t.row_end;
-        const __nv_bfloat16* gu = static_cast<const __nv_bfloat16*>(p.aux);
+        const int r = r2;
+        const bool valid = valid2;
         __nv_bfloat16* dgu = static_cast<__nv_bfloat16*>(p.out0);
         for (int c = 0; c < p.BN; c += 32) {
           uint32_t a[32];
           tmem_ld32(taddr + c, a);
+          uint4 gcur[4], ucur[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            gcur[i] = gpre[i];
+            ucur[i] = upre[i];
+          }
+          if (c + 32 < p.BN) prefetch_gu(c + 32);
           tmem_wait_ld();
           if (valid) {
-            const uint4* gsrc = reinterpret_cast<const uint4*>(gu + (size_t)r * 2 * p.I + t.n0 + c);
-            const uint4* usrc = reinterpret_cast<const uint4*>(gu + (size_t)r * 2 * p.I + p.I + t.n0 + c);
             uint4* gdst = reinterpret_cast<uint4*>(dgu + (size_t)r * 2 * p.I + t.n0 + c);
             uint4* udst = reinterpret_cast<uint4*>(dgu + (size_t)r * 2 * p.I + p.I + t.n0 + c);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const uint4 gv = __ldg(gsrc + i), uv = __ldg(usrc + i);
+              const uint4 gv = gcur[i], uv = ucur[i];
               const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
               const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
               uint32_t og[4], ou[4];

@@ -46,18 +46,30 @@ __global__ void __launch_bounds__(256) chunk_hist_kernel(const int32_t* __restri
 }
 
 // chunk_base[c][e] <- offsets[e] + sum_{c' < c} hist[c'][e]  (in place).
-__global__ void __launch_bounds__(1024) chunk_scan_kernel(int32_t* __restrict__ chunk_base,
-                                                          const int32_t* __restrict__ offsets,
-                                                          int nchunk, int E, int* status) {
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = offsets[e];
-    for (int c = 0; c < nchunk; ++c) {
-      const int v = chunk_base[(size_t)c * E + e];
-      chunk_base[(size_t)c * E + e] = run;
-      run += v;
-    }
-    if (run != offsets[e + 1]) set_status(status, MOE_STATUS_COUNT_MISMATCH);
+// One warp per expert: lane l owns a contiguous run of chunks; a warp scan of
+// the per-lane sums gives each lane its starting row.
+__global__ void __launch_bounds__(256) chunk_scan_kernel(int32_t* __restrict__ chunk_base,
+                                                         const int32_t* __restrict__ offsets,
+                                                         int nchunk, int E, int* status) {
+  const int e = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (e >= E) return;
+  const int per = (nchunk + 31) / 32;
+  const int c0 = min(nchunk, lane * per), c1 = min(nchunk, c0 + per);
+  int local = 0;
+  for (int c = c0; c < c1; ++c) local += chunk_base[(size_t)c * E + e];
+  int incl = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
   }
+  int run = offsets[e] + incl - local;
+  for (int c = c0; c < c1; ++c) {
+    const int v = chunk_base[(size_t)c * E + e];
+    chunk_base[(size_t)c * E + e] = run;
+    run += v;
+  }
+  if (lane == 31 && run != offsets[e + 1]) set_status(status, MOE_STATUS_COUNT_MISMATCH);
 }
 
 // ------------------------------------------------------- rank and row copy
@@ -323,7 +335,7 @@ int moe_dispatch(const void* x, const int32_t* topk_idx, const int32_t* offsets,
   chunk_hist_kernel<<<(nchunk + 7) / 8, 256, sizeof(int) * 8 * E, s>>>(topk_idx, T, E, k, nchunk,
                                                                        chunk_base, status);
   if (int rc = check_launch("moe_dispatch: histogram kernel")) return rc;
-  chunk_scan_kernel<<<1, 1024, 0, s>>>(chunk_base, offsets, nchunk, E, status);
+  chunk_scan_kernel<<<(E + 7) / 8, 256, 0, s>>>(chunk_base, offsets, nchunk, E, status);
   if (int rc = check_launch("moe_dispatch: scan kernel")) return rc;
   dispatch_kernel<<<nchunk, 256, sizeof(int) * (E + kChunkTok * k), s>>>(
       static_cast<const __nv_bfloat16*>(x), topk_idx, chunk_base, T, H, E, k,

@@ -16,157 +16,165 @@ namespace {
 
 // ------------------------------------------------------------ logits kernel
 //
-// CTA = 8 warps over 16 tokens x 128 experts.  Warp w sums h-block (sb + w)
-// of 256 consecutive h for all 16x128 outputs (each lane: 8 tokens x 8
-// experts, one fused multiply-add chain per output in increasing h).  The
-// eight block partials then meet in shared memory, where one thread per
-// output adds them left to right into its running sum; the bias comes last.
-constexpr int kLogitTok = 16;
-constexpr int kLogitExp = 128;
-constexpr int kLogitWarps = 8;
-constexpr int kLogitBlockH = 256;
-constexpr size_t kLogitSmem = sizeof(float) * kLogitWarps * kLogitTok * kLogitExp;  // 64 KiB
-
-__device__ __forceinline__ float bf16_elem(const uint4& v, int i) {
-  const uint32_t w = (i >> 1) == 0 ? v.x : (i >> 1) == 1 ? v.y : (i >> 1) == 2 ? v.z : v.w;
-  return (i & 1) ? bf16hi(w) : bf16lo(w);
-}
+// CTA = 4 warps over 32 tokens x 64 experts; thread = 4 tokens x 4 experts.
+// h advances in stages of 32 positions staged through shared memory (x
+// widened to fp32 once per CTA, both operands double-buffered through
+// registers).  Each thread keeps, per output, the running fused
+// multiply-add chain of the current 256-wide h-block and the running sum of
+// the finished blocks: exactly the order of the reading (block partials in
+// increasing h from 0, block sums added left to right, bias last).
+constexpr int kLogitTok = 32;
+constexpr int kLogitExp = 64;
+constexpr int kLogitThreads = 128;
+constexpr int kLogitStage = 32;   // h per stage
+constexpr int kLogitBlockH = 256; // h per summation block
 
 template <bool kVec>
-__global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16* __restrict__ x,
-                                                            const float* __restrict__ Wr,
-                                                            const float* __restrict__ bias, int T,
-                                                            int H, int E,
-                                                            float* __restrict__ logits) {
-  extern __shared__ float part[];  // [warp][token][expert]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tg = lane >> 4, eg = lane & 15;
-  const int t0 = blockIdx.x * kLogitTok;
-  const int e0 = blockIdx.y * kLogitExp;
-  const int my_e = e0 + eg * 8;
-  const int nblk = (H + kLogitBlockH - 1) / kLogitBlockH;
+__global__ void __launch_bounds__(kLogitThreads) router_logits_kernel(
+    const __nv_bfloat16* __restrict__ x, const float* __restrict__ Wr, const float* __restrict__ bias,
+    int T, int H, int E, float* __restrict__ logits) {
+  __shared__ __align__(16) float xs[2][kLogitStage][kLogitTok];
+  __shared__ __align__(16) float ws[2][kLogitStage][kLogitExp];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tg = lane & 7, eg = lane >> 3;
+  const int t0 = blockIdx.x * kLogitTok, e0 = blockIdx.y * kLogitExp;
+  const int my_tok = tg * 4, my_exp = warp * 16 + eg * 4;
 
-  float run[8];
+  // global -> register staging of one stage
+  float4 wreg[4];
+  uint4 xreg;
+  auto load_stage = [&](int h0) {
 #pragma unroll
-  for (int o = 0; o < 8; ++o) run[o] = 0.f;
-
-  for (int sb = 0; sb < nblk; sb += kLogitWarps) {
-    const int blk = sb + warp;
-    float acc[8][8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-    if (blk < nblk) {
-      const int h0 = blk * kLogitBlockH;
-      const int h1 = min(H, h0 + kLogitBlockH);
-      for (int h = h0; h < h1; h += 8) {
-        uint4 xv[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int t = t0 + tg * 8 + i;
-          xv[i] = (t < T) ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H + h))
-                          : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int hh = 0; hh < 8; ++hh) {
-          float w[8];
-          const float* wrow = Wr + (size_t)(h + hh) * E;
-          if (kVec) {
-            if (my_e < E) {
-              const float4 a = __ldg(reinterpret_cast<const float4*>(wrow + my_e));
-              const float4 b = __ldg(reinterpret_cast<const float4*>(wrow + my_e + 4));
-              w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-              w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
-            } else {
-#pragma unroll
-              for (int j = 0; j < 8; ++j) w[j] = 0.f;
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) w[j] = (my_e + j < E) ? __ldg(wrow + my_e + j) : 0.f;
-          }
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float xf = bf16_elem(xv[i], hh);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[i][j] = __fmaf_rn(xf, w[j], acc[i][j]);
-          }
-        }
+    for (int i = 0; i < 4; ++i) {
+      const int idx = tid + i * kLogitThreads;  // 0..511
+      const int row = idx >> 4, c4 = (idx & 15) * 4;
+      const int e = e0 + c4;
+      const float* src = Wr + (size_t)(h0 + row) * E + e;
+      if (kVec) {
+        wreg[i] = (e < E) ? __ldg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        wreg[i].x = (e + 0 < E) ? __ldg(src + 0) : 0.f;
+        wreg[i].y = (e + 1 < E) ? __ldg(src + 1) : 0.f;
+        wreg[i].z = (e + 2 < E) ? __ldg(src + 2) : 0.f;
+        wreg[i].w = (e + 3 < E) ? __ldg(src + 3) : 0.f;
       }
     }
+    const int tok = tid >> 2, h8 = (tid & 3) * 8;
+    const int t = t0 + tok;
+    xreg = (t < T) ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H + h0 + h8))
+                   : make_uint4(0, 0, 0, 0);
+  };
+  auto store_stage = [&](int buf) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float4* dst = reinterpret_cast<float4*>(
-          part + ((size_t)(warp * kLogitTok + tg * 8 + i) * kLogitExp + eg * 8));
-      dst[0] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-      dst[1] = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+    for (int i = 0; i < 4; ++i) {
+      const int idx = tid + i * kLogitThreads;
+      *reinterpret_cast<float4*>(&ws[buf][idx >> 4][(idx & 15) * 4]) = wreg[i];
     }
-    __syncthreads();
+    const int tok = tid >> 2, h8 = (tid & 3) * 8;
+    const uint32_t w4[4] = {xreg.x, xreg.y, xreg.z, xreg.w};
 #pragma unroll
-    for (int o = 0; o < 8; ++o) {
-      const int idx = threadIdx.x + o * 256;
-      const int tok = idx / kLogitExp, ex = idx % kLogitExp;
+    for (int i = 0; i < 4; ++i) {
+      xs[buf][h8 + 2 * i][tok] = bf16lo(w4[i]);
+      xs[buf][h8 + 2 * i + 1][tok] = bf16hi(w4[i]);
+    }
+  };
+
+  float p[4][4], run[4][4];
 #pragma unroll
-      for (int w = 0; w < kLogitWarps; ++w) {
-        const int b = sb + w;
-        if (b < nblk) {
-          const float p = part[(size_t)(w * kLogitTok + tok) * kLogitExp + ex];
-          run[o] = (b == 0) ? p : __fadd_rn(run[o], p);
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      p[i][j] = 0.f;
+      run[i][j] = 0.f;
+    }
+  const int nstage = H / kLogitStage;
+  load_stage(0);
+  store_stage(0);
+  __syncthreads();
+  for (int st = 0; st < nstage; ++st) {
+    const int buf = st & 1;
+    if (st + 1 < nstage) load_stage((st + 1) * kLogitStage);
+#pragma unroll 8
+    for (int hh = 0; hh < kLogitStage; ++hh) {
+      const float4 xv = *reinterpret_cast<const float4*>(&xs[buf][hh][my_tok]);
+      const float4 wv = *reinterpret_cast<const float4*>(&ws[buf][hh][my_exp]);
+      const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
+      const float wa[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) p[i][j] = __fmaf_rn(xa[i], wa[j], p[i][j]);
+    }
+    const int h_end = (st + 1) * kLogitStage;
+    if (h_end % kLogitBlockH == 0 || h_end == H) {
+      const bool first = h_end <= kLogitBlockH;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          run[i][j] = first ? p[i][j] : __fadd_rn(run[i][j], p[i][j]);
+          p[i][j] = 0.f;
         }
-      }
     }
-    __syncthreads();
+    if (st + 1 < nstage) {
+      store_stage(buf ^ 1);
+      __syncthreads();
+    }
   }
 #pragma unroll
-  for (int o = 0; o < 8; ++o) {
-    const int idx = threadIdx.x + o * 256;
-    const int t = t0 + idx / kLogitExp, e = e0 + idx % kLogitExp;
-    if (t < T && e < E) logits[(size_t)t * E + e] = bias ? __fadd_rn(run[o], bias[e]) : run[o];
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + my_tok + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + my_exp + j;
+      if (e < E) logits[(size_t)t * E + e] = bias ? __fadd_rn(run[i][j], __ldg(bias + e)) : run[i][j];
+    }
   }
 }
 
 // -------------------------------------------------------------- top-k kernel
 //
 // One warp per token: the token's logits sit in registers (lane l holds
-// experts l, l+32, ...); k rounds of a warp-wide arg-max over
-// (logit descending, id ascending) pick the slots in order.
+// experts l, l+32, ...; kNQ registers per lane); k rounds of a warp-wide
+// arg-max over (logit descending, id ascending) pick the slots in order.
+// Slot counts go to counts[] with integer atomics (order-independent).
 constexpr int kTopkWarps = 8;
-constexpr int kTopkTokPerWarp = 8;
+constexpr int kTopkTokPerWarp = 2;
 constexpr int kTopkTokPerBlock = kTopkWarps * kTopkTokPerWarp;
 
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
+template <int kNQ>
 __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ logits, int T,
                                                           int E, int k, int32_t* __restrict__ topk_idx,
                                                           float* __restrict__ topk_w,
-                                                          int32_t* __restrict__ blk_hist) {
-  __shared__ int hist[kMaxExperts];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
-  __syncthreads();
+                                                          int32_t* __restrict__ counts) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nq = (E + 31) / 32;
   for (int it = 0; it < kTopkTokPerWarp; ++it) {
     const int t = blockIdx.x * kTopkTokPerBlock + warp * kTopkTokPerWarp + it;
     if (t >= T) break;
-    float v[32];
+    float v[kNQ];
 #pragma unroll
-    for (int q = 0; q < 32; ++q) {
+    for (int q = 0; q < kNQ; ++q) {
       const int e = lane + 32 * q;
-      v[q] = (q < nq && e < E) ? logits[(size_t)t * E + e] : -FLT_MAX;
+      v[q] = (e < E) ? __ldg(logits + (size_t)t * E + e) : 0.f;
     }
     uint32_t taken = 0;
+#pragma unroll
+    for (int q = 0; q < kNQ; ++q)
+      if (lane + 32 * q >= E) taken |= 1u << q;  // padding never wins
     float my_v = 0.f;
     int my_i = 0;
     for (int j = 0; j < k; ++j) {
       float bv = 0.f;
       int bi = INT_MAX;
 #pragma unroll
-      for (int q = 0; q < 32; ++q) {
+      for (int q = 0; q < kNQ; ++q) {
         const int e = lane + 32 * q;
-        if (q < nq && e < E && !((taken >> q) & 1u) && (bi == INT_MAX || better(v[q], e, bv, bi))) {
+        if (!((taken >> q) & 1u) && (bi == INT_MAX || better(v[q], e, bv, bi))) {
           bv = v[q];
           bi = e;
         }
@@ -194,27 +202,25 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
     if (lane < k) {
       topk_idx[(size_t)t * k + lane] = my_i;
       topk_w[(size_t)t * k + lane] = __fdiv_rn(ex, s);
-      atomicAdd(&hist[my_i], 1);
+      atomicAdd(counts + my_i, 1);
     }
   }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) blk_hist[(size_t)blockIdx.x * E + e] = hist[e];
+}
+
+__global__ void zero_counts_kernel(int32_t* __restrict__ counts, int E) {
+  for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = 0;
 }
 
 // ------------------------------------------------------------ offsets kernel
-// One CTA: counts[e] = sum of per-block histograms, exclusive scan -> offsets,
-// EP-rank row ranges.
-__global__ void __launch_bounds__(1024) router_offsets_kernel(const int32_t* __restrict__ blk_hist,
-                                                              int nblk, int E, int ep_size,
-                                                              int32_t* __restrict__ counts,
+// One CTA: exclusive scan of counts -> offsets, EP-rank row ranges.
+__global__ void __launch_bounds__(1024) router_offsets_kernel(const int32_t* __restrict__ counts,
+                                                              int E, int ep_size,
                                                               int32_t* __restrict__ offsets,
                                                               int32_t* __restrict__ rank_offsets) {
   __shared__ int warp_sum[32];
   __shared__ int excl[kMaxExperts + 1];
   const int e = threadIdx.x;
-  int c = 0;
-  if (e < E)
-    for (int b = 0; b < nblk; ++b) c += blk_hist[(size_t)b * E + e];
+  const int c = e < E ? counts[e] : 0;
   const int lane = e & 31, warp = e >> 5;
   int incl = c;
 #pragma unroll
@@ -225,7 +231,7 @@ __global__ void __launch_bounds__(1024) router_offsets_kernel(const int32_t* __r
   if (lane == 31) warp_sum[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int ws = warp_sum[lane];
+    const int ws = warp_sum[lane];
     int wi = ws;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -237,7 +243,6 @@ __global__ void __launch_bounds__(1024) router_offsets_kernel(const int32_t* __r
   __syncthreads();
   const int ex = warp_sum[warp] + incl - c;
   if (e < E) {
-    counts[e] = c;
     offsets[e] = ex;
     excl[e] = ex;
   }
@@ -345,8 +350,8 @@ size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
 int route_ws_layout(int T, int E, size_t* logits_bytes, size_t* hist_bytes) {
   const size_t nblk = (size_t)((T + kTopkTokPerBlock - 1) / kTopkTokPerBlock);
-  *logits_bytes = align256(sizeof(float) * (size_t)T * E);
-  *hist_bytes = align256(sizeof(int32_t) * (nblk > 0 ? nblk : 1) * E);
+  *logits_bytes = align256(sizeof(float) * (size_t)(T > 0 ? T : 1) * E);
+  *hist_bytes = 0;
   return (int)nblk;
 }
 
@@ -374,8 +379,6 @@ BwdLayout bwd_layout(int T, int H, int E) {
   L.total = off;
   return L;
 }
-
-bool g_logit_attr[64] = {};
 
 }  // namespace
 }  // namespace moe
@@ -415,31 +418,33 @@ int moe_route_topk(const void* x, const float* Wr, const float* bias, int T, int
     return fail(MOE_ERR_WORKSPACE, "moe_route_topk: workspace %zu < %zu bytes", ws_bytes, lb + hb);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* logits = static_cast<float*>(ws);
-  int32_t* blk_hist = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + lb);
-  const int dev = current_device();
-  if (dev < 0) return fail(MOE_ERR_CUDA, "moe_route_topk: no current CUDA device");
-  if (!g_logit_attr[dev]) {
-    cudaFuncSetAttribute(router_logits_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)kLogitSmem);
-    cudaFuncSetAttribute(router_logits_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)kLogitSmem);
-    g_logit_attr[dev] = true;
-  }
+  zero_counts_kernel<<<1, 256, 0, s>>>(counts, E);
+  if (int rc = check_launch("moe_route_topk: zero counts")) return rc;
   if (T > 0) {
     dim3 grid((T + kLogitTok - 1) / kLogitTok, (E + kLogitExp - 1) / kLogitExp);
-    const bool vec = (E % 8) == 0;
-    if (vec)
-      router_logits_kernel<true><<<grid, 256, kLogitSmem, s>>>(
+    if (E % 4 == 0)
+      router_logits_kernel<true><<<grid, kLogitThreads, 0, s>>>(
           static_cast<const __nv_bfloat16*>(x), Wr, bias, T, H, E, logits);
     else
-      router_logits_kernel<false><<<grid, 256, kLogitSmem, s>>>(
+      router_logits_kernel<false><<<grid, kLogitThreads, 0, s>>>(
           static_cast<const __nv_bfloat16*>(x), Wr, bias, T, H, E, logits);
     if (int rc = check_launch("moe_route_topk: logits kernel")) return rc;
-    router_topk_kernel<<<nblk, 256, 0, s>>>(logits, T, E, k, topk_idx, topk_w, blk_hist);
+    const int nq = (E + 31) / 32;
+    if (nq <= 1)
+      router_topk_kernel<1><<<nblk, 256, 0, s>>>(logits, T, E, k, topk_idx, topk_w, counts);
+    else if (nq <= 2)
+      router_topk_kernel<2><<<nblk, 256, 0, s>>>(logits, T, E, k, topk_idx, topk_w, counts);
+    else if (nq <= 4)
+      router_topk_kernel<4><<<nblk, 256, 0, s>>>(logits, T, E, k, topk_idx, topk_w, counts);
+    else if (nq <= 8)
+      router_topk_kernel<8><<<nblk, 256, 0, s>>>(logits, T, E, k, topk_idx, topk_w, counts);
+    else if (nq <= 16)
+      router_topk_kernel<16><<<nblk, 256, 0, s>>>(logits, T, E, k, topk_idx, topk_w, counts);
+    else
+      router_topk_kernel<32><<<nblk, 256, 0, s>>>(logits, T, E, k, topk_idx, topk_w, counts);
     if (int rc = check_launch("moe_route_topk: top-k kernel")) return rc;
   }
-  router_offsets_kernel<<<1, 1024, 0, s>>>(blk_hist, T > 0 ? nblk : 0, E, ep_size, counts,
-                                           offsets, rank_offsets);
+  router_offsets_kernel<<<1, 1024, 0, s>>>(counts, E, ep_size, offsets, rank_offsets);
   return check_launch("moe_route_topk: offsets kernel");
 }
 

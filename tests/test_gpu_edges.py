@@ -1,0 +1,176 @@
+"""Edge cases of the CUDA path against the CPU oracle: one token, one expert
+(a plain SwiGLU MLP), k = E, empty experts, every token on one expert,
+segmented (source-rank x expert) row layouts, gradient accumulation, and the
+device status word for bad index data (kernels skip the bad entries)."""
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import moe_expert_layer_topk_gb300 as m
+import oracle
+from gpu_util import assert_close, bits, f32, inputs, oracle_backward, oracle_chain, to_dev
+from moe_expert_layer_topk_gb300.synth import LayerShape, bf16_bits, make_segment_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def run_layer(inp, bias=None):
+    g = to_dev(inp)
+    L = m.MoELayer(inp["T"], inp["H"], inp["I"], inp["E"], inp["k"], inp["ep_size"])
+    L.forward(g["x"], g["Wr"], g["bias"] if bias is None else bias, g["Wg"], g["Wu"], g["Wd"])
+    L.backward(g["dy"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"])
+    torch.cuda.synchronize()
+    assert m.moe_read_device_status(reset=True) == 0
+    return L, g
+
+
+def check_all(L, inp):
+    f = oracle_chain(inp)
+    b = oracle_backward(inp, f)
+    assert np.array_equal(L.topk_idx.cpu().numpy(), f["rt"]["topk_idx"])
+    assert np.array_equal(L.offsets.cpu().numpy(), f["rt"]["offsets"])
+    assert np.array_equal(L.row_of_slot.cpu().numpy(), f["dp"]["row_of_slot"])
+    assert_close(L.y, f["y"], "y")
+    for name in ("dx", "dWg", "dWu", "dWd", "dWr"):
+        assert_close(getattr(L, name), b[name], name)
+    return f, b
+
+
+def test_single_token():
+    inp = inputs(1, 128, 64, 8, 2, seed=11, ep=2)
+    L, _ = run_layer(inp)
+    check_all(L, inp)
+
+
+def test_one_expert_is_a_dense_swiglu_mlp():
+    inp = inputs(300, 256, 128, 1, 1, seed=12)
+    L, g = run_layer(inp)
+    check_all(L, inp)
+    assert torch.all(L.topk_w == 1.0)
+    # independent fp32 torch reference of the dense MLP
+    x = g["x"].float()
+    ref = (F.silu(x @ g["Wg"][0].float().T) * (x @ g["Wu"][0].float().T)) @ g["Wd"][0].float().T
+    assert_close(L.y, ref.cpu().numpy(), "y vs torch fp32 MLP")
+
+
+def test_k_equals_E():
+    inp = inputs(200, 128, 64, 4, 4, seed=13, router_std=0.3)
+    L, _ = run_layer(inp)
+    check_all(L, inp)
+    w = L.topk_w.cpu().double()
+    assert torch.allclose(w.sum(1), torch.ones(200, dtype=torch.float64), atol=1e-6)
+
+
+def test_empty_experts_and_accumulate():
+    inp = inputs(400, 128, 128, 8, 2, seed=14, router_std=0.3)
+    bias = torch.zeros(8)
+    bias[[1, 5, 6]] = -1.0e4
+    inp["bias"] = bias
+    L, g = run_layer(inp)
+    counts = L.counts.cpu().numpy()
+    assert counts[1] == counts[5] == counts[6] == 0
+    check_all(L, inp)
+    for name in ("dWg", "dWu", "dWd"):
+        t = getattr(L, name)
+        assert torch.count_nonzero(t[[1, 5, 6]]) == 0, name
+    keep = {n: getattr(L, n).clone() for n in ("dWg", "dWu", "dWd", "dWr")}
+    L.backward(g["dy"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"], accumulate=True)
+    torch.cuda.synchronize()
+    for n, v in keep.items():
+        assert torch.equal(getattr(L, n), v + v), n   # prev + identical fresh sum
+
+
+def test_every_token_on_one_expert():
+    inp = inputs(1000, 256, 128, 8, 1, seed=15)
+    bias = torch.zeros(8)
+    bias[3] = 1.0e4
+    inp["bias"] = bias
+    L, _ = run_layer(inp)
+    assert L.counts.cpu().tolist() == [0, 0, 0, 1000, 0, 0, 0, 0]
+    check_all(L, inp)
+
+
+def test_zero_tokens():
+    L = m.MoELayer(0, 128, 64, 8, 2, 2)
+    x = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
+    Wr = torch.randn(128, 8, device="cuda")
+    m.moe_route_topk(x, Wr, None, 0, 128, 8, 2, 2, L.topk_idx, L.topk_w, L.counts, L.offsets,
+                     L.rank_offsets, L.ws_route)
+    torch.cuda.synchronize()
+    assert L.counts.cpu().tolist() == [0] * 8
+    assert L.offsets.cpu().tolist() == [0] * 9
+    assert L.rank_offsets.cpu().tolist() == [0, 0, 0]
+
+
+@pytest.mark.parametrize("R,H,I,E,S", [(1500, 256, 128, 4, 3), (700, 128, 192, 6, 2)])
+def test_segmented_rows(R, H, I, E, S):
+    """Receive-side layout: (source rank x local expert) segments, some empty;
+    the weight gradient of an expert sums over all its segments."""
+    shape = LayerShape(T=R, H=H, I=I, E=E, k=1, ep_size=1, segments=True, src_ranks=S)
+    s = make_segment_inputs(shape, seed=16)
+    so = s["seg_offsets"].clone()
+    so[3] = so[2]              # segment 2 empty
+    so[4:] = torch.maximum(so[4:], so[3])
+    se = s["seg_expert"]
+    dev = "cuda"
+    xp, Wg, Wu, Wd = (s[n].to(dev) for n in ("x_perm", "Wg", "Wu", "Wd"))
+    so_d, se_d = so.to(dev), se.to(dev)
+    nseg = len(so) - 1
+    h = torch.zeros(R, I, dtype=torch.bfloat16, device=dev)
+    gu = torch.zeros(R, 2 * I, dtype=torch.bfloat16, device=dev)
+    y = torch.zeros(R, H, dtype=torch.bfloat16, device=dev)
+    m.moe_grouped_gemm_swiglu(xp, Wg, Wu, nseg, so_d, se_d, R, H, I, E, h, gu)
+    m.moe_grouped_gemm_down(h, Wd, nseg, so_d, se_d, R, H, I, E, y)
+    dy = torch.randn(R, H, device=dev).to(torch.bfloat16)
+    dgu = torch.zeros(R, 2 * I, dtype=torch.bfloat16, device=dev)
+    dWd = torch.empty(E, H, I, device=dev)
+    dx = torch.zeros(R, H, dtype=torch.bfloat16, device=dev)
+    dWg = torch.empty(E, I, H, device=dev)
+    dWu = torch.empty(E, I, H, device=dev)
+    m.moe_grouped_gemm_down_bwd(dy, h, gu, Wd, nseg, so_d, se_d, R, H, I, E, dgu, dWd)
+    m.moe_grouped_gemm_swiglu_bwd(dgu, xp, Wg, Wu, nseg, so_d, se_d, R, H, I, E, dx, dWg, dWu)
+    torch.cuda.synchronize()
+    assert m.moe_read_device_status(reset=True) == 0
+    son, sen = so.numpy(), se.numpy()
+    xo = oracle.widen_bf16(bf16_bits(s["x_perm"]))
+    h_ref, gu_ref = oracle.grouped_gemm_swiglu(xo, bf16_bits(s["Wg"]), bf16_bits(s["Wu"]), son, sen,
+                                               save_gu=True)
+    covered = slice(int(son[0]), int(son[-1]))
+    assert_close(h[covered], h_ref[covered], "h")
+    y_ref = oracle.grouped_gemm_down(f32(h), bf16_bits(s["Wd"]), son, sen)
+    assert_close(y[covered], y_ref[covered], "y_perm")
+    dgu_ref, dWd_ref = oracle.grouped_gemm_down_bwd(f32(dy), f32(h), f32(gu), bf16_bits(s["Wd"]), son, sen)
+    assert_close(dgu[covered], dgu_ref[covered], "dgu")
+    assert_close(dWd, dWd_ref, "dWd")
+    dx_ref, dWg_ref, dWu_ref = oracle.grouped_gemm_swiglu_bwd(f32(dgu), xo, bf16_bits(s["Wg"]),
+                                                              bf16_bits(s["Wu"]), son, sen)
+    assert_close(dx[covered], dx_ref[covered], "dx_perm")
+    assert_close(dWg, dWg_ref, "dWg")
+    assert_close(dWu, dWu_ref, "dWu")
+
+
+def test_bad_index_data_sets_status_without_fault():
+    """Out-of-range expert ids and offsets that disagree with them are skipped
+    by the kernels and reported through the device status word."""
+    inp = inputs(64, 128, 64, 8, 2, seed=17)
+    g = to_dev(inp)
+    L = m.MoELayer(64, 128, 64, 8, 2, 2)
+    L.route(g["x"], g["Wr"], None)
+    torch.cuda.synchronize()
+    assert m.moe_read_device_status(reset=True) == 0
+    bad = L.topk_idx.clone()
+    bad[5, 1] = 8          # expert id == E
+    bad[9, 0] = -3
+    m.moe_dispatch(g["x"], bad, L.offsets, 64, 128, 8, 2, L.x_perm, L.row_of_slot, L.token_of_row,
+                   L.ws_dispatch)
+    torch.cuda.synchronize()
+    st = m.moe_read_device_status(reset=True)
+    assert st & 1, st  # MOE_STATUS_BAD_INDEX
+    assert L.row_of_slot[5, 1].item() == -1 and L.row_of_slot[9, 0].item() == -1
+    # segment table running past R
+    so = L.offsets.clone()
+    so[-1] = 64 * 2 + 500
+    m.moe_grouped_gemm_swiglu(L.x_perm, g["Wg"], g["Wu"], 8, so, None, 128, 128, 64, 8, L.h, None)
+    torch.cuda.synchronize()
+    assert m.moe_read_device_status(reset=True) & 2  # MOE_STATUS_BAD_SEGMENTS
