@@ -40,7 +40,7 @@ namespace tc {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
+constexpr int STAGES = 3;
 constexpr int THREADS = 192;
 constexpr int A_BYTES = BM * BK * 2;          // 16 KiB
 constexpr int B_BYTES_MAX = 256 * BK * 2;     // 32 KiB
@@ -49,6 +49,13 @@ constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 512;
 constexpr int CHUNK_BYTES = 64 * BK * 2;      // one 64(MN) x 64(K) MN-major box: 8 KiB
 constexpr unsigned long long TIMEOUT_NS = 2000000000ull;
+// Epilogue staging: each epilogue warp owns a ring of 4 boxes of 32 rows x
+// 64 bytes (32 bf16 or 16 fp32 columns), written in the 64-byte swizzle
+// pattern and sent to global memory by TMA bulk tensor stores.
+constexpr int EP_BOX_BYTES = 32 * 64;
+constexpr int EP_SLOTS = 4;
+constexpr int EP_WARP_BYTES = EP_BOX_BYTES * EP_SLOTS;
+constexpr int EP_BYTES = 4 * EP_WARP_BYTES;
 
 enum Kind : int { GATE_UP_FWD = 0, DOWN_FWD = 1, DOWN_BWD_DX = 2, GATE_UP_BWD_DX = 3, DW = 4, DENSE_ADD = 5 };
 
@@ -91,7 +98,7 @@ struct Ctl {
   int grp_rows[kMaxSegments];       // DW: rows per output group
 };
 
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Ctl);
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + EP_BYTES + sizeof(Ctl);
 
 // ------------------------------------------------------------- PTX wrappers
 
@@ -158,6 +165,55 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
       : "memory");
 }
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// One epilogue warp's staging ring (see EP_*).  Lane i holds row i of a box.
+struct EpRing {
+  uint8_t* base;
+  int slot;
+  int lane;
+  __device__ __forceinline__ uint8_t* acquire() {
+    // the store issued from this slot EP_SLOTS boxes ago must have read it
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
+    __syncwarp();
+    return base + slot * EP_BOX_BYTES;
+  }
+  // 16-byte chunk c (0..3) of this lane's 64-byte row, 64-byte swizzle
+  __device__ __forceinline__ void put(uint8_t* box, int c, uint4 v) {
+    *reinterpret_cast<uint4*>(box + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = v;
+  }
+  __device__ __forceinline__ void issue(uint8_t* box, const CUtensorMap* map, int x, int y,
+                                        bool reduce = false) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+      if (reduce)
+        tma_reduce_add_2d(map, smem_u32(box), x, y);
+      else
+        tma_store_2d(map, smem_u32(box), x, y);
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+    slot = (slot + 1) & (EP_SLOTS - 1);
+  }
+  __device__ __forceinline__ void drain() {
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
+  }
+};
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -292,11 +348,13 @@ template <int KIND>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB0,
-                        const __grid_constant__ CUtensorMap tmB1, const Params p) {
+                        const __grid_constant__ CUtensorMap tmB1,
+                        const __grid_constant__ CUtensorMap tmO0,
+                        const __grid_constant__ CUtensorMap tmO1, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + (size_t)STAGES * STAGE_BYTES);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + (size_t)STAGES * STAGE_BYTES + EP_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int limit = Traits<KIND>::rows ? p.M : p.K;  // rows addressable through the segment table
 
@@ -370,6 +428,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB0);
       prefetch_tmap(&tmB1);
+      prefetch_tmap(&tmO0);
+      prefetch_tmap(&tmO1);
     }
   } else if (warp == 1) {
     tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
@@ -513,21 +573,26 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // ============================ epilogue ================================
     const int q = warp & 3;
-    const int row_in_tile = q * 32 + lane;
+    EpRing ring{smem + (size_t)STAGES * STAGE_BYTES + (size_t)(warp - 2) * EP_WARP_BYTES, 0, lane};
     int local = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
       const Tile t = decode_tile<KIND>(tile, p, ctl);
       const int buf = local & 1;
       const uint32_t use = (uint32_t)(local >> 1);
+      // this warp's 32 rows: full boxes go out through TMA stores, a box that
+      // straddles the end of its segment through masked per-row stores
+      const int rb = t.m0 + q * 32;
+      const int r = rb + lane;
+      const bool valid = Traits<KIND>::rows ? (r < t.row_end) : (r < p.M);
+      const bool full = Traits<KIND>::rows ? (rb + 31 < t.row_end) : (rb < p.M);
+      const bool any = Traits<KIND>::rows ? (rb < t.row_end) : (rb < p.M);
       // SwiGLU backward: the saved g, u of this thread's row do not depend on
       // the accumulator, so the first chunk is requested before waiting.
       uint4 gpre[4], upre[4];
-      const int r2 = t.m0 + row_in_tile;
-      const bool valid2 = (KIND == DOWN_BWD_DX) && r2 < t.row_end;
       const __nv_bfloat16* grow =
-          static_cast<const __nv_bfloat16*>(p.aux) + (size_t)r2 * 2 * p.I + t.n0;
+          static_cast<const __nv_bfloat16*>(p.aux) + (size_t)r * 2 * p.I + t.n0;
       auto prefetch_gu = [&](int c) {
-        if (valid2) {
+        if (KIND == DOWN_BWD_DX && valid) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             gpre[i] = __ldg(reinterpret_cast<const uint4*>(grow + c) + i);
@@ -541,27 +606,40 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * ACC_COLS);
 
       if constexpr (KIND == GATE_UP_FWD) {
-        const int r = t.m0 + row_in_tile;
-        const bool valid = r < t.row_end;
         __nv_bfloat16* h = static_cast<__nv_bfloat16*>(p.out0);
         __nv_bfloat16* gu = static_cast<__nv_bfloat16*>(p.out1);
-        for (int c = 0; c < p.NH; c += 32) {
+        for (int c = 0; any && c < p.NH; c += 32) {
           uint32_t g[32], u[32];
           tmem_ld32(taddr + c, g);
           tmem_ld32(taddr + p.NH + c, u);
           tmem_wait_ld();
-          if (valid) {
-            uint32_t hp[16], gp[16], upk[16];
+          uint32_t hp[16], gp[16], upk[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float g0 = f32(g[2 * i]), g1 = f32(g[2 * i + 1]);
-              const float u0 = f32(u[2 * i]), u1 = f32(u[2 * i + 1]);
-              const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
-              const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
-              hp[i] = pack_bf16x2(h0, h1);
-              gp[i] = pack_bf16x2(g0, g1);
-              upk[i] = pack_bf16x2(u0, u1);
+          for (int i = 0; i < 16; ++i) {
+            const float g0 = f32(g[2 * i]), g1 = f32(g[2 * i + 1]);
+            const float u0 = f32(u[2 * i]), u1 = f32(u[2 * i + 1]);
+            const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
+            const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
+            hp[i] = pack_bf16x2(h0, h1);
+            gp[i] = pack_bf16x2(g0, g1);
+            upk[i] = pack_bf16x2(u0, u1);
+          }
+          if (full) {
+            uint8_t* bx = ring.acquire();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ring.put(bx, i, make_uint4(hp[4 * i], hp[4 * i + 1], hp[4 * i + 2], hp[4 * i + 3]));
+            ring.issue(bx, &tmO0, t.n0 + c, rb);
+            if (gu) {
+              bx = ring.acquire();
+#pragma unroll
+              for (int i = 0; i < 4; ++i) ring.put(bx, i, make_uint4(gp[4 * i], gp[4 * i + 1], gp[4 * i + 2], gp[4 * i + 3]));
+              ring.issue(bx, &tmO1, t.n0 + c, rb);
+              bx = ring.acquire();
+#pragma unroll
+              for (int i = 0; i < 4; ++i) ring.put(bx, i, make_uint4(upk[4 * i], upk[4 * i + 1], upk[4 * i + 2], upk[4 * i + 3]));
+              ring.issue(bx, &tmO1, p.I + t.n0 + c, rb);
             }
+          } else if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(h + (size_t)r * p.I + t.n0 + c);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -578,18 +656,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       } else if constexpr (KIND == DOWN_FWD || KIND == GATE_UP_BWD_DX || KIND == DENSE_ADD) {
-        const int r = t.m0 + row_in_tile;
-        const bool valid = r < t.row_end;
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out0);
-        for (int c = 0; c < p.BN; c += 32) {
+        for (int c = 0; any && c < p.BN; c += 32) {
           uint32_t a[32];
           tmem_ld32(taddr + c, a);
           tmem_wait_ld();
-          if (valid) {
-            float v[32];
+          float v[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = f32(a[i]);
-            if constexpr (KIND == DENSE_ADD) {
+          for (int i = 0; i < 32; ++i) v[i] = f32(a[i]);
+          if constexpr (KIND == DENSE_ADD) {
+            if (valid) {
               const float4* add = reinterpret_cast<const float4*>(
                   static_cast<const float*>(p.aux) + (size_t)r * p.ldo + t.n0 + c);
 #pragma unroll
@@ -598,18 +674,26 @@ __global__ void __launch_bounds__(THREADS, 1)
                 v[4 * i] += w.x; v[4 * i + 1] += w.y; v[4 * i + 2] += w.z; v[4 * i + 3] += w.w;
               }
             }
+          }
+          uint4 pk[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            pk[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                               pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+          if (full) {
+            uint8_t* bx = ring.acquire();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ring.put(bx, i, pk[i]);
+            ring.issue(bx, &tmO0, t.n0 + c, rb);
+          } else if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(out + (size_t)r * p.ldo + t.n0 + c);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                                  pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+            for (int i = 0; i < 4; ++i) dst[i] = pk[i];
           }
         }
       } else if constexpr (KIND == DOWN_BWD_DX) {
-        const int r = r2;
-        const bool valid = valid2;
         __nv_bfloat16* dgu = static_cast<__nv_bfloat16*>(p.out0);
-        for (int c = 0; c < p.BN; c += 32) {
+        for (int c = 0; any && c < p.BN; c += 32) {
           uint32_t a[32];
           tmem_ld32(taddr + c, a);
           uint4 gcur[4], ucur[4];
@@ -620,49 +704,56 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           if (c + 32 < p.BN) prefetch_gu(c + 32);
           tmem_wait_ld();
-          if (valid) {
+          uint4 og4[4], ou4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t gw[4] = {gcur[i].x, gcur[i].y, gcur[i].z, gcur[i].w};
+            const uint32_t uw[4] = {ucur[i].x, ucur[i].y, ucur[i].z, ucur[i].w};
+            uint32_t og[4], ou[4];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              float dg2[2], du2[2];
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const float g = hh ? bf16hi(gw[jj]) : bf16lo(gw[jj]);
+                const float u = hh ? bf16hi(uw[jj]) : bf16lo(uw[jj]);
+                const float dh = f32(a[8 * i + 2 * jj + hh]);
+                const float sg = 1.0f / (1.0f + __expf(-g));
+                dg2[hh] = dh * u * sg * (1.0f + g * (1.0f - sg));
+                du2[hh] = dh * (g * sg);
+              }
+              og[jj] = pack_bf16x2(dg2[0], dg2[1]);
+              ou[jj] = pack_bf16x2(du2[0], du2[1]);
+            }
+            og4[i] = make_uint4(og[0], og[1], og[2], og[3]);
+            ou4[i] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+          }
+          if (full) {
+            uint8_t* bx = ring.acquire();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ring.put(bx, i, og4[i]);
+            ring.issue(bx, &tmO0, t.n0 + c, rb);
+            bx = ring.acquire();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ring.put(bx, i, ou4[i]);
+            ring.issue(bx, &tmO0, p.I + t.n0 + c, rb);
+          } else if (valid) {
             uint4* gdst = reinterpret_cast<uint4*>(dgu + (size_t)r * 2 * p.I + t.n0 + c);
             uint4* udst = reinterpret_cast<uint4*>(dgu + (size_t)r * 2 * p.I + p.I + t.n0 + c);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const uint4 gv = gcur[i], uv = ucur[i];
-              const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-              const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
-              uint32_t og[4], ou[4];
-#pragma unroll
-              for (int jj = 0; jj < 4; ++jj) {
-                float dg2[2], du2[2];
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                  const float g = hh ? bf16hi(gw[jj]) : bf16lo(gw[jj]);
-                  const float u = hh ? bf16hi(uw[jj]) : bf16lo(uw[jj]);
-                  const float dh = f32(a[8 * i + 2 * jj + hh]);
-                  const float sg = 1.0f / (1.0f + __expf(-g));
-                  dg2[hh] = dh * u * sg * (1.0f + g * (1.0f - sg));
-                  du2[hh] = dh * (g * sg);
-                }
-                og[jj] = pack_bf16x2(dg2[0], dg2[1]);
-                ou[jj] = pack_bf16x2(du2[0], du2[1]);
-              }
-              gdst[i] = make_uint4(og[0], og[1], og[2], og[3]);
-              udst[i] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+              gdst[i] = og4[i];
+              udst[i] = ou4[i];
             }
           }
         }
-      } else {  // DW
-        const int m = t.m0 + row_in_tile;
-        const bool valid = m < p.M;
+      } else {  // DW: fp32 [group, M, N] (optionally split at split_m over two tensors)
         const bool nonempty = ctl->grp_rows[t.group] > 0;
-        float* dst_row = nullptr;
-        if (valid) {
-          if (p.split_m > 0 && m >= p.split_m)
-            dst_row = static_cast<float*>(p.out1) + ((size_t)t.group * p.split_m + (m - p.split_m)) * p.ldo;
-          else if (p.split_m > 0)
-            dst_row = static_cast<float*>(p.out0) + ((size_t)t.group * p.split_m + m) * p.ldo;
-          else
-            dst_row = static_cast<float*>(p.out0) + ((size_t)t.group * p.M + m) * p.ldo;
-        }
-        if (nonempty || !p.accumulate) {
+        if (full && (nonempty || !p.accumulate)) {
+          const bool second = p.split_m > 0 && rb >= p.split_m;
+          const CUtensorMap* map = second ? &tmO1 : &tmO0;
+          const int y = p.split_m > 0 ? t.group * p.split_m + (second ? rb - p.split_m : rb)
+                                      : t.group * p.M + rb;
           for (int c = 0; c < p.BN; c += 32) {
             uint32_t a[32];
             if (nonempty) {
@@ -672,17 +763,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i) a[i] = 0u;
             }
-            if (valid) {
-              float4* dst = reinterpret_cast<float4*>(dst_row + t.n0 + c);
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                float4 v = make_float4(f32(a[4 * i]), f32(a[4 * i + 1]), f32(a[4 * i + 2]), f32(a[4 * i + 3]));
-                if (p.accumulate) {
-                  const float4 o = dst[i];
-                  v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
-                }
-                dst[i] = v;
-              }
+            for (int half = 0; half < 2; ++half) {
+              uint8_t* bx = ring.acquire();
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                ring.put(bx, i, make_uint4(a[16 * half + 4 * i], a[16 * half + 4 * i + 1],
+                                           a[16 * half + 4 * i + 2], a[16 * half + 4 * i + 3]));
+              ring.issue(bx, map, t.n0 + c + 16 * half, y, p.accumulate != 0);
             }
           }
         }
@@ -691,6 +779,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[buf]));
     }
+    ring.drain();
   }
 
   tc_fence_before();
@@ -725,22 +814,31 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor [outer, inner] row-major, box {box_inner, box_outer}, 128-byte swizzle.
+// 2-D tensor [outer, inner] row-major, box {box_inner, box_outer}.  Operand
+// maps are bf16 with the 128-byte swizzle; output maps use 64-byte boxes with
+// the 64-byte swizzle (bf16 or fp32).
 int make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
-              uint32_t box_outer) {
+              uint32_t box_outer, bool fp32 = false,
+              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const uint64_t esz = fp32 ? 4 : 2;
   cuuint64_t dims[2] = {inner, outer > 0 ? outer : 1};
-  cuuint64_t strides[1] = {inner * 2};
+  cuuint64_t strides[1] = {inner * esz};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
-                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%llu x %llu] box %u x %u",
                 (int)r, (unsigned long long)outer, (unsigned long long)inner, box_inner, box_outer);
   return MOE_OK;
+}
+
+// Output map: 32 rows x 64 bytes per box (32 bf16 / 16 fp32 columns).
+int make_out_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, bool fp32) {
+  return make_tmap(m, ptr, inner, outer, fp32 ? 16 : 32, 32, fp32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 uint32_t make_idesc(int n, bool a_mn, bool b_mn) {
@@ -757,7 +855,8 @@ bool g_attr[6][64] = {};
 
 template <int KIND>
 int launch(const Params& p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-           int upper_tiles, cudaStream_t s, const char* what) {
+           const CUtensorMap& o0, const CUtensorMap& o1, int upper_tiles, cudaStream_t s,
+           const char* what) {
   const int dev = current_device();
   if (dev < 0) return fail(MOE_ERR_CUDA, "%s: no current CUDA device", what);
   if (!g_attr[KIND][dev]) {
@@ -770,7 +869,7 @@ int launch(const Params& p, const CUtensorMap& a, const CUtensorMap& b0, const C
   if (sms <= 0) return fail(MOE_ERR_CUDA, "%s: cannot query the SM count", what);
   int grid = upper_tiles < sms ? upper_tiles : sms;
   if (grid < 1) grid = 1;
-  grouped_gemm_kernel<KIND><<<grid, THREADS, SMEM_BYTES, s>>>(a, b0, b1, p);
+  grouped_gemm_kernel<KIND><<<grid, THREADS, SMEM_BYTES, s>>>(a, b0, b1, o0, o1, p);
   return check_launch(what);
 }
 
@@ -820,7 +919,9 @@ int launch_dense_add_bf16(const void* A, const void* B, const float* add, void* 
   CUtensorMap ta, tb;
   if (int rc = make_tmap(&ta, A, K, M, 64, BM)) return rc;
   if (int rc = make_tmap(&tb, B, K, N, 64, p.BN)) return rc;
-  return launch<DENSE_ADD>(p, ta, tb, tb, row_tiles_upper(M, 1, p.n_tiles), stream,
+  CUtensorMap to;
+  if (int rc = make_out_map(&to, out, N, M, false)) return rc;
+  return launch<DENSE_ADD>(p, ta, tb, tb, to, to, row_tiles_upper(M, 1, p.n_tiles), stream,
                            "router backward dx GEMM");
 }
 
@@ -840,7 +941,9 @@ int launch_dw_split(const void* A, const void* B, int K_rows, int M, int N,
   CUtensorMap ta, tb;
   if (int rc = make_tmap(&ta, A, M, K_rows, 64, 64)) return rc;
   if (int rc = make_tmap(&tb, B, N, K_rows, 64, 64)) return rc;
-  return launch<DW>(p, ta, tb, tb, num_seg * p.m_tiles * p.n_tiles, stream,
+  CUtensorMap to;
+  if (int rc = make_out_map(&to, out, N, (uint64_t)num_seg * M, true)) return rc;
+  return launch<DW>(p, ta, tb, tb, to, to, num_seg * p.m_tiles * p.n_tiles, stream,
                     "router backward dWr GEMM");
 }
 
@@ -880,7 +983,10 @@ int moe_grouped_gemm_swiglu(const void* x_perm, const void* Wg, const void* Wu, 
   if (int rc = make_tmap(&ta, x_perm, H, R, 64, BM)) return rc;
   if (int rc = make_tmap(&tg, Wg, H, (uint64_t)E * I, 64, p.NH)) return rc;
   if (int rc = make_tmap(&tu, Wu, H, (uint64_t)E * I, 64, p.NH)) return rc;
-  return launch<GATE_UP_FWD>(p, ta, tg, tu, row_tiles_upper(R, num_seg, p.n_tiles),
+  CUtensorMap th, tgu;
+  if (int rc = make_out_map(&th, h, I, R, false)) return rc;
+  if (int rc = make_out_map(&tgu, gu_save ? gu_save : h, gu_save ? 2 * I : I, R, false)) return rc;
+  return launch<GATE_UP_FWD>(p, ta, tg, tu, th, tgu, row_tiles_upper(R, num_seg, p.n_tiles),
                              static_cast<cudaStream_t>(stream), fn);
 }
 
@@ -908,7 +1014,9 @@ int moe_grouped_gemm_down(const void* h, const void* Wd, int num_seg, const int3
   CUtensorMap ta, tb;
   if (int rc = make_tmap(&ta, h, I, R, 64, BM)) return rc;
   if (int rc = make_tmap(&tb, Wd, I, (uint64_t)E * H, 64, p.BN)) return rc;
-  return launch<DOWN_FWD>(p, ta, tb, tb, row_tiles_upper(R, num_seg, p.n_tiles),
+  CUtensorMap to;
+  if (int rc = make_out_map(&to, y_perm, H, R, false)) return rc;
+  return launch<DOWN_FWD>(p, ta, tb, tb, to, to, row_tiles_upper(R, num_seg, p.n_tiles),
                           static_cast<cudaStream_t>(stream), fn);
 }
 
@@ -942,7 +1050,9 @@ int moe_grouped_gemm_down_bwd(const void* dy_perm, const void* h, const void* gu
     CUtensorMap ta, tb;
     if (int rc = make_tmap(&ta, dy_perm, H, R, 64, BM)) return rc;
     if (int rc = make_tmap(&tb, Wd, I, (uint64_t)E * H, 64, 64)) return rc;
-    if (int rc = launch<DOWN_BWD_DX>(p, ta, tb, tb, row_tiles_upper(R, num_seg, p.n_tiles), s, fn))
+    CUtensorMap to;
+    if (int rc = make_out_map(&to, dgu, 2 * I, R, false)) return rc;
+    if (int rc = launch<DOWN_BWD_DX>(p, ta, tb, tb, to, to, row_tiles_upper(R, num_seg, p.n_tiles), s, fn))
       return rc;
   }
   // dWd[e] = dy_perm[rows of e]^T . h[rows of e]
@@ -965,7 +1075,9 @@ int moe_grouped_gemm_down_bwd(const void* dy_perm, const void* h, const void* gu
   CUtensorMap ta, tb;
   if (int rc = make_tmap(&ta, dy_perm, H, R, 64, 64)) return rc;
   if (int rc = make_tmap(&tb, h, I, R, 64, 64)) return rc;
-  return launch<DW>(p, ta, tb, tb, E * p.m_tiles * p.n_tiles, s, fn);
+  CUtensorMap to;
+  if (int rc = make_out_map(&to, dWd, I, (uint64_t)E * H, true)) return rc;
+  return launch<DW>(p, ta, tb, tb, to, to, E * p.m_tiles * p.n_tiles, s, fn);
 }
 
 int moe_grouped_gemm_swiglu_bwd(const void* dgu, const void* x_perm, const void* Wg,
@@ -1000,7 +1112,9 @@ int moe_grouped_gemm_swiglu_bwd(const void* dgu, const void* x_perm, const void*
     if (int rc = make_tmap(&ta, dgu, 2 * I, R, 64, BM)) return rc;
     if (int rc = make_tmap(&tg, Wg, H, (uint64_t)E * I, 64, 64)) return rc;
     if (int rc = make_tmap(&tu, Wu, H, (uint64_t)E * I, 64, 64)) return rc;
-    if (int rc = launch<GATE_UP_BWD_DX>(p, ta, tg, tu, row_tiles_upper(R, num_seg, p.n_tiles), s, fn))
+    CUtensorMap to;
+    if (int rc = make_out_map(&to, dx_perm, H, R, false)) return rc;
+    if (int rc = launch<GATE_UP_BWD_DX>(p, ta, tg, tu, to, to, row_tiles_upper(R, num_seg, p.n_tiles), s, fn))
       return rc;
   }
   if (num_seg == 0) {
@@ -1026,7 +1140,10 @@ int moe_grouped_gemm_swiglu_bwd(const void* dgu, const void* x_perm, const void*
   CUtensorMap ta, tb;
   if (int rc = make_tmap(&ta, dgu, 2 * I, R, 64, 64)) return rc;
   if (int rc = make_tmap(&tb, x_perm, H, R, 64, 64)) return rc;
-  return launch<DW>(p, ta, tb, tb, E * p.m_tiles * p.n_tiles, s, fn);
+  CUtensorMap tog, tou;
+  if (int rc = make_out_map(&tog, dWg, H, (uint64_t)E * I, true)) return rc;
+  if (int rc = make_out_map(&tou, dWu, H, (uint64_t)E * I, true)) return rc;
+  return launch<DW>(p, ta, tb, tb, tog, tou, E * p.m_tiles * p.n_tiles, s, fn);
 }
 
 }  // extern "C"

@@ -320,7 +320,7 @@ int moe_dispatch(const void* x, const int32_t* topk_idx, const int32_t* offsets,
   if (int rc = check_rows_args("moe_dispatch", T, H, k)) return rc;
   if (E <= 0 || E > kMaxExperts || k > E)
     return fail(MOE_ERR_UNSUPPORTED_SHAPE, "moe_dispatch: need 1<=E<=1024, k<=E");
-  if (!topk_idx || !offsets || !row_of_slot || !token_of_row || !ws || (x_perm && !x))
+  if (!ws || (T > 0 && (!topk_idx || !offsets || !row_of_slot || !token_of_row || (x_perm && !x))))
     return fail(MOE_ERR_INVALID_ARG, "moe_dispatch: NULL pointer argument");
   if ((x && !aligned16(x)) || (x_perm && !aligned16(x_perm)) || !aligned16(ws))
     return fail(MOE_ERR_ALIGNMENT, "moe_dispatch: x, x_perm and ws must be 16-byte aligned");
@@ -347,11 +347,11 @@ int moe_combine(const void* y_perm, const float* topk_w, const int32_t* row_of_s
                 int k, void* y, void* stream) {
   clear_error();
   if (int rc = check_rows_args("moe_combine", T, H, k)) return rc;
+  if (T == 0) return MOE_OK;
   if (!y_perm || !topk_w || !row_of_slot || !y)
     return fail(MOE_ERR_INVALID_ARG, "moe_combine: NULL pointer argument");
   if (!aligned16(y_perm) || !aligned16(y))
     return fail(MOE_ERR_ALIGNMENT, "moe_combine: y_perm and y must be 16-byte aligned");
-  if (T == 0) return MOE_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t work = (size_t)T * (H / 8);
   gather_sum_kernel<true, false><<<grid_for(work, 256), 256, 0, s>>>(
@@ -364,11 +364,11 @@ int moe_dispatch_bwd(const void* dx_perm, const int32_t* row_of_slot, int T, int
                      float* dx_acc, void* stream) {
   clear_error();
   if (int rc = check_rows_args("moe_dispatch_bwd", T, H, k)) return rc;
+  if (T == 0) return MOE_OK;
   if (!dx_perm || !row_of_slot || !dx_acc)
     return fail(MOE_ERR_INVALID_ARG, "moe_dispatch_bwd: NULL pointer argument");
   if (!aligned16(dx_perm) || !aligned16(dx_acc))
     return fail(MOE_ERR_ALIGNMENT, "moe_dispatch_bwd: dx_perm and dx_acc must be 16-byte aligned");
-  if (T == 0) return MOE_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t work = (size_t)T * (H / 8);
   gather_sum_kernel<false, true><<<grid_for(work, 256), 256, 0, s>>>(
@@ -382,11 +382,11 @@ int moe_combine_bwd(const void* dy, const void* y_perm, const float* topk_w,
                     void* stream) {
   clear_error();
   if (int rc = check_rows_args("moe_combine_bwd", T, H, k)) return rc;
+  if (T == 0) return MOE_OK;
   if (!dy || !y_perm || !topk_w || !row_of_slot || !dy_perm || !d_w)
     return fail(MOE_ERR_INVALID_ARG, "moe_combine_bwd: NULL pointer argument");
   if (!aligned16(dy) || !aligned16(y_perm) || !aligned16(dy_perm))
     return fail(MOE_ERR_ALIGNMENT, "moe_combine_bwd: dy, y_perm and dy_perm must be 16-byte aligned");
-  if (T == 0) return MOE_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   combine_bwd_kernel<<<T, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(dy),
                                        static_cast<const __nv_bfloat16*>(y_perm), topk_w,

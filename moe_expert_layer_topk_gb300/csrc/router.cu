@@ -408,7 +408,8 @@ int moe_route_topk(const void* x, const float* Wr, const float* bias, int T, int
                 k, H);
   if (ep_size < 1 || E % ep_size != 0)
     return fail(MOE_ERR_INVALID_ARG, "moe_route_topk: ep_size=%d must divide E=%d", ep_size, E);
-  if (!x || !Wr || !topk_idx || !topk_w || !counts || !offsets || !rank_offsets || !ws)
+  if (!counts || !offsets || !rank_offsets || !ws ||
+      (T > 0 && (!x || !Wr || !topk_idx || !topk_w)))
     return fail(MOE_ERR_INVALID_ARG, "moe_route_topk: NULL pointer argument");
   if (!aligned16(x) || !aligned16(Wr) || !aligned16(ws) || (bias && !aligned16(bias)))
     return fail(MOE_ERR_ALIGNMENT, "moe_route_topk: x, Wr, bias and ws must be 16-byte aligned");
@@ -463,7 +464,7 @@ int moe_route_topk_bwd(const float* d_w, const float* topk_w, const int32_t* top
   if (E > kMaxExperts || k > kMaxTopK || k > E || H % 64 != 0 || (long long)T * k >= (1ll << 31))
     return fail(MOE_ERR_UNSUPPORTED_SHAPE,
                 "moe_route_topk_bwd: need E<=1024, k<=min(E,32), H%%64==0 (E=%d k=%d H=%d)", E, k, H);
-  if (!d_w || !topk_w || !topk_idx || !x || !Wr || !dx_acc || !dWr || !dx || !ws)
+  if (!dWr || !ws || (T > 0 && (!d_w || !topk_w || !topk_idx || !x || !Wr || !dx_acc || !dx)))
     return fail(MOE_ERR_INVALID_ARG, "moe_route_topk_bwd: NULL pointer argument");
   if (!aligned16(x) || !aligned16(Wr) || !aligned16(dx_acc) || !aligned16(dWr) || !aligned16(dx) ||
       !aligned16(ws))
