@@ -40,7 +40,7 @@ namespace tc {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int STAGES = 3;
+constexpr int STAGES = 4;
 constexpr int THREADS = 192;
 constexpr int A_BYTES = BM * BK * 2;          // 16 KiB
 constexpr int B_BYTES_MAX = 256 * BK * 2;     // 32 KiB
@@ -49,11 +49,11 @@ constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 512;
 constexpr int CHUNK_BYTES = 64 * BK * 2;      // one 64(MN) x 64(K) MN-major box: 8 KiB
 constexpr unsigned long long TIMEOUT_NS = 2000000000ull;
-// Epilogue staging: each epilogue warp owns a ring of 4 boxes of 32 rows x
+// Epilogue staging: each epilogue warp owns a ring of 2 boxes of 32 rows x
 // 64 bytes (32 bf16 or 16 fp32 columns), written in the 64-byte swizzle
 // pattern and sent to global memory by TMA bulk tensor stores.
 constexpr int EP_BOX_BYTES = 32 * 64;
-constexpr int EP_SLOTS = 4;
+constexpr int EP_SLOTS = 2;
 constexpr int EP_WARP_BYTES = EP_BOX_BYTES * EP_SLOTS;
 constexpr int EP_BYTES = 4 * EP_WARP_BYTES;
 
@@ -99,6 +99,7 @@ struct Ctl {
 };
 
 constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + EP_BYTES + sizeof(Ctl);
+static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA exceeded");
 
 // ------------------------------------------------------------- PTX wrappers
 
@@ -188,7 +189,7 @@ struct EpRing {
   int lane;
   __device__ __forceinline__ uint8_t* acquire() {
     // the store issued from this slot EP_SLOTS boxes ago must have read it
-    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
     __syncwarp();
     return base + slot * EP_BOX_BYTES;
   }
