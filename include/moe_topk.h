@@ -137,6 +137,30 @@ int moe_dispatch(const void* x, const int32_t* topk_idx, const int32_t* offsets,
                  int E, int k, void* x_perm, int32_t* row_of_slot, int32_t* token_of_row,
                  void* ws, size_t ws_bytes, void* stream);
 
+/* moe_dispatch without a workspace (the pages have no counterpart to this
+ * entry point; it is a convenience of this library).
+ *
+ * Same arguments, results and status reporting as moe_dispatch, minus the
+ * workspace.  It exists for callers that cannot allocate device memory for a
+ * workspace: code that runs under a fixed memory plan made at start-up (no
+ * device allocation allowed afterwards), or a thin C caller with no device
+ * allocator of its own.  Its scratch is a 1 MiB array built into the library;
+ * every GPU that loads the library holds it until the process exits.
+ *   - Limit: ceil(T/32) * E <= moe_dispatch_no_alloc_max_scratch() (262144),
+ *     e.g. T <= 65536 tokens at E = 128; larger sizes return
+ *     MOE_ERR_WORKSPACE without launching anything (use moe_dispatch).
+ *   - The first call on a device looks the array's device address up
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.  No call allocates or frees memory.
+ *   - All calls on a device share the array and each call rewrites every
+ *     entry it reads, so nothing carries over between calls; calls that
+ *     overlap on the GPU (e.g. on two streams) race and must be serialised.
+ */
+size_t moe_dispatch_no_alloc_max_scratch(void);
+int moe_dispatch_no_alloc(const void* x, const int32_t* topk_idx, const int32_t* offsets, int T,
+                          int H, int E, int k, void* x_perm, int32_t* row_of_slot,
+                          int32_t* token_of_row, void* stream);
+
 /* ------------------------------------------------------------------------
  * Segment tables (grouped GEMMs).  Rows [seg_offsets[s], seg_offsets[s+1])
  * of the grouped operand belong to expert seg_expert[s], or to expert s when

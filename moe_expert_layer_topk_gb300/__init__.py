@@ -18,7 +18,7 @@ import torch
 from . import build as _build_mod
 
 __all__ = ["lib", "MoEError", "LIB_PATH", "ENTRY_POINTS",
-           "moe_route_topk", "moe_dispatch", "moe_grouped_gemm_swiglu", "moe_grouped_gemm_down",
+           "moe_route_topk", "moe_dispatch", "moe_dispatch_no_alloc", "moe_grouped_gemm_swiglu", "moe_grouped_gemm_down",
            "moe_combine", "moe_combine_bwd", "moe_grouped_gemm_down_bwd",
            "moe_grouped_gemm_swiglu_bwd", "moe_dispatch_bwd", "moe_route_topk_bwd",
            "moe_route_topk_workspace_size", "moe_dispatch_workspace_size",
@@ -37,6 +37,8 @@ ENTRY_POINTS = {
     "moe_route_topk": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _Z, _P], _I),
     "moe_dispatch_workspace_size": ([_I, _I, _I], _Z),
     "moe_dispatch": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P], _I),
+    "moe_dispatch_no_alloc_max_scratch": ([], _Z),
+    "moe_dispatch_no_alloc": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
     "moe_grouped_gemm_swiglu": ([_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P], _I),
     "moe_grouped_gemm_down": ([_P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _P], _I),
     "moe_combine": ([_P, _P, _P, _I, _I, _I, _P, _P], _I),
@@ -138,6 +140,13 @@ def moe_dispatch(x, topk_idx, offsets, T, H, E, k, x_perm, row_of_slot, token_of
                  stream=None):
     _call("moe_dispatch", _ptr(x), _ptr(topk_idx), _ptr(offsets), T, H, E, k, _ptr(x_perm),
           _ptr(row_of_slot), _ptr(token_of_row), _ptr(ws), _nbytes(ws), _stream(stream))
+
+
+def moe_dispatch_no_alloc(x, topk_idx, offsets, T, H, E, k, x_perm, row_of_slot, token_of_row,
+                          stream=None):
+    """moe_dispatch with the library's built-in scratch instead of a workspace."""
+    _call("moe_dispatch_no_alloc", _ptr(x), _ptr(topk_idx), _ptr(offsets), T, H, E, k, _ptr(x_perm),
+          _ptr(row_of_slot), _ptr(token_of_row), _stream(stream))
 
 
 def moe_grouped_gemm_swiglu(x_perm, Wg, Wu, num_seg, seg_offsets, seg_expert, R, H, I, E, h,

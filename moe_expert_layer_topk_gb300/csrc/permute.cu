@@ -11,6 +11,8 @@
 // All four kernels are HBM-bound copies/reductions over 16-byte vectors
 // (8 bf16): every row is read and written with fully coalesced 16-byte
 // accesses, and each thread keeps all k of its independent loads in flight.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -393,6 +395,85 @@ int moe_combine_bwd(const void* dy, const void* y_perm, const float* topk_w,
                                        row_of_slot, T, H, k, T * k,
                                        static_cast<__nv_bfloat16*>(dy_perm), d_w, status_word());
   return check_launch("moe_combine_bwd");
+}
+
+// ------------------------------------------------- dispatch without workspace
+//
+// moe_dispatch_no_alloc runs the same three kernels as moe_dispatch, but its
+// per-chunk histogram / row-base scratch lives in the file-scope device array
+// below instead of a caller-provided workspace.  Every device that loads the
+// library holds this array (1 MiB) until the process exits; all calls on a
+// device share it, so calls that overlap on the GPU (other streams) race.
+// Nothing has to start at zero: each call rewrites every entry it reads.
+
+}  // extern "C"
+
+namespace {
+
+constexpr size_t kNoAllocScratchInts = 262144;  // 1 MiB of int32
+static __device__ __align__(256) int32_t g_dispatch_scratch[kNoAllocScratchInts];
+
+int32_t* g_dispatch_scratch_ptr[64] = {};
+std::mutex g_dispatch_scratch_mu;
+
+// Device address of g_dispatch_scratch on the current device, looked up once
+// per device (host code cannot use the symbol's name as a device pointer).
+int dispatch_scratch(int32_t** out) {
+  const int dev = current_device();
+  if (dev < 0) return fail(MOE_ERR_CUDA, "moe_dispatch_no_alloc: no current CUDA device");
+  std::lock_guard<std::mutex> lk(g_dispatch_scratch_mu);
+  if (!g_dispatch_scratch_ptr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(MOE_ERR_CUDA, "moe_dispatch_no_alloc: cudaGetSymbolAddress failed: %s",
+                  cudaGetErrorString(e));
+    }
+    g_dispatch_scratch_ptr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_dispatch_scratch_ptr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_dispatch_no_alloc_max_scratch(void) { return kNoAllocScratchInts; }
+
+int moe_dispatch_no_alloc(const void* x, const int32_t* topk_idx, const int32_t* offsets, int T,
+                          int H, int E, int k, void* x_perm, int32_t* row_of_slot,
+                          int32_t* token_of_row, void* stream) {
+  clear_error();
+  if (int rc = check_rows_args("moe_dispatch_no_alloc", T, H, k)) return rc;
+  if (E <= 0 || E > kMaxExperts || k > E)
+    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "moe_dispatch_no_alloc: need 1<=E<=1024, k<=E");
+  if (T > 0 && (!topk_idx || !offsets || !row_of_slot || !token_of_row || (x_perm && !x)))
+    return fail(MOE_ERR_INVALID_ARG, "moe_dispatch_no_alloc: NULL pointer argument");
+  if ((x && !aligned16(x)) || (x_perm && !aligned16(x_perm)))
+    return fail(MOE_ERR_ALIGNMENT, "moe_dispatch_no_alloc: x and x_perm must be 16-byte aligned");
+  const size_t nchunk = (size_t)((T + kChunkTok - 1) / kChunkTok);
+  if (nchunk * (size_t)E > kNoAllocScratchInts)
+    return fail(MOE_ERR_WORKSPACE,
+                "moe_dispatch_no_alloc: ceil(T/32)*E = %zu exceeds the built-in scratch of %zu "
+                "entries (use moe_dispatch with a workspace)",
+                nchunk * (size_t)E, kNoAllocScratchInts);
+  int32_t* chunk_base = nullptr;
+  if (int rc = dispatch_scratch(&chunk_base)) return rc;
+  if (T == 0) return MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* status = status_word();
+  const int nc = (int)nchunk;
+  chunk_hist_kernel<<<(nc + 7) / 8, 256, sizeof(int) * 8 * E, s>>>(topk_idx, T, E, k, nc,
+                                                                   chunk_base, status);
+  if (int rc = check_launch("moe_dispatch_no_alloc: histogram kernel")) return rc;
+  chunk_scan_kernel<<<(E + 7) / 8, 256, 0, s>>>(chunk_base, offsets, nc, E, status);
+  if (int rc = check_launch("moe_dispatch_no_alloc: scan kernel")) return rc;
+  dispatch_kernel<<<nc, 256, sizeof(int) * (E + kChunkTok * k), s>>>(
+      static_cast<const __nv_bfloat16*>(x), topk_idx, chunk_base, T, H, E, k,
+      static_cast<__nv_bfloat16*>(x_perm), row_of_slot, token_of_row, status);
+  return check_launch("moe_dispatch_no_alloc: row kernel");
 }
 
 }  // extern "C"
