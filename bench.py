@@ -377,6 +377,25 @@ def run_ours(args, shape, inp):
 KERNELS_PER_STEP = 3 + 3 + 1 + 1 + 1 + 1 + 2 + 2 + 1 + 6
 
 
+def run_profile_case(args):
+    """Untimed forward+backward passes of one layer shape (for ncu captures)."""
+    import torch
+
+    import moe_expert_layer_topk_gb300 as m
+    from moe_expert_layer_topk_gb300.synth import LayerShape, make_layer_inputs
+    T, H, I, E, k = (int(v) for v in args.profile_case.split(","))
+    shape = LayerShape(T=T, H=H, I=I, E=E, k=k, ep_size=1)
+    inp = make_layer_inputs(shape, 0, with_dy=True)
+    g = {n: (v.cuda() if isinstance(v, torch.Tensor) else v) for n, v in inp.items()}
+    layer = m.MoELayer(T, H, I, E, k, 1)
+    for _ in range(args.steps):
+        layer.forward(g["x"], g["Wr"], None, g["Wg"], g["Wu"], g["Wd"])
+        layer.backward(g["dy"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"])
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": [T, H, I, E, k], "passes": args.steps,
+                      "device_status": m.moe_read_device_status(reset=True)}))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -386,7 +405,11 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=8, help="oracle tokens per reference step")
     ap.add_argument("--cpu-tokens", type=int, default=48, help="oracle tokens for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--profile-case", default=None, metavar="T,H,I,E,k",
+                    help="run --steps untimed forward+backward passes of this shape and exit")
     args = ap.parse_args(argv)
+    if args.profile_case:
+        return run_profile_case(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     from moe_expert_layer_topk_gb300.synth import CONFIGS, make_layer_inputs
