@@ -40,11 +40,9 @@ namespace tc {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
 constexpr int THREADS = 192;
 constexpr int A_BYTES = BM * BK * 2;          // 16 KiB
 constexpr int B_BYTES_MAX = 256 * BK * 2;     // 32 KiB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES_MAX;
 constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 512;
 constexpr int CHUNK_BYTES = 64 * BK * 2;      // one 64(MN) x 64(K) MN-major box: 8 KiB
@@ -84,8 +82,8 @@ struct Params {
 };
 
 struct Ctl {
-  unsigned long long full[STAGES];
-  unsigned long long empty[STAGES];
+  unsigned long long full[6];
+  unsigned long long empty[6];
   unsigned long long tfull[2];
   unsigned long long tempty[2];
   unsigned long long drain;
@@ -98,8 +96,7 @@ struct Ctl {
   int grp_rows[kMaxSegments];       // DW: rows per output group
 };
 
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + EP_BYTES + sizeof(Ctl);
-static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA exceeded");
+
 
 // ------------------------------------------------------------- PTX wrappers
 
@@ -293,16 +290,31 @@ struct Traits {
   static constexpr bool rows = (KIND != DW);
 };
 
+// CTAS = 1: one CTA per 128-row tile, whole B tile in its shared memory.
+// CTAS = 2: a cluster pair per 256-row tile (tcgen05 cta_group::2): each CTA
+// holds its own 128 rows of A and half of the B tile's N range; the leader
+// (cluster rank 0) issues the MMAs, which read both CTAs' shared memory and
+// write each CTA's 128 accumulator rows into that CTA's TMEM.
+template <int CTAS>
+struct Cfg {
+  static constexpr int STAGES = CTAS == 1 ? 4 : 6;
+  static constexpr int B_BYTES = B_BYTES_MAX / CTAS;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TILE_M = BM * CTAS;
+  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + EP_BYTES + sizeof(Ctl);
+};
+static_assert(Cfg<1>::SMEM <= 232448 && Cfg<2>::SMEM <= 232448, "shared memory budget exceeded");
+
 struct Tile {
   int group;   // expert (row kinds) / output group (DW)
-  int m0;      // first row (row kinds: of A; DW: of the output)
-  int n0;      // first output column
+  int m0;      // this CTA's first row (row kinds: of A; DW: of the output)
+  int n0;      // first output column of the tile
   int row_end; // row kinds: end of the segment (exclusive)
   int seg;     // row kinds: segment index
 };
 
-template <int KIND>
-__device__ __forceinline__ Tile decode_tile(int tile, const Params& p, const Ctl* ctl) {
+template <int KIND, int CTAS>
+__device__ __forceinline__ Tile decode_tile(int tile, const Params& p, const Ctl* ctl, int rank) {
   Tile t;
   if constexpr (Traits<KIND>::rows) {
     const int gm = tile / p.n_tiles, nt = tile % p.n_tiles;
@@ -313,14 +325,14 @@ __device__ __forceinline__ Tile decode_tile(int tile, const Params& p, const Ctl
     }
     t.seg = lo;
     t.group = ctl->seg_exp[lo];
-    t.m0 = ctl->seg_off[lo] + (gm - ctl->seg_tiles[lo]) * BM;
+    t.m0 = ctl->seg_off[lo] + (gm - ctl->seg_tiles[lo]) * Cfg<CTAS>::TILE_M + BM * rank;
     t.row_end = ctl->seg_off[lo + 1];
     t.n0 = nt * (KIND == GATE_UP_FWD ? p.NH : p.BN);
   } else {
     const int per = p.m_tiles * p.n_tiles;
     t.group = tile / per;
     const int rem = tile % per;
-    t.m0 = (rem / p.n_tiles) * BM;
+    t.m0 = (rem / p.n_tiles) * Cfg<CTAS>::TILE_M + BM * rank;
     t.n0 = (rem % p.n_tiles) * p.BN;
     t.row_end = 0;
     t.seg = 0;
@@ -345,19 +357,110 @@ __device__ __forceinline__ void for_each_kblock(const Tile& t, const Params& p, 
   }
 }
 
-template <int KIND>
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// shared::cluster address of `local` (a shared::cta address) in CTA `rank`
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+template <int CTAS>
+__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
+  if constexpr (CTAS == 1) {
+    tma_load_2d(dst, map, bar, c0, c1);
+  } else {
+    // the mbarrier may live in the peer CTA (the leader's full barrier)
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+  }
+}
+
+template <int CTAS>
+__device__ __forceinline__ void mma_issue(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+  if constexpr (CTAS == 1) {
+    mma_bf16(d, a, b, idesc, accumulate);
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
+}
+
+// Commit previously issued MMAs to `bar` (in both CTAs of the pair for CTAS = 2).
+template <int CTAS>
+__device__ __forceinline__ void mma_commit_to(uint32_t bar) {
+  if constexpr (CTAS == 1) {
+    mma_commit(bar);
+  } else {
+    const uint16_t mask = 3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(mask)
+        : "memory");
+  }
+}
+
+template <int CTAS>
+__device__ __forceinline__ void tmem_alloc_n(uint32_t dst_smem, uint32_t ncols) {
+  if constexpr (CTAS == 1) {
+    tmem_alloc(dst_smem, ncols);
+    tmem_relinquish();
+  } else {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+}
+
+template <int CTAS>
+__device__ __forceinline__ void tmem_dealloc_n(uint32_t taddr, uint32_t ncols) {
+  if constexpr (CTAS == 1) {
+    tmem_dealloc(taddr, ncols);
+  } else {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+  }
+}
+
+template <int KIND, int CTAS>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB0,
                         const __grid_constant__ CUtensorMap tmB1,
                         const __grid_constant__ CUtensorMap tmO0,
                         const __grid_constant__ CUtensorMap tmO1, const Params p) {
+  using C = Cfg<CTAS>;
+  constexpr int STG = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + (size_t)STAGES * STAGE_BYTES + EP_BYTES);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + (size_t)STG * C::STAGE_BYTES + EP_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int limit = Traits<KIND>::rows ? p.M : p.K;  // rows addressable through the segment table
+  const int rank = CTAS == 2 ? (int)cluster_rank() : 0;
+  const bool leader = rank == 0;
+  const int unit = CTAS == 2 ? (int)blockIdx.x / 2 : (int)blockIdx.x;  // tile-processing unit
+  const int nunits = CTAS == 2 ? (int)gridDim.x / 2 : (int)gridDim.x;
 
   // ---- segment table -> shared memory (clamped; bad entries become empty)
   for (int s = threadIdx.x; s <= p.num_seg; s += THREADS) {
@@ -396,7 +499,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         int n = 0;
         if (s < p.num_seg && ctl->seg_exp[s] >= 0) {
           const int len = ctl->seg_off[s + 1] - ctl->seg_off[s];
-          n = len > 0 ? (len + BM - 1) / BM : 0;
+          n = len > 0 ? (len + C::TILE_M - 1) / C::TILE_M : 0;
         }
         int incl = n;
 #pragma unroll
@@ -415,13 +518,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) ctl->total_tiles = p.num_groups * p.m_tiles * p.n_tiles;
     }
     if (lane == 0) {
-      for (int i = 0; i < STAGES; ++i) {
+      for (int i = 0; i < STG; ++i) {
         mbar_init(smem_u32(&ctl->full[i]), 1);
         mbar_init(smem_u32(&ctl->empty[i]), 1);
       }
       for (int i = 0; i < 2; ++i) {
         mbar_init(smem_u32(&ctl->tfull[i]), 1);
-        mbar_init(smem_u32(&ctl->tempty[i]), 4);
+        mbar_init(smem_u32(&ctl->tempty[i]), 4 * CTAS);
       }
       mbar_init(smem_u32(&ctl->drain), 1);
       ctl->abort_flag = 0;
@@ -433,15 +536,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       prefetch_tmap(&tmO1);
     }
   } else if (warp == 1) {
-    tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_n<CTAS>(smem_u32(&ctl->tmem_base), TMEM_COLS);
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CTAS == 2) cluster_sync();  // peer barriers initialised before any remote signal
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
   const int total = ctl->total_tiles;
-  const uint32_t b_bytes = (uint32_t)p.BN * BK * 2;
+  const uint32_t b_bytes = (uint32_t)p.BN * BK * 2 / CTAS;  // this CTA's share of a B stage
 
   if (warp == 0) {
     // ============================ TMA producer ============================
@@ -449,42 +552,51 @@ __global__ void __launch_bounds__(THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const Tile t = decode_tile<KIND>(tile, p, ctl);
+      for (int tile = unit; ok && tile < total; tile += nunits) {
+        const Tile t = decode_tile<KIND, CTAS>(tile, p, ctl, rank);
         for_each_kblock<KIND>(t, p, ctl, [&](int row0, int) -> bool {
           if (!wait_bar(smem_u32(&ctl->empty[stage]), phase ^ 1u, ctl, p.status)) {
             ok = false;
             return false;
           }
-          const uint32_t fb = smem_u32(&ctl->full[stage]);
-          const uint32_t sA = smem_u32(smem + (size_t)stage * STAGE_BYTES);
+          const uint32_t fb_local = smem_u32(&ctl->full[stage]);
+          const uint32_t fb = CTAS == 2 ? map_to_rank(fb_local, 0) : fb_local;
+          const uint32_t sA = smem_u32(smem + (size_t)stage * C::STAGE_BYTES);
           const uint32_t sB = sA + A_BYTES;
-          mbar_arrive_expect_tx(fb, A_BYTES + b_bytes);
+          if (leader) mbar_arrive_expect_tx(fb_local, CTAS * (A_BYTES + b_bytes));
+          const int nck = p.BN / 64 / CTAS;  // MN-major B chunks of this CTA
+          const int ck0 = rank * nck;
           if constexpr (KIND == DW) {
-            tma_load_2d(sA, &tmA, fb, t.m0, row0);
-            tma_load_2d(sA + CHUNK_BYTES, &tmA, fb, t.m0 + 64, row0);
-            for (int c = 0; c < p.BN / 64; ++c)
-              tma_load_2d(sB + c * CHUNK_BYTES, &tmB0, fb, t.n0 + 64 * c, row0);
+            tma_load<CTAS>(sA, &tmA, fb, t.m0, row0);
+            tma_load<CTAS>(sA + CHUNK_BYTES, &tmA, fb, t.m0 + 64, row0);
+            for (int c = 0; c < nck; ++c)
+              tma_load<CTAS>(sB + c * CHUNK_BYTES, &tmB0, fb, t.n0 + 64 * (ck0 + c), row0);
           } else {
-            tma_load_2d(sA, &tmA, fb, row0, t.m0);
+            tma_load<CTAS>(sA, &tmA, fb, row0, t.m0);
             if constexpr (KIND == GATE_UP_FWD) {
               const int brow = t.group * p.b_group_rows + t.n0;
-              tma_load_2d(sB, &tmB0, fb, row0, brow);
-              tma_load_2d(sB + (uint32_t)p.NH * BK * 2, &tmB1, fb, row0, brow);
+              if (CTAS == 1) {
+                tma_load<CTAS>(sB, &tmB0, fb, row0, brow);
+                tma_load<CTAS>(sB + (uint32_t)p.NH * BK * 2, &tmB1, fb, row0, brow);
+              } else {
+                // pair: the leader holds the gate rows, the peer the up rows
+                tma_load<CTAS>(sB, rank == 0 ? &tmB0 : &tmB1, fb, row0, brow);
+              }
             } else if constexpr (KIND == DOWN_FWD || KIND == DENSE_ADD) {
-              tma_load_2d(sB, &tmB0, fb, row0, t.group * p.b_group_rows + t.n0);
+              tma_load<CTAS>(sB, &tmB0, fb, row0,
+                             t.group * p.b_group_rows + t.n0 + rank * (p.BN / CTAS));
             } else if constexpr (KIND == DOWN_BWD_DX) {
-              for (int c = 0; c < p.BN / 64; ++c)
-                tma_load_2d(sB + c * CHUNK_BYTES, &tmB0, fb, t.n0 + 64 * c,
-                            t.group * p.b_group_rows + row0);
+              for (int c = 0; c < nck; ++c)
+                tma_load<CTAS>(sB + c * CHUNK_BYTES, &tmB0, fb, t.n0 + 64 * (ck0 + c),
+                               t.group * p.b_group_rows + row0);
             } else {  // GATE_UP_BWD_DX: k < I from Wg, k >= I from Wu
               const bool up = row0 >= p.I;
               const int krow = t.group * p.b_group_rows + (up ? row0 - p.I : row0);
-              for (int c = 0; c < p.BN / 64; ++c)
-                tma_load_2d(sB + c * CHUNK_BYTES, up ? &tmB1 : &tmB0, fb, t.n0 + 64 * c, krow);
+              for (int c = 0; c < nck; ++c)
+                tma_load<CTAS>(sB + c * CHUNK_BYTES, up ? &tmB1 : &tmB0, fb, t.n0 + 64 * (ck0 + c), krow);
             }
           }
-          if (++stage == STAGES) {
+          if (++stage == STG) {
             stage = 0;
             phase ^= 1u;
           }
@@ -494,90 +606,113 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 1) {
     // ============================ MMA issuer ==============================
-    int stage = 0;
-    uint32_t phase = 0;
-    int local = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++local) {
-      const Tile t = decode_tile<KIND>(tile, p, ctl);
-      const int buf = local & 1;
-      const uint32_t use = (uint32_t)(local >> 1);
-      if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&ctl->tempty[buf]), (use & 1u) ^ 1u, ctl, p.status))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t d = tmem_base + (uint32_t)(buf * ACC_COLS);
-      int nk = 0;
-      for_each_kblock<KIND>(t, p, ctl, [&](int, int valid) -> bool {
-        if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&ctl->full[stage]), phase, ctl, p.status))) {
+    // (CTAS = 2: only the leader issues; the peer's warp 1 just owns its TMEM)
+    if (CTAS == 1 || leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int tile = unit; ok && tile < total; tile += nunits, ++local) {
+        const Tile t = decode_tile<KIND, CTAS>(tile, p, ctl, rank);
+        const int buf = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&ctl->tempty[buf]), (use & 1u) ^ 1u, ctl, p.status))) {
           ok = false;
-          return false;
-        }
-        uint8_t* sA = smem + (size_t)stage * STAGE_BYTES;
-        uint8_t* sB = sA + A_BYTES;
-        int nkk = BK / 16;
-        if (KIND == DW && valid < BK) {
-          // Rows past the segment end belong to another group.  Only the
-          // 16-row MMA steps that hold valid rows are issued; inside the last
-          // of them the rows [valid, 16*nkk) are zeroed in both operands
-          // (each K row is one 128-byte line of every 64-wide chunk).
-          nkk = (valid + 15) / 16;
-          const int a_chunks = 2, b_chunks = p.BN / 64;
-          const int nrows = nkk * 16 - valid;
-          const int units = (a_chunks + b_chunks) * nrows * 8;
-          for (int u = lane; u < units; u += 32) {
-            const int chunk = u / (nrows * 8);
-            const int rem = u % (nrows * 8);
-            const int r = valid + rem / 8, c16 = rem % 8;
-            uint8_t* base = chunk < a_chunks ? sA + chunk * CHUNK_BYTES
-                                             : sB + (chunk - a_chunks) * CHUNK_BYTES;
-            *reinterpret_cast<uint4*>(base + r * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
-          }
-          if (nrows > 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
+          break;
         }
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            if (kk >= nkk) break;
-            const uint64_t ad = Traits<KIND>::a_mn ? sdesc(a0 + kk * 2048, CHUNK_BYTES, 1024)
-                                                   : sdesc(a0 + kk * 32, 16, 1024);
-            const uint64_t bd = Traits<KIND>::b_mn ? sdesc(b0 + kk * 2048, CHUNK_BYTES, 1024)
-                                                   : sdesc(b0 + kk * 32, 16, 1024);
-            mma_bf16(d, ad, bd, p.idesc, (nk > 0 || kk > 0) ? 1u : 0u);
+        const uint32_t d = tmem_base + (uint32_t)(buf * ACC_COLS);
+        int nk = 0;
+        for_each_kblock<KIND>(t, p, ctl, [&](int, int valid) -> bool {
+          if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&ctl->full[stage]), phase, ctl, p.status))) {
+            ok = false;
+            return false;
           }
-          mma_commit(smem_u32(&ctl->empty[stage]));
-        }
+          uint8_t* sA = smem + (size_t)stage * C::STAGE_BYTES;
+          uint8_t* sB = sA + A_BYTES;
+          int nkk = BK / 16;
+          if (KIND == DW && valid < BK) {
+            // Rows past the segment end belong to another group.  Only the
+            // 16-row MMA steps that hold valid rows are issued; inside the
+            // last of them the rows [valid, 16*nkk) are zeroed.  One CTA
+            // zeroes them in both operands; a pair zeroes them in A only, in
+            // both CTAs (a zero A row cancels whatever B holds there).
+            nkk = (valid + 15) / 16;
+            const int nrows = nkk * 16 - valid;
+            if (CTAS == 1) {
+              const int a_chunks = 2, b_chunks = p.BN / 64;
+              const int units = (a_chunks + b_chunks) * nrows * 8;
+              for (int u = lane; u < units; u += 32) {
+                const int chunk = u / (nrows * 8);
+                const int rem = u % (nrows * 8);
+                const int r = valid + rem / 8, c16 = rem % 8;
+                uint8_t* base = chunk < a_chunks ? sA + chunk * CHUNK_BYTES
+                                                 : sB + (chunk - a_chunks) * CHUNK_BYTES;
+                *reinterpret_cast<uint4*>(base + r * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
+              }
+              if (nrows > 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            } else {
+              const int units = 2 /*CTAs*/ * 2 /*A chunks*/ * nrows * 8;
+              for (int u = lane; u < units; u += 32) {
+                const int cta = u / (2 * nrows * 8);
+                const int rem0 = u % (2 * nrows * 8);
+                const int chunk = rem0 / (nrows * 8);
+                const int rem = rem0 % (nrows * 8);
+                const int r = valid + rem / 8, c16 = rem % 8;
+                const uint32_t local_addr = smem_u32(sA + chunk * CHUNK_BYTES + r * 128 + c16 * 16);
+                const uint32_t addr = map_to_rank(local_addr, (uint32_t)cta);
+                asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0)
+                             : "memory");
+              }
+              if (nrows > 0) asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+            }
+            __syncwarp();
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              if (kk >= nkk) break;
+              const uint64_t ad = Traits<KIND>::a_mn ? sdesc(a0 + kk * 2048, CHUNK_BYTES, 1024)
+                                                     : sdesc(a0 + kk * 32, 16, 1024);
+              const uint64_t bd = Traits<KIND>::b_mn ? sdesc(b0 + kk * 2048, CHUNK_BYTES, 1024)
+                                                     : sdesc(b0 + kk * 32, 16, 1024);
+              mma_issue<CTAS>(d, ad, bd, p.idesc, (nk > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit_to<CTAS>(smem_u32(&ctl->empty[stage]));
+          }
+          __syncwarp();
+          ++nk;
+          if (++stage == STG) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          return true;
+        });
+        if (!ok) break;
+        if (lane == 0) mma_commit_to<CTAS>(smem_u32(&ctl->tfull[buf]));
         __syncwarp();
-        ++nk;
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
+      }
+      if (!ok) {
+        // drain MMAs still in flight before TMEM is released
+        if (lane == 0) mma_commit_to<CTAS>(smem_u32(&ctl->drain));
+        __syncwarp();
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(smem_u32(&ctl->drain), 0) && globaltimer() - t0 < TIMEOUT_NS) {
         }
-        return true;
-      });
-      if (!ok) break;
-      if (lane == 0) mma_commit(smem_u32(&ctl->tfull[buf]));
-      __syncwarp();
-    }
-    if (!ok) {
-      // drain MMAs still in flight before TMEM is released
-      if (lane == 0) mma_commit(smem_u32(&ctl->drain));
-      __syncwarp();
-      const unsigned long long t0 = globaltimer();
-      while (!mbar_try_wait(smem_u32(&ctl->drain), 0) && globaltimer() - t0 < TIMEOUT_NS) {
       }
     }
   } else {
     // ============================ epilogue ================================
     const int q = warp & 3;
-    EpRing ring{smem + (size_t)STAGES * STAGE_BYTES + (size_t)(warp - 2) * EP_WARP_BYTES, 0, lane};
+    EpRing ring{smem + (size_t)STG * C::STAGE_BYTES + (size_t)(warp - 2) * EP_WARP_BYTES, 0, lane};
+    const uint32_t tempty_leader[2] = {
+        CTAS == 2 ? map_to_rank(smem_u32(&ctl->tempty[0]), 0) : smem_u32(&ctl->tempty[0]),
+        CTAS == 2 ? map_to_rank(smem_u32(&ctl->tempty[1]), 0) : smem_u32(&ctl->tempty[1])};
     int local = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
-      const Tile t = decode_tile<KIND>(tile, p, ctl);
+    for (int tile = unit; tile < total; tile += nunits, ++local) {
+      const Tile t = decode_tile<KIND, CTAS>(tile, p, ctl, rank);
       const int buf = local & 1;
       const uint32_t use = (uint32_t)(local >> 1);
       // this warp's 32 rows: full boxes go out through TMA stores, a box that
@@ -778,16 +913,24 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[buf]));
+      if (lane == 0) {
+        if (CTAS == 1)
+          mbar_arrive(tempty_leader[buf]);
+        else
+          asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                           tempty_leader[buf])
+                       : "memory");
+      }
     }
     ring.drain();
   }
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (CTAS == 2) cluster_sync();  // neither CTA frees TMEM while the pair still uses it
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_n<CTAS>(tmem_base, TMEM_COLS);
   }
 }
 
@@ -842,36 +985,74 @@ int make_out_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer
   return make_tmap(m, ptr, inner, outer, fp32 ? 16 : 32, 32, fp32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-uint32_t make_idesc(int n, bool a_mn, bool b_mn) {
+uint32_t make_idesc(int n, int m, bool a_mn, bool b_mn) {
   return (1u << 4)                    // D fp32
          | (1u << 7) | (1u << 10)     // A, B bf16
          | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
          ((uint32_t)(n >> 3) << 17)   // N / 8
-         | ((uint32_t)(BM >> 4) << 24);  // M / 16
+         | ((uint32_t)(m >> 4) << 24);  // M / 16
 }
 
 int pick_bn(int n) { return n % 256 == 0 ? 256 : (n % 128 == 0 ? 128 : 64); }
 
-bool g_attr[6][64] = {};
+// Tiles at least 128 columns wide run as cluster pairs (256-row tiles).
+bool use_pair(int bn) { return bn >= 128; }
 
-template <int KIND>
-int launch(const Params& p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-           const CUtensorMap& o0, const CUtensorMap& o1, int upper_tiles, cudaStream_t s,
-           const char* what) {
+bool g_attr[6][2][64] = {};
+
+// Launches grouped_gemm_kernel<KIND, CTAS>: completes the CTAS-dependent
+// parameters, sizes the persistent grid to the SM count and, for pairs, sets
+// the cluster dimension.
+template <int KIND, int CTAS>
+int launch(Params p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+           const CUtensorMap& o0, const CUtensorMap& o1, cudaStream_t s, const char* what) {
+  constexpr bool a_mn = KIND == DW;
+  constexpr bool b_mn = KIND == DOWN_BWD_DX || KIND == GATE_UP_BWD_DX || KIND == DW;
+  p.idesc = make_idesc(p.BN, BM * CTAS, a_mn, b_mn);
+  long long upper;
+  if (KIND == DW) {
+    upper = (long long)p.num_groups * p.m_tiles * p.n_tiles;
+  } else {
+    upper = ((long long)(p.M + BM * CTAS - 1) / (BM * CTAS) + p.num_seg) * p.n_tiles;
+  }
   const int dev = current_device();
   if (dev < 0) return fail(MOE_ERR_CUDA, "%s: no current CUDA device", what);
-  if (!g_attr[KIND][dev]) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<KIND>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+  auto kern = grouped_gemm_kernel<KIND, CTAS>;
+  const int smem = (int)Cfg<CTAS>::SMEM;
+  if (!g_attr[KIND][CTAS - 1][dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
-    g_attr[KIND][dev] = true;
+    g_attr[KIND][CTAS - 1][dev] = true;
   }
   const int sms = sm_count();
   if (sms <= 0) return fail(MOE_ERR_CUDA, "%s: cannot query the SM count", what);
-  int grid = upper_tiles < sms ? upper_tiles : sms;
-  if (grid < 1) grid = 1;
-  grouped_gemm_kernel<KIND><<<grid, THREADS, SMEM_BYTES, s>>>(a, b0, b1, o0, o1, p);
+  const long long units_max = sms / CTAS;
+  long long units = upper < units_max ? upper : units_max;
+  if (units < 1) units = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(units * CTAS));
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (CTAS == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, b0, b1, o0, o1, p);
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
   return check_launch(what);
+}
+
+template <int KIND>
+int run(bool pair, const Params& p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+        const CUtensorMap& o0, const CUtensorMap& o1, cudaStream_t s, const char* what) {
+  return pair ? launch<KIND, 2>(p, a, b0, b1, o0, o1, s, what)
+              : launch<KIND, 1>(p, a, b0, b1, o0, o1, s, what);
 }
 
 int check_grouped(const char* fn, int num_seg, const int32_t* seg_offsets, int R, int H, int I, int E) {
@@ -894,9 +1075,6 @@ Params base_params(int num_seg, const int32_t* so, const int32_t* se, int groups
   return p;
 }
 
-int row_tiles_upper(int R, int num_seg, int n_tiles) {
-  return (int)(((long long)(R + BM - 1) / BM + num_seg) * n_tiles);
-}
 
 }  // namespace tc
 
@@ -914,16 +1092,15 @@ int launch_dense_add_bf16(const void* A, const void* B, const float* add, void* 
   p.n_tiles = N / p.BN;
   p.b_group_rows = 0;
   p.ldo = N;
-  p.idesc = make_idesc(p.BN, false, false);
   p.out0 = out;
   p.aux = add;
   CUtensorMap ta, tb;
   if (int rc = make_tmap(&ta, A, K, M, 64, BM)) return rc;
-  if (int rc = make_tmap(&tb, B, K, N, 64, p.BN)) return rc;
+  const bool pair = use_pair(p.BN);
+  if (int rc = make_tmap(&tb, B, K, N, 64, p.BN / (pair ? 2 : 1))) return rc;
   CUtensorMap to;
   if (int rc = make_out_map(&to, out, N, M, false)) return rc;
-  return launch<DENSE_ADD>(p, ta, tb, tb, to, to, row_tiles_upper(M, 1, p.n_tiles), stream,
-                           "router backward dx GEMM");
+  return run<DENSE_ADD>(pair, p, ta, tb, tb, to, to, stream, "router backward dx GEMM");
 }
 
 int launch_dw_split(const void* A, const void* B, int K_rows, int M, int N,
@@ -937,15 +1114,13 @@ int launch_dw_split(const void* A, const void* B, int K_rows, int M, int N,
   p.n_tiles = N / p.BN;
   p.m_tiles = (M + BM - 1) / BM;
   p.ldo = N;
-  p.idesc = make_idesc(p.BN, true, true);
   p.out0 = out;
   CUtensorMap ta, tb;
   if (int rc = make_tmap(&ta, A, M, K_rows, 64, 64)) return rc;
   if (int rc = make_tmap(&tb, B, N, K_rows, 64, 64)) return rc;
   CUtensorMap to;
   if (int rc = make_out_map(&to, out, N, (uint64_t)num_seg * M, true)) return rc;
-  return launch<DW>(p, ta, tb, tb, to, to, num_seg * p.m_tiles * p.n_tiles, stream,
-                    "router backward dWr GEMM");
+  return run<DW>(use_pair(p.BN), p, ta, tb, tb, to, to, stream, "router backward dWr GEMM");
 }
 
 }  // namespace moe
@@ -977,7 +1152,6 @@ int moe_grouped_gemm_swiglu(const void* x_perm, const void* Wg, const void* Wu, 
   p.n_tiles = I / p.NH;
   p.b_group_rows = I;
   p.I = I;
-  p.idesc = make_idesc(p.BN, false, false);
   p.out0 = h;
   p.out1 = gu_save;
   CUtensorMap ta, tg, tu;
@@ -987,8 +1161,7 @@ int moe_grouped_gemm_swiglu(const void* x_perm, const void* Wg, const void* Wu, 
   CUtensorMap th, tgu;
   if (int rc = make_out_map(&th, h, I, R, false)) return rc;
   if (int rc = make_out_map(&tgu, gu_save ? gu_save : h, gu_save ? 2 * I : I, R, false)) return rc;
-  return launch<GATE_UP_FWD>(p, ta, tg, tu, th, tgu, row_tiles_upper(R, num_seg, p.n_tiles),
-                             static_cast<cudaStream_t>(stream), fn);
+  return run<GATE_UP_FWD>(use_pair(p.BN), p, ta, tg, tu, th, tgu, static_cast<cudaStream_t>(stream), fn);
 }
 
 int moe_grouped_gemm_down(const void* h, const void* Wd, int num_seg, const int32_t* seg_offsets,
@@ -1010,15 +1183,14 @@ int moe_grouped_gemm_down(const void* h, const void* Wd, int num_seg, const int3
   p.n_tiles = H / p.BN;
   p.b_group_rows = H;
   p.ldo = H;
-  p.idesc = make_idesc(p.BN, false, false);
   p.out0 = y_perm;
   CUtensorMap ta, tb;
   if (int rc = make_tmap(&ta, h, I, R, 64, BM)) return rc;
-  if (int rc = make_tmap(&tb, Wd, I, (uint64_t)E * H, 64, p.BN)) return rc;
+  const bool pair = use_pair(p.BN);
+  if (int rc = make_tmap(&tb, Wd, I, (uint64_t)E * H, 64, p.BN / (pair ? 2 : 1))) return rc;
   CUtensorMap to;
   if (int rc = make_out_map(&to, y_perm, H, R, false)) return rc;
-  return launch<DOWN_FWD>(p, ta, tb, tb, to, to, row_tiles_upper(R, num_seg, p.n_tiles),
-                          static_cast<cudaStream_t>(stream), fn);
+  return run<DOWN_FWD>(pair, p, ta, tb, tb, to, to, static_cast<cudaStream_t>(stream), fn);
 }
 
 int moe_grouped_gemm_down_bwd(const void* dy_perm, const void* h, const void* gu_save,
@@ -1045,7 +1217,6 @@ int moe_grouped_gemm_down_bwd(const void* dy_perm, const void* h, const void* gu
     p.n_tiles = I / p.BN;
     p.b_group_rows = H;
     p.I = I;
-    p.idesc = make_idesc(p.BN, false, true);
     p.out0 = dgu;
     p.aux = gu_save;
     CUtensorMap ta, tb;
@@ -1053,7 +1224,7 @@ int moe_grouped_gemm_down_bwd(const void* dy_perm, const void* h, const void* gu
     if (int rc = make_tmap(&tb, Wd, I, (uint64_t)E * H, 64, 64)) return rc;
     CUtensorMap to;
     if (int rc = make_out_map(&to, dgu, 2 * I, R, false)) return rc;
-    if (int rc = launch<DOWN_BWD_DX>(p, ta, tb, tb, to, to, row_tiles_upper(R, num_seg, p.n_tiles), s, fn))
+    if (int rc = run<DOWN_BWD_DX>(use_pair(p.BN), p, ta, tb, tb, to, to, s, fn))
       return rc;
   }
   // dWd[e] = dy_perm[rows of e]^T . h[rows of e]
@@ -1070,7 +1241,6 @@ int moe_grouped_gemm_down_bwd(const void* dy_perm, const void* h, const void* gu
   p.n_tiles = I / p.BN;
   p.m_tiles = (H + BM - 1) / BM;
   p.ldo = I;
-  p.idesc = make_idesc(p.BN, true, true);
   p.accumulate = accumulate;
   p.out0 = dWd;
   CUtensorMap ta, tb;
@@ -1078,7 +1248,7 @@ int moe_grouped_gemm_down_bwd(const void* dy_perm, const void* h, const void* gu
   if (int rc = make_tmap(&tb, h, I, R, 64, 64)) return rc;
   CUtensorMap to;
   if (int rc = make_out_map(&to, dWd, I, (uint64_t)E * H, true)) return rc;
-  return launch<DW>(p, ta, tb, tb, to, to, E * p.m_tiles * p.n_tiles, s, fn);
+  return run<DW>(use_pair(p.BN), p, ta, tb, tb, to, to, s, fn);
 }
 
 int moe_grouped_gemm_swiglu_bwd(const void* dgu, const void* x_perm, const void* Wg,
@@ -1107,7 +1277,6 @@ int moe_grouped_gemm_swiglu_bwd(const void* dgu, const void* x_perm, const void*
     p.b_group_rows = I;
     p.I = I;
     p.ldo = H;
-    p.idesc = make_idesc(p.BN, false, true);
     p.out0 = dx_perm;
     CUtensorMap ta, tg, tu;
     if (int rc = make_tmap(&ta, dgu, 2 * I, R, 64, BM)) return rc;
@@ -1115,7 +1284,7 @@ int moe_grouped_gemm_swiglu_bwd(const void* dgu, const void* x_perm, const void*
     if (int rc = make_tmap(&tu, Wu, H, (uint64_t)E * I, 64, 64)) return rc;
     CUtensorMap to;
     if (int rc = make_out_map(&to, dx_perm, H, R, false)) return rc;
-    if (int rc = launch<GATE_UP_BWD_DX>(p, ta, tg, tu, to, to, row_tiles_upper(R, num_seg, p.n_tiles), s, fn))
+    if (int rc = run<GATE_UP_BWD_DX>(use_pair(p.BN), p, ta, tg, tu, to, to, s, fn))
       return rc;
   }
   if (num_seg == 0) {
@@ -1134,7 +1303,6 @@ int moe_grouped_gemm_swiglu_bwd(const void* dgu, const void* x_perm, const void*
   p.m_tiles = (2 * I + BM - 1) / BM;
   p.split_m = I;
   p.ldo = H;
-  p.idesc = make_idesc(p.BN, true, true);
   p.accumulate = accumulate;
   p.out0 = dWg;
   p.out1 = dWu;
@@ -1144,7 +1312,7 @@ int moe_grouped_gemm_swiglu_bwd(const void* dgu, const void* x_perm, const void*
   CUtensorMap tog, tou;
   if (int rc = make_out_map(&tog, dWg, H, (uint64_t)E * I, true)) return rc;
   if (int rc = make_out_map(&tou, dWu, H, (uint64_t)E * I, true)) return rc;
-  return launch<DW>(p, ta, tb, tb, tog, tou, E * p.m_tiles * p.n_tiles, s, fn);
+  return run<DW>(use_pair(p.BN), p, ta, tb, tb, tog, tou, s, fn);
 }
 
 }  // extern "C"
