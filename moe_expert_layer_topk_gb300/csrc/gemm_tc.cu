@@ -164,6 +164,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
@@ -347,6 +356,12 @@ __device__ __forceinline__ void for_each_kblock(const Tile& t, const Params& p, 
     const int nkb = p.K / BK;
     for (int kb = 0; kb < nkb; ++kb)
       if (!f(kb * BK, BK)) return;
+  } else if (p.seg_expert == nullptr) {
+    // identity table: group g owns exactly segment g
+    const int a = ctl->seg_off[t.group], b = ctl->seg_off[t.group + 1];
+    if (ctl->seg_exp[t.group] >= 0)
+      for (int r = a; r < b; r += BK)
+        if (!f(r, min(BK, b - r))) return;
   } else {
     for (int s = 0; s < p.num_seg; ++s) {
       if (ctl->seg_exp[s] != t.group) continue;
@@ -385,6 +400,22 @@ __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, u
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+  }
+}
+
+// MN-major operand stage: one 3-D box {64 elements, 64 K rows, nchunks} whose
+// chunks land 8 KiB apart, i.e. the canonical MN-major layout with LBO = 8 KiB.
+template <int CTAS>
+__device__ __forceinline__ void tma_load_mn(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int krow, int chunk0) {
+  if constexpr (CTAS == 1) {
+    tma_load_3d(dst, map, bar, 0, krow, chunk0);
+  } else {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(0), "r"(krow), "r"(chunk0)
         : "memory");
   }
 }
@@ -564,13 +595,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t sA = smem_u32(smem + (size_t)stage * C::STAGE_BYTES);
           const uint32_t sB = sA + A_BYTES;
           if (leader) mbar_arrive_expect_tx(fb_local, CTAS * (A_BYTES + b_bytes));
-          const int nck = p.BN / 64 / CTAS;  // MN-major B chunks of this CTA
-          const int ck0 = rank * nck;
+          const int ck0 = rank * (p.BN / 64 / CTAS);  // first MN-major B chunk of this CTA
           if constexpr (KIND == DW) {
-            tma_load<CTAS>(sA, &tmA, fb, t.m0, row0);
-            tma_load<CTAS>(sA + CHUNK_BYTES, &tmA, fb, t.m0 + 64, row0);
-            for (int c = 0; c < nck; ++c)
-              tma_load<CTAS>(sB + c * CHUNK_BYTES, &tmB0, fb, t.n0 + 64 * (ck0 + c), row0);
+            tma_load_mn<CTAS>(sA, &tmA, fb, row0, t.m0 / 64);
+            tma_load_mn<CTAS>(sB, &tmB0, fb, row0, t.n0 / 64 + ck0);
           } else {
             tma_load<CTAS>(sA, &tmA, fb, row0, t.m0);
             if constexpr (KIND == GATE_UP_FWD) {
@@ -586,14 +614,11 @@ __global__ void __launch_bounds__(THREADS, 1)
               tma_load<CTAS>(sB, &tmB0, fb, row0,
                              t.group * p.b_group_rows + t.n0 + rank * (p.BN / CTAS));
             } else if constexpr (KIND == DOWN_BWD_DX) {
-              for (int c = 0; c < nck; ++c)
-                tma_load<CTAS>(sB + c * CHUNK_BYTES, &tmB0, fb, t.n0 + 64 * (ck0 + c),
-                               t.group * p.b_group_rows + row0);
+              tma_load_mn<CTAS>(sB, &tmB0, fb, t.group * p.b_group_rows + row0, t.n0 / 64 + ck0);
             } else {  // GATE_UP_BWD_DX: k < I from Wg, k >= I from Wu
               const bool up = row0 >= p.I;
               const int krow = t.group * p.b_group_rows + (up ? row0 - p.I : row0);
-              for (int c = 0; c < nck; ++c)
-                tma_load<CTAS>(sB + c * CHUNK_BYTES, up ? &tmB1 : &tmB0, fb, t.n0 + 64 * (ck0 + c), krow);
+              tma_load_mn<CTAS>(sB, up ? &tmB1 : &tmB0, fb, krow, t.n0 / 64 + ck0);
             }
           }
           if (++stage == STG) {
@@ -980,6 +1005,25 @@ int make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
   return MOE_OK;
 }
 
+// MN-major operand map: the bf16 tensor [rows, cols] seen as 3-D
+// {64 columns, rows, cols/64 chunks} (strides: row pitch, 128 B), box
+// {64, 64 rows, nck chunks}: one load fills nck 8 KiB chunks of a stage.
+int make_tmap_mn(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t nck) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {64, rows > 0 ? rows : 1, cols / 64};
+  cuuint64_t strides[2] = {cols * 2, 128};
+  cuuint32_t box[3] = {64, 64, nck};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed (%d) for [%llu x %llu] x %u chunks",
+                (int)r, (unsigned long long)rows, (unsigned long long)cols, nck);
+  return MOE_OK;
+}
+
 // Output map: 32 rows x 64 bytes per box (32 bf16 / 16 fp32 columns).
 int make_out_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, bool fp32) {
   return make_tmap(m, ptr, inner, outer, fp32 ? 16 : 32, 32, fp32, CU_TENSOR_MAP_SWIZZLE_64B);
@@ -995,8 +1039,12 @@ uint32_t make_idesc(int n, int m, bool a_mn, bool b_mn) {
 
 int pick_bn(int n) { return n % 256 == 0 ? 256 : (n % 128 == 0 ? 128 : 64); }
 
-// Tiles at least 128 columns wide run as cluster pairs (256-row tiles).
+// Cluster pairs (256-row tiles) pay off where they were measured faster: the
+// gate/up backward dX GEMM (K = 2I, MN-major B).  Other kinds run one CTA
+// per 128-row tile.
 bool use_pair(int bn) { return bn >= 128; }
+template <int KIND>
+bool pair_for(int bn) { return KIND == GATE_UP_BWD_DX && use_pair(bn); }
 
 bool g_attr[6][2][64] = {};
 
@@ -1096,11 +1144,10 @@ int launch_dense_add_bf16(const void* A, const void* B, const float* add, void* 
   p.aux = add;
   CUtensorMap ta, tb;
   if (int rc = make_tmap(&ta, A, K, M, 64, BM)) return rc;
-  const bool pair = use_pair(p.BN);
-  if (int rc = make_tmap(&tb, B, K, N, 64, p.BN / (pair ? 2 : 1))) return rc;
+  if (int rc = make_tmap(&tb, B, K, N, 64, p.BN)) return rc;
   CUtensorMap to;
   if (int rc = make_out_map(&to, out, N, M, false)) return rc;
-  return run<DENSE_ADD>(pair, p, ta, tb, tb, to, to, stream, "router backward dx GEMM");
+  return run<DENSE_ADD>(false, p, ta, tb, tb, to, to, stream, "router backward dx GEMM");
 }
 
 int launch_dw_split(const void* A, const void* B, int K_rows, int M, int N,
@@ -1116,11 +1163,11 @@ int launch_dw_split(const void* A, const void* B, int K_rows, int M, int N,
   p.ldo = N;
   p.out0 = out;
   CUtensorMap ta, tb;
-  if (int rc = make_tmap(&ta, A, M, K_rows, 64, 64)) return rc;
-  if (int rc = make_tmap(&tb, B, N, K_rows, 64, 64)) return rc;
+  if (int rc = make_tmap_mn(&ta, A, M, K_rows, BM / 64)) return rc;
+  if (int rc = make_tmap_mn(&tb, B, N, K_rows, p.BN / 64)) return rc;
   CUtensorMap to;
   if (int rc = make_out_map(&to, out, N, (uint64_t)num_seg * M, true)) return rc;
-  return run<DW>(use_pair(p.BN), p, ta, tb, tb, to, to, stream, "router backward dWr GEMM");
+  return run<DW>(false, p, ta, tb, tb, to, to, stream, "router backward dWr GEMM");
 }
 
 }  // namespace moe
@@ -1161,7 +1208,7 @@ int moe_grouped_gemm_swiglu(const void* x_perm, const void* Wg, const void* Wu, 
   CUtensorMap th, tgu;
   if (int rc = make_out_map(&th, h, I, R, false)) return rc;
   if (int rc = make_out_map(&tgu, gu_save ? gu_save : h, gu_save ? 2 * I : I, R, false)) return rc;
-  return run<GATE_UP_FWD>(use_pair(p.BN), p, ta, tg, tu, th, tgu, static_cast<cudaStream_t>(stream), fn);
+  return run<GATE_UP_FWD>(false, p, ta, tg, tu, th, tgu, static_cast<cudaStream_t>(stream), fn);
 }
 
 int moe_grouped_gemm_down(const void* h, const void* Wd, int num_seg, const int32_t* seg_offsets,
@@ -1186,8 +1233,8 @@ int moe_grouped_gemm_down(const void* h, const void* Wd, int num_seg, const int3
   p.out0 = y_perm;
   CUtensorMap ta, tb;
   if (int rc = make_tmap(&ta, h, I, R, 64, BM)) return rc;
-  const bool pair = use_pair(p.BN);
-  if (int rc = make_tmap(&tb, Wd, I, (uint64_t)E * H, 64, p.BN / (pair ? 2 : 1))) return rc;
+  const bool pair = false;
+  if (int rc = make_tmap(&tb, Wd, I, (uint64_t)E * H, 64, p.BN)) return rc;
   CUtensorMap to;
   if (int rc = make_out_map(&to, y_perm, H, R, false)) return rc;
   return run<DOWN_FWD>(pair, p, ta, tb, tb, to, to, static_cast<cudaStream_t>(stream), fn);
@@ -1221,10 +1268,10 @@ int moe_grouped_gemm_down_bwd(const void* dy_perm, const void* h, const void* gu
     p.aux = gu_save;
     CUtensorMap ta, tb;
     if (int rc = make_tmap(&ta, dy_perm, H, R, 64, BM)) return rc;
-    if (int rc = make_tmap(&tb, Wd, I, (uint64_t)E * H, 64, 64)) return rc;
+    if (int rc = make_tmap_mn(&tb, Wd, I, (uint64_t)E * H, p.BN / 64)) return rc;
     CUtensorMap to;
     if (int rc = make_out_map(&to, dgu, 2 * I, R, false)) return rc;
-    if (int rc = run<DOWN_BWD_DX>(use_pair(p.BN), p, ta, tb, tb, to, to, s, fn))
+    if (int rc = run<DOWN_BWD_DX>(false, p, ta, tb, tb, to, to, s, fn))
       return rc;
   }
   // dWd[e] = dy_perm[rows of e]^T . h[rows of e]
@@ -1244,11 +1291,11 @@ int moe_grouped_gemm_down_bwd(const void* dy_perm, const void* h, const void* gu
   p.accumulate = accumulate;
   p.out0 = dWd;
   CUtensorMap ta, tb;
-  if (int rc = make_tmap(&ta, dy_perm, H, R, 64, 64)) return rc;
-  if (int rc = make_tmap(&tb, h, I, R, 64, 64)) return rc;
+  if (int rc = make_tmap_mn(&ta, dy_perm, H, R, BM / 64)) return rc;
+  if (int rc = make_tmap_mn(&tb, h, I, R, p.BN / 64)) return rc;
   CUtensorMap to;
   if (int rc = make_out_map(&to, dWd, I, (uint64_t)E * H, true)) return rc;
-  return run<DW>(use_pair(p.BN), p, ta, tb, tb, to, to, s, fn);
+  return run<DW>(false, p, ta, tb, tb, to, to, s, fn);
 }
 
 int moe_grouped_gemm_swiglu_bwd(const void* dgu, const void* x_perm, const void* Wg,
@@ -1280,11 +1327,12 @@ int moe_grouped_gemm_swiglu_bwd(const void* dgu, const void* x_perm, const void*
     p.out0 = dx_perm;
     CUtensorMap ta, tg, tu;
     if (int rc = make_tmap(&ta, dgu, 2 * I, R, 64, BM)) return rc;
-    if (int rc = make_tmap(&tg, Wg, H, (uint64_t)E * I, 64, 64)) return rc;
-    if (int rc = make_tmap(&tu, Wu, H, (uint64_t)E * I, 64, 64)) return rc;
+    const uint32_t nck = p.BN / 64 / (pair_for<GATE_UP_BWD_DX>(p.BN) ? 2 : 1);
+    if (int rc = make_tmap_mn(&tg, Wg, H, (uint64_t)E * I, nck)) return rc;
+    if (int rc = make_tmap_mn(&tu, Wu, H, (uint64_t)E * I, nck)) return rc;
     CUtensorMap to;
     if (int rc = make_out_map(&to, dx_perm, H, R, false)) return rc;
-    if (int rc = run<GATE_UP_BWD_DX>(use_pair(p.BN), p, ta, tg, tu, to, to, s, fn))
+    if (int rc = run<GATE_UP_BWD_DX>(pair_for<GATE_UP_BWD_DX>(p.BN), p, ta, tg, tu, to, to, s, fn))
       return rc;
   }
   if (num_seg == 0) {
@@ -1307,12 +1355,12 @@ int moe_grouped_gemm_swiglu_bwd(const void* dgu, const void* x_perm, const void*
   p.out0 = dWg;
   p.out1 = dWu;
   CUtensorMap ta, tb;
-  if (int rc = make_tmap(&ta, dgu, 2 * I, R, 64, 64)) return rc;
-  if (int rc = make_tmap(&tb, x_perm, H, R, 64, 64)) return rc;
+  if (int rc = make_tmap_mn(&ta, dgu, 2 * I, R, BM / 64)) return rc;
+  if (int rc = make_tmap_mn(&tb, x_perm, H, R, p.BN / 64)) return rc;
   CUtensorMap tog, tou;
   if (int rc = make_out_map(&tog, dWg, H, (uint64_t)E * I, true)) return rc;
   if (int rc = make_out_map(&tou, dWu, H, (uint64_t)E * I, true)) return rc;
-  return run<DW>(use_pair(p.BN), p, ta, tb, tb, tog, tou, s, fn);
+  return run<DW>(false, p, ta, tb, tb, tog, tou, s, fn);
 }
 
 }  // extern "C"
