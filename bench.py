@@ -69,7 +69,7 @@ class ClockSampler:
             self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                 "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -251,7 +251,7 @@ def run_ours(args, shape, inp):
     barrier(dist, dev)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
-        time.sleep(0.3)
+        time.sleep(0.1)
         t_start.record(stream)
         for i in range(args.steps):
             step(evs[i])
@@ -399,7 +399,7 @@ def run_profile_case(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--ref-tokens", type=int, default=8, help="oracle tokens per reference step")

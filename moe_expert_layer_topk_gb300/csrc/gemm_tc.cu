@@ -748,20 +748,24 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool full = Traits<KIND>::rows ? (rb + 31 < t.row_end) : (rb < p.M);
       const bool any = Traits<KIND>::rows ? (rb < t.row_end) : (rb < p.M);
       // SwiGLU backward: the saved g, u of this thread's row do not depend on
-      // the accumulator, so the first chunk is requested before waiting.
-      uint4 gpre[4], upre[4];
+      // the accumulator, so the first two chunks are requested before waiting
+      // and every chunk's are requested two chunks ahead.
+      uint4 gpre[4], upre[4], gpre2[4], upre2[4];
       const __nv_bfloat16* grow =
           static_cast<const __nv_bfloat16*>(p.aux) + (size_t)r * 2 * p.I + t.n0;
-      auto prefetch_gu = [&](int c) {
-        if (KIND == DOWN_BWD_DX && valid) {
+      auto prefetch_gu = [&](int c, uint4 (&gd)[4], uint4 (&ud)[4]) {
+        if (KIND == DOWN_BWD_DX && valid && c < p.BN) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            gpre[i] = __ldg(reinterpret_cast<const uint4*>(grow + c) + i);
-            upre[i] = __ldg(reinterpret_cast<const uint4*>(grow + p.I + c) + i);
+            gd[i] = __ldg(reinterpret_cast<const uint4*>(grow + c) + i);
+            ud[i] = __ldg(reinterpret_cast<const uint4*>(grow + p.I + c) + i);
           }
         }
       };
-      if constexpr (KIND == DOWN_BWD_DX) prefetch_gu(0);
+      if constexpr (KIND == DOWN_BWD_DX) {
+        prefetch_gu(0, gpre, upre);
+        prefetch_gu(32, gpre2, upre2);
+      }
       if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&ctl->tfull[buf]), use & 1u, ctl, p.status))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * ACC_COLS);
@@ -862,8 +866,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int i = 0; i < 4; ++i) {
             gcur[i] = gpre[i];
             ucur[i] = upre[i];
+            gpre[i] = gpre2[i];
+            upre[i] = upre2[i];
           }
-          if (c + 32 < p.BN) prefetch_gu(c + 32);
+          prefetch_gu(c + 64, gpre2, upre2);
           tmem_wait_ld();
           uint4 og4[4], ou4[4];
 #pragma unroll
