@@ -53,7 +53,9 @@ constexpr unsigned long long TIMEOUT_NS = 2000000000ull;
 constexpr int EP_BOX_BYTES = 32 * 64;
 constexpr int EP_SLOTS = 2;
 constexpr int EP_WARP_BYTES = EP_BOX_BYTES * EP_SLOTS;
-constexpr int EP_BYTES = 4 * EP_WARP_BYTES;
+// DOWN_BWD_DX also loads the saved g, u boxes by TMA: 4 sets of (g, u) slots.
+constexpr int EP_GU_SETS = 4;
+constexpr int EP_GU_WARP_BYTES = EP_BOX_BYTES * 2 * EP_GU_SETS;
 
 enum Kind : int { GATE_UP_FWD = 0, DOWN_FWD = 1, DOWN_BWD_DX = 2, GATE_UP_BWD_DX = 3, DW = 4, DENSE_ADD = 5 };
 
@@ -94,6 +96,7 @@ struct Ctl {
   int seg_off[kMaxSegments + 1];
   int seg_exp[kMaxSegments];
   int grp_rows[kMaxSegments];       // DW: rows per output group
+  unsigned long long ep_bar[4][EP_GU_SETS];  // DOWN_BWD_DX: g,u box loads per epilogue warp
 };
 
 
@@ -304,15 +307,21 @@ struct Traits {
 // holds its own 128 rows of A and half of the B tile's N range; the leader
 // (cluster rank 0) issues the MMAs, which read both CTAs' shared memory and
 // write each CTA's 128 accumulator rows into that CTA's TMEM.
-template <int CTAS>
+template <int KIND, int CTAS>
 struct Cfg {
-  static constexpr int STAGES = CTAS == 1 ? 4 : 6;
+  // The SwiGLU-backward kind gives one pipeline stage to its g,u staging.
+  static constexpr bool gu_tma = KIND == DOWN_BWD_DX;
+  static constexpr int STAGES = CTAS == 1 ? (gu_tma ? 3 : 4) : (gu_tma ? 4 : 6);
   static constexpr int B_BYTES = B_BYTES_MAX / CTAS;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TILE_M = BM * CTAS;
-  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + EP_BYTES + sizeof(Ctl);
+  static constexpr int EP_WARP = gu_tma ? EP_GU_WARP_BYTES : EP_WARP_BYTES;
+  static constexpr int EP_TOTAL = 4 * EP_WARP;
+  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + EP_TOTAL + sizeof(Ctl);
 };
-static_assert(Cfg<1>::SMEM <= 232448 && Cfg<2>::SMEM <= 232448, "shared memory budget exceeded");
+static_assert(Cfg<GATE_UP_FWD, 1>::SMEM <= 232448 && Cfg<GATE_UP_FWD, 2>::SMEM <= 232448 &&
+                  Cfg<DOWN_BWD_DX, 1>::SMEM <= 232448 && Cfg<DOWN_BWD_DX, 2>::SMEM <= 232448,
+              "shared memory budget exceeded");
 
 struct Tile {
   int group;   // expert (row kinds) / output group (DW)
@@ -334,14 +343,14 @@ __device__ __forceinline__ Tile decode_tile(int tile, const Params& p, const Ctl
     }
     t.seg = lo;
     t.group = ctl->seg_exp[lo];
-    t.m0 = ctl->seg_off[lo] + (gm - ctl->seg_tiles[lo]) * Cfg<CTAS>::TILE_M + BM * rank;
+    t.m0 = ctl->seg_off[lo] + (gm - ctl->seg_tiles[lo]) * Cfg<KIND, CTAS>::TILE_M + BM * rank;
     t.row_end = ctl->seg_off[lo + 1];
     t.n0 = nt * (KIND == GATE_UP_FWD ? p.NH : p.BN);
   } else {
     const int per = p.m_tiles * p.n_tiles;
     t.group = tile / per;
     const int rem = tile % per;
-    t.m0 = (rem / p.n_tiles) * Cfg<CTAS>::TILE_M + BM * rank;
+    t.m0 = (rem / p.n_tiles) * Cfg<KIND, CTAS>::TILE_M + BM * rank;
     t.n0 = (rem % p.n_tiles) * p.BN;
     t.row_end = 0;
     t.seg = 0;
@@ -480,12 +489,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const __grid_constant__ CUtensorMap tmB1,
                         const __grid_constant__ CUtensorMap tmO0,
                         const __grid_constant__ CUtensorMap tmO1, const Params p) {
-  using C = Cfg<CTAS>;
+  using C = Cfg<KIND, CTAS>;
   constexpr int STG = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + (size_t)STG * C::STAGE_BYTES + EP_BYTES);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + (size_t)STG * C::STAGE_BYTES + C::EP_TOTAL);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int limit = Traits<KIND>::rows ? p.M : p.K;  // rows addressable through the segment table
   const int rank = CTAS == 2 ? (int)cluster_rank() : 0;
@@ -558,6 +567,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_init(smem_u32(&ctl->tempty[i]), 4 * CTAS);
       }
       mbar_init(smem_u32(&ctl->drain), 1);
+      for (int w = 0; w < 4; ++w)
+        for (int i = 0; i < EP_GU_SETS; ++i) mbar_init(smem_u32(&ctl->ep_bar[w][i]), 1);
       ctl->abort_flag = 0;
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
       prefetch_tmap(&tmA);
@@ -731,7 +742,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // ============================ epilogue ================================
     const int q = warp & 3;
-    EpRing ring{smem + (size_t)STG * C::STAGE_BYTES + (size_t)(warp - 2) * EP_WARP_BYTES, 0, lane};
+    uint8_t* ep_base = smem + (size_t)STG * C::STAGE_BYTES + (size_t)(warp - 2) * C::EP_WARP;
+    EpRing ring{ep_base, 0, lane};
+    int gu_ctr = 0;  // DOWN_BWD_DX: running count of this warp's 32-column chunks
     const uint32_t tempty_leader[2] = {
         CTAS == 2 ? map_to_rank(smem_u32(&ctl->tempty[0]), 0) : smem_u32(&ctl->tempty[0]),
         CTAS == 2 ? map_to_rank(smem_u32(&ctl->tempty[1]), 0) : smem_u32(&ctl->tempty[1])};
@@ -747,24 +760,27 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool valid = Traits<KIND>::rows ? (r < t.row_end) : (r < p.M);
       const bool full = Traits<KIND>::rows ? (rb + 31 < t.row_end) : (rb < p.M);
       const bool any = Traits<KIND>::rows ? (rb < t.row_end) : (rb < p.M);
-      // SwiGLU backward: the saved g, u of this thread's row do not depend on
-      // the accumulator, so the first two chunks are requested before waiting
-      // and every chunk's are requested two chunks ahead.
-      uint4 gpre[4], upre[4], gpre2[4], upre2[4];
-      const __nv_bfloat16* grow =
-          static_cast<const __nv_bfloat16*>(p.aux) + (size_t)r * 2 * p.I + t.n0;
-      auto prefetch_gu = [&](int c, uint4 (&gd)[4], uint4 (&ud)[4]) {
-        if (KIND == DOWN_BWD_DX && valid && c < p.BN) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            gd[i] = __ldg(reinterpret_cast<const uint4*>(grow + c) + i);
-            ud[i] = __ldg(reinterpret_cast<const uint4*>(grow + p.I + c) + i);
-          }
+      // SwiGLU backward: the saved g, u boxes (32 rows x 32 columns each) of
+      // this warp's rows do not depend on the accumulator.  They arrive by
+      // TMA into set (chunk counter mod 4) of the warp's staging, two chunks
+      // ahead; the first two are requested before waiting for the MMAs.  A
+      // set is reloaded only after the stores that used it (two chunks
+      // earlier, two bulk groups per chunk) have read it.
+      const uint32_t gu_bar0 = smem_u32(&ctl->ep_bar[warp - 2][0]);
+      auto gu_load = [&](int c, int ctr) {
+        if (KIND == DOWN_BWD_DX && any && c < p.BN && lane == 0) {
+          const int set = ctr & (EP_GU_SETS - 1);
+          asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory");
+          const uint32_t bar = gu_bar0 + 8u * (uint32_t)set;
+          const uint32_t g_slot = smem_u32(ep_base + (2 * set) * EP_BOX_BYTES);
+          mbar_arrive_expect_tx(bar, 2 * EP_BOX_BYTES);
+          tma_load_2d(g_slot, &tmB1, bar, t.n0 + c, rb);
+          tma_load_2d(g_slot + EP_BOX_BYTES, &tmB1, bar, p.I + t.n0 + c, rb);
         }
       };
       if constexpr (KIND == DOWN_BWD_DX) {
-        prefetch_gu(0, gpre, upre);
-        prefetch_gu(32, gpre2, upre2);
+        gu_load(0, gu_ctr);
+        gu_load(32, gu_ctr + 1);
       }
       if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&ctl->tfull[buf]), use & 1u, ctl, p.status))) break;
       tc_fence_after();
@@ -858,24 +874,25 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       } else if constexpr (KIND == DOWN_BWD_DX) {
         __nv_bfloat16* dgu = static_cast<__nv_bfloat16*>(p.out0);
-        for (int c = 0; any && c < p.BN; c += 32) {
+        for (int c = 0; any && c < p.BN; c += 32, ++gu_ctr) {
+          gu_load(c + 64, gu_ctr + 2);
           uint32_t a[32];
           tmem_ld32(taddr + c, a);
-          uint4 gcur[4], ucur[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            gcur[i] = gpre[i];
-            ucur[i] = upre[i];
-            gpre[i] = gpre2[i];
-            upre[i] = upre2[i];
-          }
-          prefetch_gu(c + 64, gpre2, upre2);
+          const int set = gu_ctr & (EP_GU_SETS - 1);
+          uint8_t* gbox = ep_base + (2 * set) * EP_BOX_BYTES;
+          uint8_t* ubox = gbox + EP_BOX_BYTES;
+          const bool ok = __all_sync(0xffffffffu, wait_bar(gu_bar0 + 8u * (uint32_t)set,
+                                                           (uint32_t)(gu_ctr >> 2) & 1u, ctl, p.status));
           tmem_wait_ld();
+          if (!ok) break;
+          const int sw = (lane >> 1) & 3;  // 64-byte swizzle of this lane's row
           uint4 og4[4], ou4[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const uint32_t gw[4] = {gcur[i].x, gcur[i].y, gcur[i].z, gcur[i].w};
-            const uint32_t uw[4] = {ucur[i].x, ucur[i].y, ucur[i].z, ucur[i].w};
+            const uint4 gv = *reinterpret_cast<const uint4*>(gbox + lane * 64 + ((i ^ sw) << 4));
+            const uint4 uv = *reinterpret_cast<const uint4*>(ubox + lane * 64 + ((i ^ sw) << 4));
+            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+            const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
             uint32_t og[4], ou[4];
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
@@ -896,21 +913,34 @@ __global__ void __launch_bounds__(THREADS, 1)
             ou4[i] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
           }
           if (full) {
-            uint8_t* bx = ring.acquire();
-#pragma unroll
-            for (int i = 0; i < 4; ++i) ring.put(bx, i, og4[i]);
-            ring.issue(bx, &tmO0, t.n0 + c, rb);
-            bx = ring.acquire();
-#pragma unroll
-            for (int i = 0; i < 4; ++i) ring.put(bx, i, ou4[i]);
-            ring.issue(bx, &tmO0, p.I + t.n0 + c, rb);
-          } else if (valid) {
-            uint4* gdst = reinterpret_cast<uint4*>(dgu + (size_t)r * 2 * p.I + t.n0 + c);
-            uint4* udst = reinterpret_cast<uint4*>(dgu + (size_t)r * 2 * p.I + p.I + t.n0 + c);
+            // results overwrite the g, u boxes in place (each lane its own row)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              gdst[i] = og4[i];
-              udst[i] = ou4[i];
+              *reinterpret_cast<uint4*>(gbox + lane * 64 + ((i ^ sw) << 4)) = og4[i];
+              *reinterpret_cast<uint4*>(ubox + lane * 64 + ((i ^ sw) << 4)) = ou4[i];
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmO0, smem_u32(gbox), t.n0 + c, rb);
+              asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+              tma_store_2d(&tmO0, smem_u32(ubox), p.I + t.n0 + c, rb);
+              asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            }
+          } else {
+            if (valid) {
+              uint4* gdst = reinterpret_cast<uint4*>(dgu + (size_t)r * 2 * p.I + t.n0 + c);
+              uint4* udst = reinterpret_cast<uint4*>(dgu + (size_t)r * 2 * p.I + p.I + t.n0 + c);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                gdst[i] = og4[i];
+                udst[i] = ou4[i];
+              }
+            }
+            __syncwarp();
+            if (lane == 0) {  // keep two bulk groups per chunk
+              asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+              asm volatile("cp.async.bulk.commit_group;" ::: "memory");
             }
           }
         }
@@ -1072,7 +1102,7 @@ int launch(Params p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensor
   const int dev = current_device();
   if (dev < 0) return fail(MOE_ERR_CUDA, "%s: no current CUDA device", what);
   auto kern = grouped_gemm_kernel<KIND, CTAS>;
-  const int smem = (int)Cfg<CTAS>::SMEM;
+  const int smem = (int)Cfg<KIND, CTAS>::SMEM;
   if (!g_attr[KIND][CTAS - 1][dev]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -1275,9 +1305,10 @@ int moe_grouped_gemm_down_bwd(const void* dy_perm, const void* h, const void* gu
     CUtensorMap ta, tb;
     if (int rc = make_tmap(&ta, dy_perm, H, R, 64, BM)) return rc;
     if (int rc = make_tmap_mn(&tb, Wd, I, (uint64_t)E * H, p.BN / 64)) return rc;
-    CUtensorMap to;
+    CUtensorMap to, tgu;
     if (int rc = make_out_map(&to, dgu, 2 * I, R, false)) return rc;
-    if (int rc = run<DOWN_BWD_DX>(false, p, ta, tb, tb, to, to, s, fn))
+    if (int rc = make_out_map(&tgu, gu_save, 2 * I, R, false)) return rc;  // g,u boxes in
+    if (int rc = run<DOWN_BWD_DX>(false, p, ta, tb, tgu, to, to, s, fn))
       return rc;
   }
   // dWd[e] = dy_perm[rows of e]^T . h[rows of e]
