@@ -741,9 +741,44 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // ============================ epilogue ================================
+    // Each warp owns 32 accumulator rows of the tile (TMEM lanes
+    // 32*(warp%4)..+31).  Results leave in boxes of 32 rows x 64 bytes:
+    // every lane writes its own row of the box into shared memory (64-byte
+    // swizzle, conflict-free), then the warp reads the box back row-segment
+    // by row-segment and writes it with coalesced 16-byte stores (8 full
+    // 64-byte row segments per instruction), skipping rows past the end of
+    // the expert's rows.  These stores do not queue behind the operand
+    // loads on the TMA unit.
     const int q = warp & 3;
     uint8_t* ep_base = smem + (size_t)STG * C::STAGE_BYTES + (size_t)(warp - 2) * C::EP_WARP;
-    EpRing ring{ep_base, 0, lane};
+    const int sw = (lane >> 1) & 3;  // 64-byte swizzle phase of this lane's row
+    auto put = [&](uint8_t* box, int c, uint4 v) {
+      *reinterpret_cast<uint4*>(box + lane * 64 + ((c ^ sw) << 4)) = v;
+    };
+    auto get = [&](const uint8_t* box, int c) -> uint4 {
+      return *reinterpret_cast<const uint4*>(box + lane * 64 + ((c ^ sw) << 4));
+    };
+    // box -> rows [row0, row0 + nvalid) of a row-major tensor at byte column col
+    auto flush = [&](const uint8_t* box, void* base, size_t pitch, size_t col, int row0, int nvalid,
+                     bool acc_f32) {
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int rr = (lane >> 2) + 8 * j, cc = lane & 3;
+        uint4 v = *reinterpret_cast<const uint4*>(box + rr * 64 + ((cc ^ ((rr >> 1) & 3)) << 4));
+        if (rr < nvalid) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(base) + (size_t)(row0 + rr) * pitch +
+                                                col + cc * 16);
+          if (acc_f32) {
+            const float4 o = *reinterpret_cast<const float4*>(dst);
+            v = make_uint4(__float_as_uint(__uint_as_float(v.x) + o.x), __float_as_uint(__uint_as_float(v.y) + o.y),
+                           __float_as_uint(__uint_as_float(v.z) + o.z), __float_as_uint(__uint_as_float(v.w) + o.w));
+          }
+          *dst = v;
+        }
+      }
+      __syncwarp();
+    };
     int gu_ctr = 0;  // DOWN_BWD_DX: running count of this warp's 32-column chunks
     const uint32_t tempty_leader[2] = {
         CTAS == 2 ? map_to_rank(smem_u32(&ctl->tempty[0]), 0) : smem_u32(&ctl->tempty[0]),
@@ -753,24 +788,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       const Tile t = decode_tile<KIND, CTAS>(tile, p, ctl, rank);
       const int buf = local & 1;
       const uint32_t use = (uint32_t)(local >> 1);
-      // this warp's 32 rows: full boxes go out through TMA stores, a box that
-      // straddles the end of its segment through masked per-row stores
       const int rb = t.m0 + q * 32;
-      const int r = rb + lane;
-      const bool valid = Traits<KIND>::rows ? (r < t.row_end) : (r < p.M);
-      const bool full = Traits<KIND>::rows ? (rb + 31 < t.row_end) : (rb < p.M);
-      const bool any = Traits<KIND>::rows ? (rb < t.row_end) : (rb < p.M);
+      const int lim = Traits<KIND>::rows ? t.row_end : p.M;
+      const int nvalid = lim - rb < 0 ? 0 : (lim - rb > 32 ? 32 : lim - rb);
+      const bool any = nvalid > 0;
       // SwiGLU backward: the saved g, u boxes (32 rows x 32 columns each) of
       // this warp's rows do not depend on the accumulator.  They arrive by
       // TMA into set (chunk counter mod 4) of the warp's staging, two chunks
-      // ahead; the first two are requested before waiting for the MMAs.  A
-      // set is reloaded only after the stores that used it (two chunks
-      // earlier, two bulk groups per chunk) have read it.
+      // ahead; the first two are requested before waiting for the MMAs.
       const uint32_t gu_bar0 = smem_u32(&ctl->ep_bar[warp - 2][0]);
       auto gu_load = [&](int c, int ctr) {
         if (KIND == DOWN_BWD_DX && any && c < p.BN && lane == 0) {
           const int set = ctr & (EP_GU_SETS - 1);
-          asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory");
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier reads of the set
           const uint32_t bar = gu_bar0 + 8u * (uint32_t)set;
           const uint32_t g_slot = smem_u32(ep_base + (2 * set) * EP_BOX_BYTES);
           mbar_arrive_expect_tx(bar, 2 * EP_BOX_BYTES);
@@ -787,8 +817,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * ACC_COLS);
 
       if constexpr (KIND == GATE_UP_FWD) {
-        __nv_bfloat16* h = static_cast<__nv_bfloat16*>(p.out0);
-        __nv_bfloat16* gu = static_cast<__nv_bfloat16*>(p.out1);
+        const size_t hp_pitch = (size_t)p.I * 2, gu_pitch = (size_t)p.I * 4;
         for (int c = 0; any && c < p.NH; c += 32) {
           uint32_t g[32], u[32];
           tmem_ld32(taddr + c, g);
@@ -799,45 +828,27 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int i = 0; i < 16; ++i) {
             const float g0 = f32(g[2 * i]), g1 = f32(g[2 * i + 1]);
             const float u0 = f32(u[2 * i]), u1 = f32(u[2 * i + 1]);
-            const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
-            const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
+            const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
+            const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
             hp[i] = pack_bf16x2(h0, h1);
             gp[i] = pack_bf16x2(g0, g1);
             upk[i] = pack_bf16x2(u0, u1);
           }
-          if (full) {
-            uint8_t* bx = ring.acquire();
 #pragma unroll
-            for (int i = 0; i < 4; ++i) ring.put(bx, i, make_uint4(hp[4 * i], hp[4 * i + 1], hp[4 * i + 2], hp[4 * i + 3]));
-            ring.issue(bx, &tmO0, t.n0 + c, rb);
-            if (gu) {
-              bx = ring.acquire();
+          for (int i = 0; i < 4; ++i) put(ep_base, i, make_uint4(hp[4 * i], hp[4 * i + 1], hp[4 * i + 2], hp[4 * i + 3]));
+          flush(ep_base, p.out0, hp_pitch, (size_t)(t.n0 + c) * 2, rb, nvalid, false);
+          if (p.out1) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i) ring.put(bx, i, make_uint4(gp[4 * i], gp[4 * i + 1], gp[4 * i + 2], gp[4 * i + 3]));
-              ring.issue(bx, &tmO1, t.n0 + c, rb);
-              bx = ring.acquire();
+            for (int i = 0; i < 4; ++i) put(ep_base, i, make_uint4(gp[4 * i], gp[4 * i + 1], gp[4 * i + 2], gp[4 * i + 3]));
+            flush(ep_base, p.out1, gu_pitch, (size_t)(t.n0 + c) * 2, rb, nvalid, false);
 #pragma unroll
-              for (int i = 0; i < 4; ++i) ring.put(bx, i, make_uint4(upk[4 * i], upk[4 * i + 1], upk[4 * i + 2], upk[4 * i + 3]));
-              ring.issue(bx, &tmO1, p.I + t.n0 + c, rb);
-            }
-          } else if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(h + (size_t)r * p.I + t.n0 + c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(hp[4 * i], hp[4 * i + 1], hp[4 * i + 2], hp[4 * i + 3]);
-            if (gu) {
-              uint4* dg = reinterpret_cast<uint4*>(gu + (size_t)r * 2 * p.I + t.n0 + c);
-              uint4* du = reinterpret_cast<uint4*>(gu + (size_t)r * 2 * p.I + p.I + t.n0 + c);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                dg[i] = make_uint4(gp[4 * i], gp[4 * i + 1], gp[4 * i + 2], gp[4 * i + 3]);
-                du[i] = make_uint4(upk[4 * i], upk[4 * i + 1], upk[4 * i + 2], upk[4 * i + 3]);
-              }
-            }
+            for (int i = 0; i < 4; ++i) put(ep_base, i, make_uint4(upk[4 * i], upk[4 * i + 1], upk[4 * i + 2], upk[4 * i + 3]));
+            flush(ep_base, p.out1, gu_pitch, (size_t)(p.I + t.n0 + c) * 2, rb, nvalid, false);
           }
         }
       } else if constexpr (KIND == DOWN_FWD || KIND == GATE_UP_BWD_DX || KIND == DENSE_ADD) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out0);
+        const size_t pitch = (size_t)p.ldo * 2;
+        const int r = rb + lane;
         for (int c = 0; any && c < p.BN; c += 32) {
           uint32_t a[32];
           tmem_ld32(taddr + c, a);
@@ -846,7 +857,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = f32(a[i]);
           if constexpr (KIND == DENSE_ADD) {
-            if (valid) {
+            if (lane < nvalid) {
               const float4* add = reinterpret_cast<const float4*>(
                   static_cast<const float*>(p.aux) + (size_t)r * p.ldo + t.n0 + c);
 #pragma unroll
@@ -856,24 +867,14 @@ __global__ void __launch_bounds__(THREADS, 1)
               }
             }
           }
-          uint4 pk[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            pk[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                               pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
-          if (full) {
-            uint8_t* bx = ring.acquire();
-#pragma unroll
-            for (int i = 0; i < 4; ++i) ring.put(bx, i, pk[i]);
-            ring.issue(bx, &tmO0, t.n0 + c, rb);
-          } else if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(out + (size_t)r * p.ldo + t.n0 + c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = pk[i];
-          }
+            put(ep_base, i, make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                       pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7])));
+          flush(ep_base, p.out0, pitch, (size_t)(t.n0 + c) * 2, rb, nvalid, false);
         }
       } else if constexpr (KIND == DOWN_BWD_DX) {
-        __nv_bfloat16* dgu = static_cast<__nv_bfloat16*>(p.out0);
+        const size_t pitch = (size_t)p.I * 4;
         for (int c = 0; any && c < p.BN; c += 32, ++gu_ctr) {
           gu_load(c + 64, gu_ctr + 2);
           uint32_t a[32];
@@ -885,12 +886,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                                                            (uint32_t)(gu_ctr >> 2) & 1u, ctl, p.status));
           tmem_wait_ld();
           if (!ok) break;
-          const int sw = (lane >> 1) & 3;  // 64-byte swizzle of this lane's row
-          uint4 og4[4], ou4[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const uint4 gv = *reinterpret_cast<const uint4*>(gbox + lane * 64 + ((i ^ sw) << 4));
-            const uint4 uv = *reinterpret_cast<const uint4*>(ubox + lane * 64 + ((i ^ sw) << 4));
+            const uint4 gv = get(gbox, i), uv = get(ubox, i);
             const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
             const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
             uint32_t og[4], ou[4];
@@ -902,55 +900,28 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const float g = hh ? bf16hi(gw[jj]) : bf16lo(gw[jj]);
                 const float u = hh ? bf16hi(uw[jj]) : bf16lo(uw[jj]);
                 const float dh = f32(a[8 * i + 2 * jj + hh]);
-                const float sg = 1.0f / (1.0f + __expf(-g));
+                const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
                 dg2[hh] = dh * u * sg * (1.0f + g * (1.0f - sg));
                 du2[hh] = dh * (g * sg);
               }
               og[jj] = pack_bf16x2(dg2[0], dg2[1]);
               ou[jj] = pack_bf16x2(du2[0], du2[1]);
             }
-            og4[i] = make_uint4(og[0], og[1], og[2], og[3]);
-            ou4[i] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
-          }
-          if (full) {
             // results overwrite the g, u boxes in place (each lane its own row)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              *reinterpret_cast<uint4*>(gbox + lane * 64 + ((i ^ sw) << 4)) = og4[i];
-              *reinterpret_cast<uint4*>(ubox + lane * 64 + ((i ^ sw) << 4)) = ou4[i];
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&tmO0, smem_u32(gbox), t.n0 + c, rb);
-              asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-              tma_store_2d(&tmO0, smem_u32(ubox), p.I + t.n0 + c, rb);
-              asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-            }
-          } else {
-            if (valid) {
-              uint4* gdst = reinterpret_cast<uint4*>(dgu + (size_t)r * 2 * p.I + t.n0 + c);
-              uint4* udst = reinterpret_cast<uint4*>(dgu + (size_t)r * 2 * p.I + p.I + t.n0 + c);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                gdst[i] = og4[i];
-                udst[i] = ou4[i];
-              }
-            }
-            __syncwarp();
-            if (lane == 0) {  // keep two bulk groups per chunk
-              asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-              asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-            }
+            put(gbox, i, make_uint4(og[0], og[1], og[2], og[3]));
+            put(ubox, i, make_uint4(ou[0], ou[1], ou[2], ou[3]));
           }
+          flush(gbox, p.out0, pitch, (size_t)(t.n0 + c) * 2, rb, nvalid, false);
+          flush(ubox, p.out0, pitch, (size_t)(p.I + t.n0 + c) * 2, rb, nvalid, false);
         }
       } else {  // DW: fp32 [group, M, N] (optionally split at split_m over two tensors)
         const bool nonempty = ctl->grp_rows[t.group] > 0;
-        if (full && (nonempty || !p.accumulate)) {
+        if (any && (nonempty || !p.accumulate)) {
           const bool second = p.split_m > 0 && rb >= p.split_m;
-          const CUtensorMap* map = second ? &tmO1 : &tmO0;
+          void* base = second ? p.out1 : p.out0;
           const int y = p.split_m > 0 ? t.group * p.split_m + (second ? rb - p.split_m : rb)
                                       : t.group * p.M + rb;
+          const size_t pitch = (size_t)p.ldo * 4;
           for (int c = 0; c < p.BN; c += 32) {
             uint32_t a[32];
             if (nonempty) {
@@ -962,12 +933,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-              uint8_t* bx = ring.acquire();
 #pragma unroll
               for (int i = 0; i < 4; ++i)
-                ring.put(bx, i, make_uint4(a[16 * half + 4 * i], a[16 * half + 4 * i + 1],
+                put(ep_base, i, make_uint4(a[16 * half + 4 * i], a[16 * half + 4 * i + 1],
                                            a[16 * half + 4 * i + 2], a[16 * half + 4 * i + 3]));
-              ring.issue(bx, map, t.n0 + c + 16 * half, y, p.accumulate != 0);
+              flush(ep_base, base, pitch, (size_t)(t.n0 + c + 16 * half) * 4, y, nvalid, p.accumulate != 0);
             }
           }
         }
@@ -983,7 +953,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                        : "memory");
       }
     }
-    ring.drain();
   }
 
   tc_fence_before();

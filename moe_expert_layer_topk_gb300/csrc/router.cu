@@ -16,66 +16,75 @@ namespace {
 
 // ------------------------------------------------------------ logits kernel
 //
-// CTA = 4 warps over 32 tokens x 64 experts; thread = 4 tokens x 4 experts.
-// h advances in stages of 32 positions staged through shared memory (x
-// widened to fp32 once per CTA, both operands double-buffered through
-// registers).  Each thread keeps, per output, the running fused
+// CTA = 2 warps over 32 tokens x 32 experts; thread = 4 tokens x 4 experts.
+// h advances in stages of 32 positions: a 4-deep cp.async pipeline brings
+// the Wr tile [32 h][32 e] (fp32) and the x tile [32 tokens][32 h] (bf16)
+// into shared memory; x is widened once per stage into a transposed fp32
+// tile [32 h][32 tokens].  Each thread keeps, per output, the fused
 // multiply-add chain of the current 256-wide h-block and the running sum of
 // the finished blocks: exactly the order of the reading (block partials in
 // increasing h from 0, block sums added left to right, bias last).
 constexpr int kLogitTok = 32;
-constexpr int kLogitExp = 64;
-constexpr int kLogitThreads = 128;
+constexpr int kLogitExp = 32;
+constexpr int kLogitThreads = 64;
 constexpr int kLogitStage = 32;   // h per stage
 constexpr int kLogitBlockH = 256; // h per summation block
+constexpr int kLogitDepth = 4;    // stages in flight
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(pred ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool pred) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(pred ? 4 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 template <bool kVec>
 __global__ void __launch_bounds__(kLogitThreads) router_logits_kernel(
     const __nv_bfloat16* __restrict__ x, const float* __restrict__ Wr, const float* __restrict__ bias,
     int T, int H, int E, float* __restrict__ logits) {
-  __shared__ __align__(16) float xs[2][kLogitStage][kLogitTok];
-  __shared__ __align__(16) float ws[2][kLogitStage][kLogitExp];
+  __shared__ __align__(16) float ws[kLogitDepth][kLogitStage][kLogitExp];
+  __shared__ __align__(16) __nv_bfloat16 xraw[kLogitDepth][kLogitTok][kLogitStage];
+  __shared__ __align__(16) float xs[kLogitStage][kLogitTok];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tg = lane & 7, eg = lane >> 3;
   const int t0 = blockIdx.x * kLogitTok, e0 = blockIdx.y * kLogitExp;
   const int my_tok = tg * 4, my_exp = warp * 16 + eg * 4;
+  const int nstage = H / kLogitStage;
 
-  // global -> register staging of one stage
-  float4 wreg[4];
-  uint4 xreg;
-  auto load_stage = [&](int h0) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int idx = tid + i * kLogitThreads;  // 0..511
-      const int row = idx >> 4, c4 = (idx & 15) * 4;
-      const int e = e0 + c4;
-      const float* src = Wr + (size_t)(h0 + row) * E + e;
-      if (kVec) {
-        wreg[i] = (e < E) ? __ldg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
-      } else {
-        wreg[i].x = (e + 0 < E) ? __ldg(src + 0) : 0.f;
-        wreg[i].y = (e + 1 < E) ? __ldg(src + 1) : 0.f;
-        wreg[i].z = (e + 2 < E) ? __ldg(src + 2) : 0.f;
-        wreg[i].w = (e + 3 < E) ? __ldg(src + 3) : 0.f;
-      }
-    }
-    const int tok = tid >> 2, h8 = (tid & 3) * 8;
-    const int t = t0 + tok;
-    xreg = (t < T) ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H + h0 + h8))
-                   : make_uint4(0, 0, 0, 0);
-  };
-  auto store_stage = [&](int buf) {
+  auto issue = [&](int st) {
+    const int buf = st % kLogitDepth;
+    const int h0 = st * kLogitStage;
+    // Wr: 32 rows x 32 experts = 256 x 16 bytes, 4 per thread
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int idx = tid + i * kLogitThreads;
-      *reinterpret_cast<float4*>(&ws[buf][idx >> 4][(idx & 15) * 4]) = wreg[i];
-    }
-    const int tok = tid >> 2, h8 = (tid & 3) * 8;
-    const uint32_t w4[4] = {xreg.x, xreg.y, xreg.z, xreg.w};
+      const int row = idx >> 3, c4 = (idx & 7) * 4;
+      const int e = e0 + c4;
+      const float* src = Wr + (size_t)(h0 + row) * E + e;
+      const uint32_t dst = (uint32_t)__cvta_generic_to_shared(&ws[buf][row][c4]);
+      if (kVec) {
+        cp_async16(dst, e < E ? src : Wr, e < E);
+      } else {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      xs[buf][h8 + 2 * i][tok] = bf16lo(w4[i]);
-      xs[buf][h8 + 2 * i + 1][tok] = bf16hi(w4[i]);
+        for (int j = 0; j < 4; ++j) cp_async4(dst + 4 * j, e + j < E ? src + j : Wr, e + j < E);
+      }
+    }
+    // x: 32 tokens x 32 h (bf16) = 128 x 16 bytes, 2 per thread
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int idx = tid + i * kLogitThreads;
+      const int tok = idx >> 2, h8 = (idx & 3) * 8;
+      const int t = t0 + tok;
+      const uint32_t dst = (uint32_t)__cvta_generic_to_shared(&xraw[buf][tok][h8]);
+      cp_async16(dst, t < T ? (const void*)(x + (size_t)t * H + h0 + h8) : (const void*)x, t < T);
     }
   };
 
@@ -87,16 +96,36 @@ __global__ void __launch_bounds__(kLogitThreads) router_logits_kernel(
       p[i][j] = 0.f;
       run[i][j] = 0.f;
     }
-  const int nstage = H / kLogitStage;
-  load_stage(0);
-  store_stage(0);
-  __syncthreads();
+#pragma unroll
+  for (int st = 0; st < kLogitDepth - 1; ++st) {
+    if (st < nstage) issue(st);
+    cp_async_commit();
+  }
   for (int st = 0; st < nstage; ++st) {
-    const int buf = st & 1;
-    if (st + 1 < nstage) load_stage((st + 1) * kLogitStage);
+    const int buf = st % kLogitDepth;
+    cp_async_wait<kLogitDepth - 2>();
+    __syncthreads();  // stage st landed for every thread; stage st-1 fully consumed
+    // widen x: thread converts 16 values [tok][h..h+15] -> xs[h][tok]
+    {
+      const int tok = tid >> 1, hh0 = (tid & 1) * 16;
+      const uint4* src = reinterpret_cast<const uint4*>(&xraw[buf][tok][hh0]);
+#pragma unroll
+      for (int v = 0; v < 2; ++v) {
+        const uint4 q = src[v];
+        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          xs[hh0 + 8 * v + 2 * i][tok] = bf16lo(w4[i]);
+          xs[hh0 + 8 * v + 2 * i + 1][tok] = bf16hi(w4[i]);
+        }
+      }
+    }
+    if (st + kLogitDepth - 1 < nstage) issue(st + kLogitDepth - 1);
+    cp_async_commit();
+    __syncthreads();
 #pragma unroll 8
     for (int hh = 0; hh < kLogitStage; ++hh) {
-      const float4 xv = *reinterpret_cast<const float4*>(&xs[buf][hh][my_tok]);
+      const float4 xv = *reinterpret_cast<const float4*>(&xs[hh][my_tok]);
       const float4 wv = *reinterpret_cast<const float4*>(&ws[buf][hh][my_exp]);
       const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
       const float wa[4] = {wv.x, wv.y, wv.z, wv.w};
@@ -116,11 +145,8 @@ __global__ void __launch_bounds__(kLogitThreads) router_logits_kernel(
           p[i][j] = 0.f;
         }
     }
-    if (st + 1 < nstage) {
-      store_stage(buf ^ 1);
-      __syncthreads();
-    }
   }
+  cp_async_wait<0>();
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int t = t0 + my_tok + i;
