@@ -377,6 +377,24 @@ def run_ours(args, shape, inp):
 KERNELS_PER_STEP = 3 + 3 + 1 + 1 + 1 + 1 + 2 + 2 + 1 + 6
 
 
+def run_profile_router(args):
+    """Untimed router passes (moe_route_topk only) of T tokens (for ncu captures)."""
+    import torch
+
+    import moe_expert_layer_topk_gb300 as m
+    from moe_expert_layer_topk_gb300.synth import LayerShape, make_layer_inputs
+    T, H, E, k = (int(v) for v in args.profile_router.split(","))
+    g = torch.Generator().manual_seed(0)
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16).cuda()
+    Wr = (torch.randn(H, E, generator=g) * 0.02).cuda()
+    layer = m.MoELayer(T, H, 64, E, k, 1, training=False)
+    for _ in range(args.steps):
+        layer.route(x, Wr, None)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_router": [T, H, E, k], "passes": args.steps,
+                      "device_status": m.moe_read_device_status(reset=True)}))
+
+
 def run_profile_case(args):
     """Untimed forward+backward passes of one layer shape (for ncu captures)."""
     import torch
@@ -407,7 +425,11 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--profile-case", default=None, metavar="T,H,I,E,k",
                     help="run --steps untimed forward+backward passes of this shape and exit")
+    ap.add_argument("--profile-router", default=None, metavar="T,H,E,k",
+                    help="run --steps untimed router passes and exit")
     args = ap.parse_args(argv)
+    if args.profile_router:
+        return run_profile_router(args)
     if args.profile_case:
         return run_profile_case(args)
     if args.warmup < 3:

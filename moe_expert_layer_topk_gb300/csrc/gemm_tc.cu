@@ -779,6 +779,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       __syncwarp();
     };
+    // Full boxes of the fp32 weight gradients and of the down projection go
+    // out through TMA bulk stores instead (measured faster for those two).
+    constexpr bool kTmaOut = KIND == DW || KIND == DOWN_FWD;
+    EpRing ring{ep_base, 0, lane};
     int gu_ctr = 0;  // DOWN_BWD_DX: running count of this warp's 32-column chunks
     const uint32_t tempty_leader[2] = {
         CTAS == 2 ? map_to_rank(smem_u32(&ctl->tempty[0]), 0) : smem_u32(&ctl->tempty[0]),
@@ -867,11 +871,23 @@ __global__ void __launch_bounds__(THREADS, 1)
               }
             }
           }
+          uint4 pk[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            put(ep_base, i, make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                                       pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7])));
-          flush(ep_base, p.out0, pitch, (size_t)(t.n0 + c) * 2, rb, nvalid, false);
+            pk[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                               pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+          if (kTmaOut && nvalid == 32) {
+            uint8_t* bx = ring.acquire();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ring.put(bx, i, pk[i]);
+            ring.issue(bx, &tmO0, t.n0 + c, rb);
+          } else {
+            // a free slot (not awaiting a TMA store's read) for the direct path
+            uint8_t* bx = kTmaOut ? ring.acquire() : ep_base;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) put(bx, i, pk[i]);
+            flush(bx, p.out0, pitch, (size_t)(t.n0 + c) * 2, rb, nvalid, false);
+          }
         }
       } else if constexpr (KIND == DOWN_BWD_DX) {
         const size_t pitch = (size_t)p.I * 4;
@@ -918,10 +934,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const bool nonempty = ctl->grp_rows[t.group] > 0;
         if (any && (nonempty || !p.accumulate)) {
           const bool second = p.split_m > 0 && rb >= p.split_m;
-          void* base = second ? p.out1 : p.out0;
           const int y = p.split_m > 0 ? t.group * p.split_m + (second ? rb - p.split_m : rb)
                                       : t.group * p.M + rb;
-          const size_t pitch = (size_t)p.ldo * 4;
           for (int c = 0; c < p.BN; c += 32) {
             uint32_t a[32];
             if (nonempty) {
@@ -933,11 +947,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
+              uint8_t* bx = ring.acquire();
 #pragma unroll
               for (int i = 0; i < 4; ++i)
-                put(ep_base, i, make_uint4(a[16 * half + 4 * i], a[16 * half + 4 * i + 1],
+                ring.put(bx, i, make_uint4(a[16 * half + 4 * i], a[16 * half + 4 * i + 1],
                                            a[16 * half + 4 * i + 2], a[16 * half + 4 * i + 3]));
-              flush(ep_base, base, pitch, (size_t)(t.n0 + c + 16 * half) * 4, y, nvalid, p.accumulate != 0);
+              ring.issue(bx, second ? &tmO1 : &tmO0, t.n0 + c + 16 * half, y, p.accumulate != 0);
             }
           }
         }
@@ -953,6 +968,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                        : "memory");
       }
     }
+    ring.drain();
   }
 
   tc_fence_before();
