@@ -233,9 +233,10 @@ def run_ours(args, shape, inp):
         m.moe_combine_bwd(g["dy"], layer.y_perm, layer.topk_w, layer.row_of_slot, T, H, k, layer.dy_perm,
                           layer.d_w); mark(6)
         m.moe_grouped_gemm_down_bwd(layer.dy_perm, layer.h, layer.gu, g["Wd"], E, layer.offsets, None, R, H,
-                                    I, E, layer.dgu, layer.dWd); mark(7)
+                                    I, E, layer.dgu, layer.dWd, 0, layer.ws_gemm_bwd); mark(7)
         m.moe_grouped_gemm_swiglu_bwd(layer.dgu, layer.x_perm, g["Wg"], g["Wu"], E, layer.offsets, None, R,
-                                      H, I, E, layer.dx_perm, layer.dWg, layer.dWu); mark(8)
+                                      H, I, E, layer.dx_perm, layer.dWg, layer.dWu, 0,
+                                      layer.ws_gemm_bwd); mark(8)
         m.moe_dispatch_bwd(layer.dx_perm, layer.row_of_slot, T, H, k, layer.dx_acc); mark(9)
         m.moe_route_topk_bwd(layer.d_w, layer.topk_w, layer.topk_idx, g["x"], g["Wr"], layer.dx_acc, T, H,
                              E, k, layer.dWr, layer.dx, 0, layer.ws_route_bwd); mark(10)
@@ -373,8 +374,9 @@ def run_ours(args, shape, inp):
 
 # kernels launched per step by the calls in run_ours.step():
 # route 3, dispatch 3, gate/up 1, down 1, combine 1, combine_bwd 1,
-# down_bwd 2, gate/up bwd 2, dispatch_bwd 1, route_bwd 6
-KERNELS_PER_STEP = 3 + 3 + 1 + 1 + 1 + 1 + 2 + 2 + 1 + 6
+# down_bwd 3 and gate/up bwd 3 (dX GEMM, segment maps, dW GEMM),
+# dispatch_bwd 1, route_bwd 7
+KERNELS_PER_STEP = 3 + 3 + 1 + 1 + 1 + 1 + 3 + 3 + 1 + 7
 
 
 def run_profile_router(args):

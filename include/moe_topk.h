@@ -42,7 +42,9 @@
  *     MOE_ERR_UNSUPPORTED_SHAPE / MOE_ERR_ALIGNMENT and launch nothing.
  *   - Scratch memory ("workspace", device, caller-owned) is sized by the
  *     matching *_workspace_size query; a smaller ws_bytes returns
- *     MOE_ERR_WORKSPACE.  A workspace may be reused by later calls on the
+ *     MOE_ERR_WORKSPACE.  Workspaces are 16-byte aligned, except those of
+ *     the backward GEMMs and the router backward, which hold TMA
+ *     descriptors and must be 128-byte aligned (else MOE_ERR_ALIGNMENT).  A workspace may be reused by later calls on the
  *     same stream; calls that overlap on the GPU need separate workspaces.
  *   - Index data that lives on the device (topk_idx, offsets, segment
  *     tables) cannot be checked on the host.  Kernels clamp every access
@@ -203,14 +205,20 @@ int moe_combine_bwd(const void* dy, const void* y_perm, const float* topk_w,
                     const int32_t* row_of_slot, int T, int H, int k, void* dy_perm, float* d_w,
                     void* stream);
 
+/* Workspace of B2 and B3: two 128-byte TMA descriptors per segment, which
+ * let the weight-gradient GEMM read each segment's rows with the rows past
+ * its end filled with zeros.  0 when num_seg <= 0. */
+size_t moe_grouped_gemm_bwd_workspace_size(int num_seg);
+
 /* B2  down backward with the SwiGLU backward in its epilogue.
  *   dh = dy_perm[r] . Wd[e]                         (fp32)
  *   with s = sigmoid(g): dg = dh * u * s * (1 + g*(1 - s)),  du = dh * g * s
  *   dgu[r] = [dg | du]                              -> bf16 [R,2I]
  *   dWd[e] = sum over e's rows of dy_perm[r]^T h[r] (fp32 [E,H,I])
  * gu_save is the [g|u] tensor written by moe_grouped_gemm_swiglu.  Experts
- * with no rows get dWd[e] = 0 (or unchanged when accumulate != 0).  ws may be
- * NULL. */
+ * with no rows get dWd[e] = 0 (or unchanged when accumulate != 0).
+ * ws: moe_grouped_gemm_bwd_workspace_size(num_seg) bytes, 128-byte aligned
+ * (the weight-gradient GEMM's per-segment TMA descriptors). */
 int moe_grouped_gemm_down_bwd(const void* dy_perm, const void* h, const void* gu_save,
                               const void* Wd, int num_seg, const int32_t* seg_offsets,
                               const int32_t* seg_expert, int R, int H, int I, int E, void* dgu,
@@ -219,7 +227,8 @@ int moe_grouped_gemm_down_bwd(const void* dy_perm, const void* h, const void* gu
 /* B3  gate/up backward.
  *   dx_perm[r] = dg[r] . Wg[e] + du[r] . Wu[e]   (one fp32 sum over 2I terms) -> bf16 [R,H]
  *   dWg[e] = sum over e's rows of dg[r]^T x_perm[r],  dWu[e] likewise with du  (fp32 [E,I,H])
- * dgu bf16 [R,2I] from moe_grouped_gemm_down_bwd.  ws may be NULL. */
+ * dgu bf16 [R,2I] from moe_grouped_gemm_down_bwd.
+ * ws: moe_grouped_gemm_bwd_workspace_size(num_seg) bytes, 128-byte aligned. */
 int moe_grouped_gemm_swiglu_bwd(const void* dgu, const void* x_perm, const void* Wg,
                                 const void* Wu, int num_seg, const int32_t* seg_offsets,
                                 const int32_t* seg_expert, int R, int H, int I, int E,

@@ -22,7 +22,8 @@ __all__ = ["lib", "MoEError", "LIB_PATH", "ENTRY_POINTS",
            "moe_combine", "moe_combine_bwd", "moe_grouped_gemm_down_bwd",
            "moe_grouped_gemm_swiglu_bwd", "moe_dispatch_bwd", "moe_route_topk_bwd",
            "moe_route_topk_workspace_size", "moe_dispatch_workspace_size",
-           "moe_route_topk_bwd_workspace_size", "moe_read_device_status", "moe_abi_version"]
+           "moe_route_topk_bwd_workspace_size", "moe_grouped_gemm_bwd_workspace_size",
+           "moe_read_device_status", "moe_abi_version"]
 
 LIB_PATH: Path = _build_mod.LIB
 
@@ -43,6 +44,7 @@ ENTRY_POINTS = {
     "moe_grouped_gemm_down": ([_P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _P], _I),
     "moe_combine": ([_P, _P, _P, _I, _I, _I, _P, _P], _I),
     "moe_combine_bwd": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _P], _I),
+    "moe_grouped_gemm_bwd_workspace_size": ([_I], _Z),
     "moe_grouped_gemm_down_bwd": ([_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _Z, _P], _I),
     "moe_grouped_gemm_swiglu_bwd": ([_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _Z, _P],
                                     _I),
@@ -121,6 +123,10 @@ def moe_dispatch_workspace_size(T, E, k) -> int:
 
 def moe_route_topk_bwd_workspace_size(T, H, E) -> int:
     return lib().moe_route_topk_bwd_workspace_size(T, H, E)
+
+
+def moe_grouped_gemm_bwd_workspace_size(num_seg) -> int:
+    return lib().moe_grouped_gemm_bwd_workspace_size(num_seg)
 
 
 def moe_read_device_status(reset: bool = True, stream=None) -> int:

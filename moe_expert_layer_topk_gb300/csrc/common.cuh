@@ -48,9 +48,13 @@ int launch_dense_add_bf16(const void* A, const void* B, const float* add, void* 
                           int K, cudaStream_t stream);
 // out[g] (fp32 [groups, M, N]) = sum over the K rows of segment g of A^T B,
 // with A [K_rows, M] and B [K_rows, N] bf16 row-major (both MN-major).  Used
-// by the router backward (split-K partials, overwrite).
+// by the router backward (split-K partials, overwrite).  `maps` is device
+// scratch of dw_split_maps_bytes(num_seg) bytes, 128-byte aligned, for the
+// per-segment TMA descriptors.
+size_t dw_split_maps_bytes(int num_seg);
 int launch_dw_split(const void* A, const void* B, int K_rows, int M, int N,
-                    const int32_t* seg_offsets, int num_seg, float* out, cudaStream_t stream);
+                    const int32_t* seg_offsets, int num_seg, float* out, void* maps,
+                    cudaStream_t stream);
 
 // ---------------------------------------------------------------- device side
 

@@ -80,6 +80,7 @@ struct Params {
   void* out0;
   void* out1;
   const void* aux;
+  const CUtensorMap* seg_maps;  // DW: per segment s, the A map (2s) and the B map (2s+1)
   int* status;
 };
 
@@ -309,8 +310,10 @@ struct Traits {
 // write each CTA's 128 accumulator rows into that CTA's TMEM.
 template <int KIND, int CTAS>
 struct Cfg {
-  // The SwiGLU-backward kind gives one pipeline stage to its g,u staging.
-  static constexpr bool gu_tma = KIND == DOWN_BWD_DX;
+  // The kinds whose epilogue reads a second input tile by TMA (SwiGLU
+  // backward: saved g, u; router dX: the fp32 addend) give one pipeline
+  // stage to that staging.
+  static constexpr bool gu_tma = KIND == DOWN_BWD_DX || KIND == DENSE_ADD;
   static constexpr int STAGES = CTAS == 1 ? (gu_tma ? 3 : 4) : (gu_tma ? 4 : 6);
   static constexpr int B_BYTES = B_BYTES_MAX / CTAS;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -358,27 +361,38 @@ __device__ __forceinline__ Tile decode_tile(int tile, const Params& p, const Ctl
   return t;
 }
 
-// Calls f(row0, valid_rows) for every k-block of a tile, in order.
+// Calls f(k0, valid_rows, seg) for every k-block of a tile, in order.  Row
+// kinds: k0 is the reduction offset.  DW: k0 is the first row of the k-block
+// counted from the start of segment `seg` (the segment's own tensor maps
+// address rows from there).
 template <int KIND, class F>
 __device__ __forceinline__ void for_each_kblock(const Tile& t, const Params& p, const Ctl* ctl, F&& f) {
   if constexpr (Traits<KIND>::rows) {
     const int nkb = p.K / BK;
     for (int kb = 0; kb < nkb; ++kb)
-      if (!f(kb * BK, BK)) return;
+      if (!f(kb * BK, BK, t.seg)) return;
   } else if (p.seg_expert == nullptr) {
     // identity table: group g owns exactly segment g
-    const int a = ctl->seg_off[t.group], b = ctl->seg_off[t.group + 1];
+    const int len = ctl->seg_off[t.group + 1] - ctl->seg_off[t.group];
     if (ctl->seg_exp[t.group] >= 0)
-      for (int r = a; r < b; r += BK)
-        if (!f(r, min(BK, b - r))) return;
+      for (int r = 0; r < len; r += BK)
+        if (!f(r, min(BK, len - r), t.group)) return;
   } else {
     for (int s = 0; s < p.num_seg; ++s) {
       if (ctl->seg_exp[s] != t.group) continue;
-      const int a = ctl->seg_off[s], b = ctl->seg_off[s + 1];
-      for (int r = a; r < b; r += BK)
-        if (!f(r, min(BK, b - r))) return;
+      const int len = ctl->seg_off[s + 1] - ctl->seg_off[s];
+      for (int r = 0; r < len; r += BK)
+        if (!f(r, min(BK, len - r), s)) return;
     }
   }
+}
+
+// Makes this thread's later TMA loads through `map` see a tensor map that
+// was written in global memory (by the segment-map kernel).
+__device__ __forceinline__ void tmap_acquire(const CUtensorMap* map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(
+                   reinterpret_cast<uint64_t>(map))
+               : "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -594,9 +608,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      int map_seg = -1;  // DW: segment whose maps this thread last acquired
       for (int tile = unit; ok && tile < total; tile += nunits) {
         const Tile t = decode_tile<KIND, CTAS>(tile, p, ctl, rank);
-        for_each_kblock<KIND>(t, p, ctl, [&](int row0, int) -> bool {
+        for_each_kblock<KIND>(t, p, ctl, [&](int row0, int, int seg) -> bool {
           if (!wait_bar(smem_u32(&ctl->empty[stage]), phase ^ 1u, ctl, p.status)) {
             ok = false;
             return false;
@@ -608,8 +623,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (leader) mbar_arrive_expect_tx(fb_local, CTAS * (A_BYTES + b_bytes));
           const int ck0 = rank * (p.BN / 64 / CTAS);  // first MN-major B chunk of this CTA
           if constexpr (KIND == DW) {
-            tma_load_mn<CTAS>(sA, &tmA, fb, row0, t.m0 / 64);
-            tma_load_mn<CTAS>(sB, &tmB0, fb, row0, t.n0 / 64 + ck0);
+            // the segment's own maps end at its last row: TMA fills the
+            // rows of a tail k-block past it with zeros
+            const CUtensorMap* ma = p.seg_maps + 2 * seg;
+            if (seg != map_seg) {
+              tmap_acquire(ma);
+              tmap_acquire(ma + 1);
+              map_seg = seg;
+            }
+            tma_load_mn<CTAS>(sA, ma, fb, row0, t.m0 / 64);
+            tma_load_mn<CTAS>(sB, ma + 1, fb, row0, t.n0 / 64 + ck0);
           } else {
             tma_load<CTAS>(sA, &tmA, fb, row0, t.m0);
             if constexpr (KIND == GATE_UP_FWD) {
@@ -659,51 +682,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(buf * ACC_COLS);
         int nk = 0;
-        for_each_kblock<KIND>(t, p, ctl, [&](int, int valid) -> bool {
+        for_each_kblock<KIND>(t, p, ctl, [&](int, int valid, int) -> bool {
           if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&ctl->full[stage]), phase, ctl, p.status))) {
             ok = false;
             return false;
           }
           uint8_t* sA = smem + (size_t)stage * C::STAGE_BYTES;
           uint8_t* sB = sA + A_BYTES;
-          int nkk = BK / 16;
-          if (KIND == DW && valid < BK) {
-            // Rows past the segment end belong to another group.  Only the
-            // 16-row MMA steps that hold valid rows are issued; inside the
-            // last of them the rows [valid, 16*nkk) are zeroed.  One CTA
-            // zeroes them in both operands; a pair zeroes them in A only, in
-            // both CTAs (a zero A row cancels whatever B holds there).
-            nkk = (valid + 15) / 16;
-            const int nrows = nkk * 16 - valid;
-            if (CTAS == 1) {
-              const int a_chunks = 2, b_chunks = p.BN / 64;
-              const int units = (a_chunks + b_chunks) * nrows * 8;
-              for (int u = lane; u < units; u += 32) {
-                const int chunk = u / (nrows * 8);
-                const int rem = u % (nrows * 8);
-                const int r = valid + rem / 8, c16 = rem % 8;
-                uint8_t* base = chunk < a_chunks ? sA + chunk * CHUNK_BYTES
-                                                 : sB + (chunk - a_chunks) * CHUNK_BYTES;
-                *reinterpret_cast<uint4*>(base + r * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
-              }
-              if (nrows > 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            } else {
-              const int units = 2 /*CTAs*/ * 2 /*A chunks*/ * nrows * 8;
-              for (int u = lane; u < units; u += 32) {
-                const int cta = u / (2 * nrows * 8);
-                const int rem0 = u % (2 * nrows * 8);
-                const int chunk = rem0 / (nrows * 8);
-                const int rem = rem0 % (nrows * 8);
-                const int r = valid + rem / 8, c16 = rem % 8;
-                const uint32_t local_addr = smem_u32(sA + chunk * CHUNK_BYTES + r * 128 + c16 * 16);
-                const uint32_t addr = map_to_rank(local_addr, (uint32_t)cta);
-                asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0)
-                             : "memory");
-              }
-              if (nrows > 0) asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-            }
-            __syncwarp();
-          }
+          // DW tail k-block: the rows past the segment end arrived as zeros;
+          // only the 16-deep MMA steps that hold valid rows are issued.
+          const int nkk = KIND == DW ? (valid + 15) / 16 : BK / 16;
           tc_fence_after();
           if (lane == 0) {
             const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
@@ -783,7 +771,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // out through TMA bulk stores instead (measured faster for those two).
     constexpr bool kTmaOut = KIND == DW || KIND == DOWN_FWD;
     EpRing ring{ep_base, 0, lane};
-    int gu_ctr = 0;  // DOWN_BWD_DX: running count of this warp's 32-column chunks
+    int gu_ctr = 0;  // DOWN_BWD_DX, DENSE_ADD: running count of this warp's 32-column chunks
     const uint32_t tempty_leader[2] = {
         CTAS == 2 ? map_to_rank(smem_u32(&ctl->tempty[0]), 0) : smem_u32(&ctl->tempty[0]),
         CTAS == 2 ? map_to_rank(smem_u32(&ctl->tempty[1]), 0) : smem_u32(&ctl->tempty[1])};
@@ -796,23 +784,25 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int lim = Traits<KIND>::rows ? t.row_end : p.M;
       const int nvalid = lim - rb < 0 ? 0 : (lim - rb > 32 ? 32 : lim - rb);
       const bool any = nvalid > 0;
-      // SwiGLU backward: the saved g, u boxes (32 rows x 32 columns each) of
-      // this warp's rows do not depend on the accumulator.  They arrive by
-      // TMA into set (chunk counter mod 4) of the warp's staging, two chunks
-      // ahead; the first two are requested before waiting for the MMAs.
+      // Second input of the epilogue, which does not depend on the
+      // accumulator: SwiGLU backward reads the saved g, u boxes (32 rows x
+      // 32 bf16 columns each), router dX the fp32 addend (two boxes of 32
+      // rows x 16 columns).  They arrive by TMA into set (chunk counter mod
+      // 4) of the warp's staging, two chunks ahead; the first two are
+      // requested before waiting for the MMAs.
       const uint32_t gu_bar0 = smem_u32(&ctl->ep_bar[warp - 2][0]);
       auto gu_load = [&](int c, int ctr) {
-        if (KIND == DOWN_BWD_DX && any && c < p.BN && lane == 0) {
+        if (C::gu_tma && any && c < p.BN && lane == 0) {
           const int set = ctr & (EP_GU_SETS - 1);
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier reads of the set
           const uint32_t bar = gu_bar0 + 8u * (uint32_t)set;
           const uint32_t g_slot = smem_u32(ep_base + (2 * set) * EP_BOX_BYTES);
           mbar_arrive_expect_tx(bar, 2 * EP_BOX_BYTES);
           tma_load_2d(g_slot, &tmB1, bar, t.n0 + c, rb);
-          tma_load_2d(g_slot + EP_BOX_BYTES, &tmB1, bar, p.I + t.n0 + c, rb);
+          tma_load_2d(g_slot + EP_BOX_BYTES, &tmB1, bar, (KIND == DENSE_ADD ? 16 : p.I) + t.n0 + c, rb);
         }
       };
-      if constexpr (KIND == DOWN_BWD_DX) {
+      if constexpr (C::gu_tma) {
         gu_load(0, gu_ctr);
         gu_load(32, gu_ctr + 1);
       }
@@ -850,9 +840,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             flush(ep_base, p.out1, gu_pitch, (size_t)(p.I + t.n0 + c) * 2, rb, nvalid, false);
           }
         }
-      } else if constexpr (KIND == DOWN_FWD || KIND == GATE_UP_BWD_DX || KIND == DENSE_ADD) {
+      } else if constexpr (KIND == DOWN_FWD || KIND == GATE_UP_BWD_DX) {
         const size_t pitch = (size_t)p.ldo * 2;
-        const int r = rb + lane;
         for (int c = 0; any && c < p.BN; c += 32) {
           uint32_t a[32];
           tmem_ld32(taddr + c, a);
@@ -860,17 +849,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = f32(a[i]);
-          if constexpr (KIND == DENSE_ADD) {
-            if (lane < nvalid) {
-              const float4* add = reinterpret_cast<const float4*>(
-                  static_cast<const float*>(p.aux) + (size_t)r * p.ldo + t.n0 + c);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float4 w = __ldg(add + i);
-                v[4 * i] += w.x; v[4 * i + 1] += w.y; v[4 * i + 2] += w.z; v[4 * i + 3] += w.w;
-              }
-            }
-          }
           uint4 pk[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i)
@@ -888,6 +866,38 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int i = 0; i < 4; ++i) put(bx, i, pk[i]);
             flush(bx, p.out0, pitch, (size_t)(t.n0 + c) * 2, rb, nvalid, false);
           }
+        }
+      } else if constexpr (KIND == DENSE_ADD) {
+        // out = bf16(acc + add): the addend's two 16-column boxes of this
+        // chunk sit in set (gu_ctr mod 4); the result goes out through the
+        // first box of the set.
+        const size_t pitch = (size_t)p.ldo * 2;
+        for (int c = 0; any && c < p.BN; c += 32, ++gu_ctr) {
+          gu_load(c + 64, gu_ctr + 2);
+          uint32_t a[32];
+          tmem_ld32(taddr + c, a);
+          const int set = gu_ctr & (EP_GU_SETS - 1);
+          uint8_t* lo = ep_base + (2 * set) * EP_BOX_BYTES;
+          uint8_t* hi = lo + EP_BOX_BYTES;
+          const bool ok = __all_sync(0xffffffffu, wait_bar(gu_bar0 + 8u * (uint32_t)set,
+                                                           (uint32_t)(gu_ctr >> 2) & 1u, ctl, p.status));
+          tmem_wait_ld();
+          if (!ok) break;
+          uint4 pk[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 w = get(i < 2 ? lo : hi, (2 * i) & 3);
+            const uint4 w2 = get(i < 2 ? lo : hi, (2 * i + 1) & 3);
+            const float* av = reinterpret_cast<const float*>(&a[8 * i]);
+            pk[i] = make_uint4(pack_bf16x2(av[0] + __uint_as_float(w.x), av[1] + __uint_as_float(w.y)),
+                               pack_bf16x2(av[2] + __uint_as_float(w.z), av[3] + __uint_as_float(w.w)),
+                               pack_bf16x2(av[4] + __uint_as_float(w2.x), av[5] + __uint_as_float(w2.y)),
+                               pack_bf16x2(av[6] + __uint_as_float(w2.z), av[7] + __uint_as_float(w2.w)));
+          }
+          __syncwarp();  // every lane has read its addend row before the box is reused
+#pragma unroll
+          for (int i = 0; i < 4; ++i) put(lo, i, pk[i]);
+          flush(lo, p.out0, pitch, (size_t)(t.n0 + c) * 2, rb, nvalid, false);
         }
       } else if constexpr (KIND == DOWN_BWD_DX) {
         const size_t pitch = (size_t)p.I * 4;
@@ -978,6 +988,44 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     tmem_dealloc_n<CTAS>(tmem_base, TMEM_COLS);
   }
+}
+
+// Per-segment operand maps of the weight-gradient GEMM.  Thread i writes
+// map i = 2s (A) or 2s+1 (B): a copy of the MN-major template whose base
+// address is moved to segment s's first row and whose row extent is the
+// segment's length (rows clamped to [0, rows) like the kernel's own table).
+// An empty segment keeps the template unchanged; no k-block ever reads it.
+__global__ void dw_segment_maps_kernel(const __grid_constant__ CUtensorMap tplA,
+                                       const __grid_constant__ CUtensorMap tplB,
+                                       const int32_t* seg_offsets, int num_seg, int rows,
+                                       const uint8_t* baseA, size_t pitchA, const uint8_t* baseB,
+                                       size_t pitchB, CUtensorMap* maps) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= 2 * num_seg) return;
+  const int s = i >> 1;
+  const bool isB = (i & 1) != 0;
+  int a = seg_offsets ? seg_offsets[s] : 0;
+  int b = seg_offsets ? seg_offsets[s + 1] : rows;
+  a = a < 0 ? 0 : (a > rows ? rows : a);
+  b = b < 0 ? 0 : (b > rows ? rows : b);
+  CUtensorMap* m = maps + i;
+  const uint4* src = reinterpret_cast<const uint4*>(isB ? &tplB : &tplA);
+  uint4* dst = reinterpret_cast<uint4*>(m);
+#pragma unroll
+  for (int j = 0; j < (int)(sizeof(CUtensorMap) / sizeof(uint4)); ++j) dst[j] = src[j];
+  if (b > a) {
+    const uint64_t base = reinterpret_cast<uint64_t>(isB ? baseB : baseA) + (uint64_t)a * (isB ? pitchB : pitchA);
+    const uint32_t len = (uint32_t)(b - a);
+    asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "l"(base)
+                 : "memory");
+    asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(len)
+                 : "memory");
+  }
+  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
 }
 
 // --------------------------------------------------------------- host side
@@ -1080,6 +1128,7 @@ int launch(Params p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensor
   p.idesc = make_idesc(p.BN, BM * CTAS, a_mn, b_mn);
   long long upper;
   if (KIND == DW) {
+    p.m_tiles = (p.M + BM * CTAS - 1) / (BM * CTAS);
     upper = (long long)p.num_groups * p.m_tiles * p.n_tiles;
   } else {
     upper = ((long long)(p.M + BM * CTAS - 1) / (BM * CTAS) + p.num_seg) * p.n_tiles;
@@ -1124,6 +1173,37 @@ int run(bool pair, const Params& p, const CUtensorMap& a, const CUtensorMap& b0,
               : launch<KIND, 1>(p, a, b0, b1, o0, o1, s, what);
 }
 
+constexpr size_t kSegMapBytes = 2 * sizeof(CUtensorMap);  // A and B map of one segment
+
+// Weight-gradient GEMM dW[g] = sum over g's rows of A^T B with A bf16
+// [K_rows, M] and B bf16 [K_rows, N] (both MN-major operands): writes the
+// per-segment maps into `maps` (num_seg * kSegMapBytes, 128-byte aligned),
+// then runs the GEMM.  p must hold M, N, K, BN, n_tiles and the outputs.
+int run_dw(bool pair, Params p, const void* A, const void* B, const CUtensorMap& o0,
+           const CUtensorMap& o1, void* maps, cudaStream_t s, const char* what) {
+  CUtensorMap ta, tb;
+  const uint32_t nckB = p.BN / 64 / (pair ? 2 : 1);
+  if (int rc = make_tmap_mn(&ta, A, p.M, p.K, BM / 64)) return rc;
+  if (int rc = make_tmap_mn(&tb, B, p.N, p.K, nckB)) return rc;
+  const int nmaps = 2 * p.num_seg;
+  dw_segment_maps_kernel<<<(nmaps + 127) / 128, 128, 0, s>>>(
+      ta, tb, p.seg_offsets, p.num_seg, p.K, static_cast<const uint8_t*>(A), (size_t)p.M * 2,
+      static_cast<const uint8_t*>(B), (size_t)p.N * 2, static_cast<CUtensorMap*>(maps));
+  if (int rc = check_launch(what)) return rc;
+  p.seg_maps = static_cast<const CUtensorMap*>(maps);
+  return run<DW>(pair, p, ta, tb, tb, o0, o1, s, what);
+}
+
+// The backward GEMMs' workspace: the per-segment maps.
+int check_bwd_ws(const char* fn, int num_seg, const void* ws, size_t ws_bytes) {
+  const size_t need = (size_t)num_seg * kSegMapBytes;
+  if (num_seg > 0 && (!ws || ws_bytes < need))
+    return fail(MOE_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws ? ws_bytes : (size_t)0, need);
+  if (ws && (reinterpret_cast<uintptr_t>(ws) & 127u))
+    return fail(MOE_ERR_ALIGNMENT, "%s: ws must be 128-byte aligned", fn);
+  return MOE_OK;
+}
+
 int check_grouped(const char* fn, int num_seg, const int32_t* seg_offsets, int R, int H, int I, int E) {
   if (R < 0 || H <= 0 || I <= 0 || E <= 0 || num_seg < 0)
     return fail(MOE_ERR_INVALID_ARG, "%s: need R>=0, H>0, I>0, E>0, num_seg>=0", fn);
@@ -1166,13 +1246,17 @@ int launch_dense_add_bf16(const void* A, const void* B, const float* add, void* 
   CUtensorMap ta, tb;
   if (int rc = make_tmap(&ta, A, K, M, 64, BM)) return rc;
   if (int rc = make_tmap(&tb, B, K, N, 64, p.BN)) return rc;
-  CUtensorMap to;
+  CUtensorMap to, tadd;
   if (int rc = make_out_map(&to, out, N, M, false)) return rc;
-  return run<DENSE_ADD>(false, p, ta, tb, tb, to, to, stream, "router backward dx GEMM");
+  if (int rc = make_out_map(&tadd, add, N, M, true)) return rc;  // addend boxes in
+  return run<DENSE_ADD>(false, p, ta, tb, tadd, to, to, stream, "router backward dx GEMM");
 }
 
+size_t dw_split_maps_bytes(int num_seg) { return (size_t)num_seg * tc::kSegMapBytes; }
+
 int launch_dw_split(const void* A, const void* B, int K_rows, int M, int N,
-                    const int32_t* seg_offsets, int num_seg, float* out, cudaStream_t stream) {
+                    const int32_t* seg_offsets, int num_seg, float* out, void* maps,
+                    cudaStream_t stream) {
   using namespace tc;
   Params p = base_params(num_seg, seg_offsets, nullptr, num_seg);
   p.M = M;
@@ -1180,15 +1264,11 @@ int launch_dw_split(const void* A, const void* B, int K_rows, int M, int N,
   p.K = K_rows;
   p.BN = pick_bn(N);
   p.n_tiles = N / p.BN;
-  p.m_tiles = (M + BM - 1) / BM;
   p.ldo = N;
   p.out0 = out;
-  CUtensorMap ta, tb;
-  if (int rc = make_tmap_mn(&ta, A, M, K_rows, BM / 64)) return rc;
-  if (int rc = make_tmap_mn(&tb, B, N, K_rows, p.BN / 64)) return rc;
   CUtensorMap to;
   if (int rc = make_out_map(&to, out, N, (uint64_t)num_seg * M, true)) return rc;
-  return run<DW>(false, p, ta, tb, tb, to, to, stream, "router backward dWr GEMM");
+  return run_dw(false, p, A, B, to, to, maps, stream, "router backward dWr GEMM");
 }
 
 }  // namespace moe
@@ -1197,6 +1277,10 @@ using namespace moe;
 using namespace moe::tc;
 
 extern "C" {
+
+size_t moe_grouped_gemm_bwd_workspace_size(int num_seg) {
+  return num_seg > 0 ? (size_t)num_seg * kSegMapBytes : 0;
+}
 
 int moe_grouped_gemm_swiglu(const void* x_perm, const void* Wg, const void* Wu, int num_seg,
                             const int32_t* seg_offsets, const int32_t* seg_expert, int R, int H,
@@ -1265,7 +1349,6 @@ int moe_grouped_gemm_down_bwd(const void* dy_perm, const void* h, const void* gu
                               const void* Wd, int num_seg, const int32_t* seg_offsets,
                               const int32_t* seg_expert, int R, int H, int I, int E, void* dgu,
                               float* dWd, int accumulate, void* ws, size_t ws_bytes, void* stream) {
-  (void)ws; (void)ws_bytes;
   clear_error();
   const char* fn = "moe_grouped_gemm_down_bwd";
   if (int rc = check_grouped(fn, num_seg, seg_offsets, R, H, I, E)) return rc;
@@ -1274,6 +1357,7 @@ int moe_grouped_gemm_down_bwd(const void* dy_perm, const void* h, const void* gu
   if (!aligned16(dy_perm) || !aligned16(h) || !aligned16(gu_save) || !aligned16(Wd) ||
       !aligned16(dgu) || !aligned16(dWd))
     return fail(MOE_ERR_ALIGNMENT, "%s: tensors must be 16-byte aligned", fn);
+  if (int rc = check_bwd_ws(fn, num_seg, ws, ws_bytes)) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (R > 0 && num_seg > 0) {
     // dgu = SwiGLU'(dy_perm . Wd[e])
@@ -1308,16 +1392,12 @@ int moe_grouped_gemm_down_bwd(const void* dy_perm, const void* h, const void* gu
   p.K = R;
   p.BN = pick_bn(I);
   p.n_tiles = I / p.BN;
-  p.m_tiles = (H + BM - 1) / BM;
   p.ldo = I;
   p.accumulate = accumulate;
   p.out0 = dWd;
-  CUtensorMap ta, tb;
-  if (int rc = make_tmap_mn(&ta, dy_perm, H, R, BM / 64)) return rc;
-  if (int rc = make_tmap_mn(&tb, h, I, R, p.BN / 64)) return rc;
   CUtensorMap to;
   if (int rc = make_out_map(&to, dWd, I, (uint64_t)E * H, true)) return rc;
-  return run<DW>(false, p, ta, tb, tb, to, to, s, fn);
+  return run_dw(pair_for<DW>(p.BN), p, dy_perm, h, to, to, ws, s, fn);
 }
 
 int moe_grouped_gemm_swiglu_bwd(const void* dgu, const void* x_perm, const void* Wg,
@@ -1325,7 +1405,6 @@ int moe_grouped_gemm_swiglu_bwd(const void* dgu, const void* x_perm, const void*
                                 const int32_t* seg_expert, int R, int H, int I, int E,
                                 void* dx_perm, float* dWg, float* dWu, int accumulate, void* ws,
                                 size_t ws_bytes, void* stream) {
-  (void)ws; (void)ws_bytes;
   clear_error();
   const char* fn = "moe_grouped_gemm_swiglu_bwd";
   if (int rc = check_grouped(fn, num_seg, seg_offsets, R, H, I, E)) return rc;
@@ -1334,6 +1413,7 @@ int moe_grouped_gemm_swiglu_bwd(const void* dgu, const void* x_perm, const void*
   if (!aligned16(dgu) || !aligned16(x_perm) || !aligned16(Wg) || !aligned16(Wu) ||
       !aligned16(dx_perm) || !aligned16(dWg) || !aligned16(dWu))
     return fail(MOE_ERR_ALIGNMENT, "%s: tensors must be 16-byte aligned", fn);
+  if (int rc = check_bwd_ws(fn, num_seg, ws, ws_bytes)) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (R > 0 && num_seg > 0) {
     // dx_perm = [dg du] . [Wg[e]; Wu[e]]
@@ -1370,19 +1450,15 @@ int moe_grouped_gemm_swiglu_bwd(const void* dgu, const void* x_perm, const void*
   p.K = R;
   p.BN = pick_bn(H);
   p.n_tiles = H / p.BN;
-  p.m_tiles = (2 * I + BM - 1) / BM;
   p.split_m = I;
   p.ldo = H;
   p.accumulate = accumulate;
   p.out0 = dWg;
   p.out1 = dWu;
-  CUtensorMap ta, tb;
-  if (int rc = make_tmap_mn(&ta, dgu, 2 * I, R, BM / 64)) return rc;
-  if (int rc = make_tmap_mn(&tb, x_perm, H, R, p.BN / 64)) return rc;
   CUtensorMap tog, tou;
   if (int rc = make_out_map(&tog, dWg, H, (uint64_t)E * I, true)) return rc;
   if (int rc = make_out_map(&tou, dWu, H, (uint64_t)E * I, true)) return rc;
-  return run<DW>(false, p, ta, tb, tb, tog, tou, s, fn);
+  return run_dw(pair_for<DW>(p.BN), p, dgu, x_perm, tog, tou, ws, s, fn);
 }
 
 }  // extern "C"

@@ -383,7 +383,7 @@ int route_ws_layout(int T, int E, size_t* logits_bytes, size_t* hist_bytes) {
 
 struct BwdLayout {
   int Ep, S;
-  size_t dl2, dl3, wr3, seg, part, total;
+  size_t dl2, dl3, wr3, seg, part, maps, total;
 };
 
 BwdLayout bwd_layout(int T, int H, int E) {
@@ -402,6 +402,7 @@ BwdLayout bwd_layout(int T, int H, int E) {
   L.wr3 = off; off += align256(sizeof(__nv_bfloat16) * (size_t)H * 3 * L.Ep);
   L.seg = off; off += align256(sizeof(int32_t) * (size_t)(S + 1));
   L.part = off; off += align256(sizeof(float) * (size_t)S * H * 2 * L.Ep);
+  L.maps = off; off += align256(dw_split_maps_bytes(S));
   L.total = off;
   return L;
 }
@@ -493,8 +494,9 @@ int moe_route_topk_bwd(const float* d_w, const float* topk_w, const int32_t* top
   if (!dWr || !ws || (T > 0 && (!d_w || !topk_w || !topk_idx || !x || !Wr || !dx_acc || !dx)))
     return fail(MOE_ERR_INVALID_ARG, "moe_route_topk_bwd: NULL pointer argument");
   if (!aligned16(x) || !aligned16(Wr) || !aligned16(dx_acc) || !aligned16(dWr) || !aligned16(dx) ||
-      !aligned16(ws))
-    return fail(MOE_ERR_ALIGNMENT, "moe_route_topk_bwd: tensors and ws must be 16-byte aligned");
+      (reinterpret_cast<uintptr_t>(ws) & 127u))
+    return fail(MOE_ERR_ALIGNMENT,
+                "moe_route_topk_bwd: tensors must be 16-byte and ws 128-byte aligned");
   const BwdLayout L = bwd_layout(T, H, E);
   if (ws_bytes < L.total)
     return fail(MOE_ERR_WORKSPACE, "moe_route_topk_bwd: workspace %zu < %zu bytes", ws_bytes, L.total);
@@ -526,7 +528,7 @@ int moe_route_topk_bwd(const float* d_w, const float* topk_w, const int32_t* top
   // dx = bf16(dx_acc + dl . Wr^T)
   if (int rc = launch_dense_add_bf16(dl3, wr3, dx_acc, dx, T, H, 3 * L.Ep, s)) return rc;
   // split-K partials of x^T . [dl_hi | dl_lo]
-  if (int rc = launch_dw_split(x, dl2, T, H, 2 * L.Ep, seg, L.S, part, s)) return rc;
+  if (int rc = launch_dw_split(x, dl2, T, H, 2 * L.Ep, seg, L.S, part, base + L.maps, s)) return rc;
   const size_t nred = (size_t)H * E;
   router_bwd_reduce_kernel<<<(int)((nred + 255) / 256 < 4096 ? (nred + 255) / 256 : 4096), 256, 0,
                              s>>>(part, L.S, H, E, L.Ep, dWr, accumulate);

@@ -10,7 +10,8 @@ from __future__ import annotations
 import torch
 
 from . import (moe_combine, moe_combine_bwd, moe_dispatch, moe_dispatch_bwd,
-               moe_dispatch_workspace_size, moe_grouped_gemm_down, moe_grouped_gemm_down_bwd,
+               moe_dispatch_workspace_size, moe_grouped_gemm_bwd_workspace_size,
+               moe_grouped_gemm_down, moe_grouped_gemm_down_bwd,
                moe_grouped_gemm_swiglu, moe_grouped_gemm_swiglu_bwd, moe_route_topk,
                moe_route_topk_bwd, moe_route_topk_bwd_workspace_size,
                moe_route_topk_workspace_size)
@@ -57,6 +58,7 @@ class MoELayer:
             self.dWd = e(E, H, I, dt=f32)
             self.dWr = e(H, E, dt=f32)
             self.ws_route_bwd = _ws(moe_route_topk_bwd_workspace_size(T, H, E), dev)
+            self.ws_gemm_bwd = _ws(moe_grouped_gemm_bwd_workspace_size(E), dev)
 
     # ---------------------------------------------------------------- forward
     def route(self, x, Wr, bias=None, stream=None):
@@ -92,9 +94,10 @@ class MoELayer:
         moe_combine_bwd(dy, self.y_perm, self.topk_w, self.row_of_slot, T, H, k, self.dy_perm,
                         self.d_w, stream)
         moe_grouped_gemm_down_bwd(self.dy_perm, self.h, self.gu, Wd, E, self.offsets, None, R, H, I,
-                                  E, self.dgu, self.dWd, accumulate, None, stream)
+                                  E, self.dgu, self.dWd, accumulate, self.ws_gemm_bwd, stream)
         moe_grouped_gemm_swiglu_bwd(self.dgu, self.x_perm, Wg, Wu, E, self.offsets, None, R, H, I, E,
-                                    self.dx_perm, self.dWg, self.dWu, accumulate, None, stream)
+                                    self.dx_perm, self.dWg, self.dWu, accumulate, self.ws_gemm_bwd,
+                                    stream)
         moe_dispatch_bwd(self.dx_perm, self.row_of_slot, T, H, k, self.dx_acc, stream)
         moe_route_topk_bwd(self.d_w, self.topk_w, self.topk_idx, x, Wr, self.dx_acc, T, H, E, k,
                            self.dWr, self.dx, accumulate, self.ws_route_bwd, stream)

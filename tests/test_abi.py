@@ -76,6 +76,16 @@ def test_grouped_gemm_rejects_bad_shapes(L):
                                        None) == INVALID
     assert L.moe_grouped_gemm_swiglu_bwd(P, P, P, P, 8, P, None, 64, 128, 96, 8, P, P, P, 0, None, 0,
                                          None) == SHAPE
+    # the backward GEMMs need 256 bytes of 128-byte aligned workspace per segment
+    assert L.moe_grouped_gemm_bwd_workspace_size(8) == 8 * 256
+    assert L.moe_grouped_gemm_bwd_workspace_size(0) == 0
+    assert L.moe_grouped_gemm_down_bwd(P, P, P, P, 8, P, None, 64, 128, 64, 8, P, P, 0, None, 0,
+                                       None) == WS
+    assert "workspace" in _err(L)
+    assert L.moe_grouped_gemm_swiglu_bwd(P, P, P, P, 8, P, None, 64, 128, 64, 8, P, P, P, 0, P, 2047,
+                                         None) == WS
+    assert L.moe_grouped_gemm_down_bwd(P, P, P, P, 8, P, None, 64, 128, 64, 8, P, P, 0, P + 64, 4096,
+                                       None) == ALIGN
 
 
 def test_rows_ops_reject_bad_args(L):

@@ -128,8 +128,9 @@ def test_segmented_rows(R, H, I, E, S):
     dx = torch.zeros(R, H, dtype=torch.bfloat16, device=dev)
     dWg = torch.empty(E, I, H, device=dev)
     dWu = torch.empty(E, I, H, device=dev)
-    m.moe_grouped_gemm_down_bwd(dy, h, gu, Wd, nseg, so_d, se_d, R, H, I, E, dgu, dWd)
-    m.moe_grouped_gemm_swiglu_bwd(dgu, xp, Wg, Wu, nseg, so_d, se_d, R, H, I, E, dx, dWg, dWu)
+    ws = torch.empty(m.moe_grouped_gemm_bwd_workspace_size(nseg), dtype=torch.uint8, device=dev)
+    m.moe_grouped_gemm_down_bwd(dy, h, gu, Wd, nseg, so_d, se_d, R, H, I, E, dgu, dWd, 0, ws)
+    m.moe_grouped_gemm_swiglu_bwd(dgu, xp, Wg, Wu, nseg, so_d, se_d, R, H, I, E, dx, dWg, dWu, 0, ws)
     torch.cuda.synchronize()
     assert m.moe_read_device_status(reset=True) == 0
     son, sen = so.numpy(), se.numpy()
