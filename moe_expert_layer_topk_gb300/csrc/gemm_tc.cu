@@ -55,7 +55,6 @@ constexpr int EP_SLOTS = 2;
 constexpr int EP_WARP_BYTES = EP_BOX_BYTES * EP_SLOTS;
 // DOWN_BWD_DX also loads the saved g, u boxes by TMA: 4 sets of (g, u) slots.
 constexpr int EP_GU_SETS = 4;
-constexpr int EP_GU_WARP_BYTES = EP_BOX_BYTES * 2 * EP_GU_SETS;
 
 enum Kind : int { GATE_UP_FWD = 0, DOWN_FWD = 1, DOWN_BWD_DX = 2, GATE_UP_BWD_DX = 3, DW = 4, DENSE_ADD = 5 };
 
@@ -93,12 +92,20 @@ struct Ctl {
   uint32_t tmem_base;
   int abort_flag;
   int total_tiles;
-  int seg_tiles[kMaxSegments + 1];  // prefix sum of 128-row tiles per segment
-  int seg_off[kMaxSegments + 1];
-  int seg_exp[kMaxSegments];
-  int grp_rows[kMaxSegments];       // DW: rows per output group
-  unsigned long long ep_bar[4][EP_GU_SETS];  // DOWN_BWD_DX: g,u box loads per epilogue warp
+  // Segment tables, in the shared memory right after this struct, sized by
+  // the launch: num_seg + 1, num_seg + 1, num_seg and (DW) num_groups ints.
+  int* seg_off;
+  int* seg_tiles;                   // prefix sum of tiles per segment (row kinds)
+  int* seg_exp;
+  int* grp_rows;                    // DW: rows per output group
+  unsigned long long ep_bar[4][EP_GU_SETS];  // g,u / addend box loads per epilogue warp
 };
+
+// Bytes of the segment tables that follow Ctl.
+__host__ __device__ constexpr size_t seg_table_bytes(int num_seg, int num_groups, bool dw) {
+  return ((size_t)(3 * num_seg + 2 + (dw ? num_groups : 0)) * 4 + 15) / 16 * 16;
+}
+constexpr size_t kMaxTableBytes = seg_table_bytes(kMaxSegments, kMaxExperts, true);
 
 
 
@@ -308,23 +315,35 @@ struct Traits {
 // holds its own 128 rows of A and half of the B tile's N range; the leader
 // (cluster rank 0) issues the MMAs, which read both CTAs' shared memory and
 // write each CTA's 128 accumulator rows into that CTA's TMEM.
-template <int KIND, int CTAS>
+//
+// The kinds whose epilogue reads a second input tile by TMA (SwiGLU
+// backward: saved g, u; router dX: the fp32 addend) stage GU_SETS sets of
+// it, GU_SETS/2 chunks ahead, and run one pipeline stage fewer.  DEEP (the
+// SwiGLU-backward kind, when the segment tables are small enough) keeps all
+// four stages and stages two sets, one chunk ahead.
+template <int KIND, int CTAS, bool DEEP = false>
 struct Cfg {
-  // The kinds whose epilogue reads a second input tile by TMA (SwiGLU
-  // backward: saved g, u; router dX: the fp32 addend) give one pipeline
-  // stage to that staging.
   static constexpr bool gu_tma = KIND == DOWN_BWD_DX || KIND == DENSE_ADD;
-  static constexpr int STAGES = CTAS == 1 ? (gu_tma ? 3 : 4) : (gu_tma ? 4 : 6);
+  static constexpr int GU_SETS = DEEP ? 2 : EP_GU_SETS;
+  static constexpr int STAGES = CTAS == 1 ? ((gu_tma && !DEEP) ? 3 : 4) : (gu_tma ? 4 : 6);
   static constexpr int B_BYTES = B_BYTES_MAX / CTAS;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TILE_M = BM * CTAS;
-  static constexpr int EP_WARP = gu_tma ? EP_GU_WARP_BYTES : EP_WARP_BYTES;
+  static constexpr int EP_WARP = gu_tma ? EP_BOX_BYTES * 2 * GU_SETS : EP_WARP_BYTES;
   static constexpr int EP_TOTAL = 4 * EP_WARP;
-  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + EP_TOTAL + sizeof(Ctl);
+  // without the segment tables
+  static constexpr size_t SMEM_FIXED = 1024 + (size_t)STAGES * STAGE_BYTES + EP_TOTAL + sizeof(Ctl);
 };
-static_assert(Cfg<GATE_UP_FWD, 1>::SMEM <= 232448 && Cfg<GATE_UP_FWD, 2>::SMEM <= 232448 &&
-                  Cfg<DOWN_BWD_DX, 1>::SMEM <= 232448 && Cfg<DOWN_BWD_DX, 2>::SMEM <= 232448,
+constexpr size_t kSmemMax = 232448;
+static_assert(Cfg<GATE_UP_FWD, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
+                  Cfg<GATE_UP_FWD, 2>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
+                  Cfg<DOWN_BWD_DX, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
+                  Cfg<DOWN_BWD_DX, 2>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
+                  Cfg<DENSE_ADD, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
+                  Cfg<DW, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax,
               "shared memory budget exceeded");
+static_assert(Cfg<DOWN_BWD_DX, 1, true>::SMEM_FIXED + seg_table_bytes(128, 0, false) <= kSmemMax,
+              "the deep SwiGLU-backward configuration must fit 128 segments");
 
 struct Tile {
   int group;   // expert (row kinds) / output group (DW)
@@ -496,14 +515,14 @@ __device__ __forceinline__ void tmem_dealloc_n(uint32_t taddr, uint32_t ncols) {
   }
 }
 
-template <int KIND, int CTAS>
+template <int KIND, int CTAS, bool DEEP>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB0,
                         const __grid_constant__ CUtensorMap tmB1,
                         const __grid_constant__ CUtensorMap tmO0,
                         const __grid_constant__ CUtensorMap tmO1, const Params p) {
-  using C = Cfg<KIND, CTAS>;
+  using C = Cfg<KIND, CTAS, DEEP>;
   constexpr int STG = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -517,6 +536,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int nunits = CTAS == 2 ? (int)gridDim.x / 2 : (int)gridDim.x;
 
   // ---- segment table -> shared memory (clamped; bad entries become empty)
+  {
+    int* tab = reinterpret_cast<int*>(ctl + 1);
+    if (threadIdx.x == 0) {
+      ctl->seg_off = tab;
+      ctl->seg_tiles = tab + p.num_seg + 1;
+      ctl->seg_exp = tab + 2 * (p.num_seg + 1);
+      ctl->grp_rows = tab + 3 * p.num_seg + 2;
+    }
+    __syncthreads();
+  }
   for (int s = threadIdx.x; s <= p.num_seg; s += THREADS) {
     // a null table means one segment covering every row
     int o = p.seg_offsets ? p.seg_offsets[s] : (s == 0 ? 0 : limit);
@@ -793,7 +822,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t gu_bar0 = smem_u32(&ctl->ep_bar[warp - 2][0]);
       auto gu_load = [&](int c, int ctr) {
         if (C::gu_tma && any && c < p.BN && lane == 0) {
-          const int set = ctr & (EP_GU_SETS - 1);
+          const int set = ctr & (C::GU_SETS - 1);
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier reads of the set
           const uint32_t bar = gu_bar0 + 8u * (uint32_t)set;
           const uint32_t g_slot = smem_u32(ep_base + (2 * set) * EP_BOX_BYTES);
@@ -802,9 +831,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           tma_load_2d(g_slot + EP_BOX_BYTES, &tmB1, bar, (KIND == DENSE_ADD ? 16 : p.I) + t.n0 + c, rb);
         }
       };
+      constexpr int GU_AHEAD = C::GU_SETS / 2;  // chunks requested ahead
       if constexpr (C::gu_tma) {
-        gu_load(0, gu_ctr);
-        gu_load(32, gu_ctr + 1);
+#pragma unroll
+        for (int a = 0; a < GU_AHEAD; ++a) gu_load(32 * a, gu_ctr + a);
       }
       if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&ctl->tfull[buf]), use & 1u, ctl, p.status))) break;
       tc_fence_after();
@@ -873,14 +903,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         // first box of the set.
         const size_t pitch = (size_t)p.ldo * 2;
         for (int c = 0; any && c < p.BN; c += 32, ++gu_ctr) {
-          gu_load(c + 64, gu_ctr + 2);
+          gu_load(c + 32 * GU_AHEAD, gu_ctr + GU_AHEAD);
           uint32_t a[32];
           tmem_ld32(taddr + c, a);
-          const int set = gu_ctr & (EP_GU_SETS - 1);
+          const int set = gu_ctr & (C::GU_SETS - 1);
           uint8_t* lo = ep_base + (2 * set) * EP_BOX_BYTES;
           uint8_t* hi = lo + EP_BOX_BYTES;
           const bool ok = __all_sync(0xffffffffu, wait_bar(gu_bar0 + 8u * (uint32_t)set,
-                                                           (uint32_t)(gu_ctr >> 2) & 1u, ctl, p.status));
+                                                           (uint32_t)(gu_ctr / C::GU_SETS) & 1u, ctl, p.status));
           tmem_wait_ld();
           if (!ok) break;
           uint4 pk[4];
@@ -902,14 +932,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       } else if constexpr (KIND == DOWN_BWD_DX) {
         const size_t pitch = (size_t)p.I * 4;
         for (int c = 0; any && c < p.BN; c += 32, ++gu_ctr) {
-          gu_load(c + 64, gu_ctr + 2);
+          gu_load(c + 32 * GU_AHEAD, gu_ctr + GU_AHEAD);
           uint32_t a[32];
           tmem_ld32(taddr + c, a);
-          const int set = gu_ctr & (EP_GU_SETS - 1);
+          const int set = gu_ctr & (C::GU_SETS - 1);
           uint8_t* gbox = ep_base + (2 * set) * EP_BOX_BYTES;
           uint8_t* ubox = gbox + EP_BOX_BYTES;
           const bool ok = __all_sync(0xffffffffu, wait_bar(gu_bar0 + 8u * (uint32_t)set,
-                                                           (uint32_t)(gu_ctr >> 2) & 1u, ctl, p.status));
+                                                           (uint32_t)(gu_ctr / C::GU_SETS) & 1u, ctl, p.status));
           tmem_wait_ld();
           if (!ok) break;
 #pragma unroll
@@ -1115,12 +1145,13 @@ bool use_pair(int bn) { return bn >= 128; }
 template <int KIND>
 bool pair_for(int bn) { return KIND == GATE_UP_BWD_DX && use_pair(bn); }
 
-bool g_attr[6][2][64] = {};
+bool g_attr[6][2][2][64] = {};
 
-// Launches grouped_gemm_kernel<KIND, CTAS>: completes the CTAS-dependent
-// parameters, sizes the persistent grid to the SM count and, for pairs, sets
-// the cluster dimension.
-template <int KIND, int CTAS>
+// Launches grouped_gemm_kernel<KIND, CTAS, DEEP>: completes the
+// CTAS-dependent parameters, sizes the shared memory to the segment tables
+// and the persistent grid to the SM count and, for pairs, sets the cluster
+// dimension.
+template <int KIND, int CTAS, bool DEEP = false>
 int launch(Params p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
            const CUtensorMap& o0, const CUtensorMap& o1, cudaStream_t s, const char* what) {
   constexpr bool a_mn = KIND == DW;
@@ -1135,12 +1166,14 @@ int launch(Params p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensor
   }
   const int dev = current_device();
   if (dev < 0) return fail(MOE_ERR_CUDA, "%s: no current CUDA device", what);
-  auto kern = grouped_gemm_kernel<KIND, CTAS>;
-  const int smem = (int)Cfg<KIND, CTAS>::SMEM;
-  if (!g_attr[KIND][CTAS - 1][dev]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto kern = grouped_gemm_kernel<KIND, CTAS, DEEP>;
+  const size_t smem_sz = Cfg<KIND, CTAS, DEEP>::SMEM_FIXED + seg_table_bytes(p.num_seg, p.num_groups, KIND == DW);
+  if (smem_sz > kSmemMax) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "%s: segment tables too large", what);
+  const int smem = (int)smem_sz;
+  if (!g_attr[KIND][CTAS - 1][DEEP][dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMax);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
-    g_attr[KIND][CTAS - 1][dev] = true;
+    g_attr[KIND][CTAS - 1][DEEP][dev] = true;
   }
   const int sms = sm_count();
   if (sms <= 0) return fail(MOE_ERR_CUDA, "%s: cannot query the SM count", what);
@@ -1166,11 +1199,20 @@ int launch(Params p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensor
   return check_launch(what);
 }
 
+// Cluster pairs are built only for the gate/up backward dX GEMM; the
+// SwiGLU-backward GEMM runs its deep configuration whenever its segment
+// tables leave room for it.
 template <int KIND>
 int run(bool pair, const Params& p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
         const CUtensorMap& o0, const CUtensorMap& o1, cudaStream_t s, const char* what) {
-  return pair ? launch<KIND, 2>(p, a, b0, b1, o0, o1, s, what)
-              : launch<KIND, 1>(p, a, b0, b1, o0, o1, s, what);
+  if constexpr (KIND == GATE_UP_BWD_DX) {
+    if (pair) return launch<KIND, 2>(p, a, b0, b1, o0, o1, s, what);
+  }
+  if constexpr (KIND == DOWN_BWD_DX) {
+    if (Cfg<KIND, 1, true>::SMEM_FIXED + seg_table_bytes(p.num_seg, p.num_groups, false) <= kSmemMax)
+      return launch<KIND, 1, true>(p, a, b0, b1, o0, o1, s, what);
+  }
+  return launch<KIND, 1>(p, a, b0, b1, o0, o1, s, what);
 }
 
 constexpr size_t kSegMapBytes = 2 * sizeof(CUtensorMap);  // A and B map of one segment
