@@ -16,20 +16,29 @@ namespace {
 
 // ------------------------------------------------------------ logits kernel
 //
-// CTA = 2 warps over 32 tokens x 32 experts; thread = 4 tokens x 4 experts.
-// h advances in stages of 32 positions: a 4-deep cp.async pipeline brings
-// the Wr tile [32 h][32 e] (fp32) and the x tile [32 tokens][32 h] (bf16)
-// into shared memory; x is widened once per stage into a transposed fp32
-// tile [32 h][32 tokens].  Each thread keeps, per output, the fused
-// multiply-add chain of the current 256-wide h-block and the running sum of
-// the finished blocks: exactly the order of the reading (block partials in
-// increasing h from 0, block sums added left to right, bias last).
-constexpr int kLogitTok = 32;
-constexpr int kLogitExp = 32;
-constexpr int kLogitThreads = 64;
+// The reading's summation order makes every 256-wide h-block an independent
+// fused multiply-add chain from 0; the block partials are then added left to
+// right and the bias last.  This kernel computes the partials: one CTA per
+// (64 tokens, one h-block, 128 experts), written to part[block][t][e]; the
+// top-k kernel adds them in order.  Splitting over h-blocks gives enough
+// CTAs to fill the GPU evenly and keeps only the 64 running chains of a
+// thread in registers.
+//
+// CTA = 4 warps; thread = 8 tokens x 8 experts (tg = tid % 8, eg = tid / 8):
+// tokens 4tg..4tg+3 and 32+4tg..32+4tg+3 (so the eight tg of a warp read 128
+// contiguous bytes of xs per load, free of bank conflicts), experts
+// 8eg..8eg+7.
+// h advances in stages of 32: a 3-deep cp.async pipeline brings the Wr tile
+// [32 h][128 e] (fp32) into shared memory; the x tile [64 tokens][32 h]
+// (bf16) is read into registers one stage ahead, widened and stored
+// transposed as xs[32 h][64 tokens] (two buffers).
+constexpr int kLogitTok = 64;
+constexpr int kLogitExp = 128;
+constexpr int kLogitThreads = 128;
 constexpr int kLogitStage = 32;   // h per stage
 constexpr int kLogitBlockH = 256; // h per summation block
-constexpr int kLogitDepth = 4;    // stages in flight
+constexpr int kLogitDepth = 3;    // W stages in flight
+constexpr size_t kLogitSmem = sizeof(float) * (kLogitDepth * kLogitStage * kLogitExp + 2 * kLogitStage * kLogitTok);
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
@@ -47,26 +56,32 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 template <bool kVec>
-__global__ void __launch_bounds__(kLogitThreads) router_logits_kernel(
-    const __nv_bfloat16* __restrict__ x, const float* __restrict__ Wr, const float* __restrict__ bias,
-    int T, int H, int E, float* __restrict__ logits) {
-  __shared__ __align__(16) float ws[kLogitDepth][kLogitStage][kLogitExp];
-  __shared__ __align__(16) __nv_bfloat16 xraw[kLogitDepth][kLogitTok][kLogitStage];
-  __shared__ __align__(16) float xs[kLogitStage][kLogitTok];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int tg = lane & 7, eg = lane >> 3;
-  const int t0 = blockIdx.x * kLogitTok, e0 = blockIdx.y * kLogitExp;
-  const int my_tok = tg * 4, my_exp = warp * 16 + eg * 4;
-  const int nstage = H / kLogitStage;
+__global__ void __launch_bounds__(kLogitThreads) router_partials_kernel(
+    const __nv_bfloat16* __restrict__ x, const float* __restrict__ Wr, int T, int H, int E,
+    float* __restrict__ part) {
+  extern __shared__ __align__(16) float lsm[];
+  float(*ws)[kLogitStage][kLogitExp] = reinterpret_cast<float(*)[kLogitStage][kLogitExp]>(lsm);
+  float(*xs)[kLogitStage][kLogitTok] =
+      reinterpret_cast<float(*)[kLogitStage][kLogitTok]>(lsm + kLogitDepth * kLogitStage * kLogitExp);
+  const int tid = threadIdx.x;
+  const int tg = tid & 7, eg = tid >> 3;
+  const int t0 = blockIdx.x * kLogitTok, blk = blockIdx.y, e0 = blockIdx.z * kLogitExp;
+  const int hb0 = blk * kLogitBlockH;
+  const int hb1 = min(H, hb0 + kLogitBlockH);
+  const int nstage = (hb1 - hb0) / kLogitStage;
+  // x staging: thread -> token tid % 64, h half (tid / 64) * 16 of the stage
+  const int xt = tid & 63, xh = (tid >> 6) * 16;
+  const bool xok = t0 + xt < T;
+  const uint4* xrow = reinterpret_cast<const uint4*>(x + (size_t)(xok ? t0 + xt : 0) * H);
 
-  auto issue = [&](int st) {
+  auto issue_w = [&](int st) {
     const int buf = st % kLogitDepth;
-    const int h0 = st * kLogitStage;
-    // Wr: 32 rows x 32 experts = 256 x 16 bytes, 4 per thread
+    const int h0 = hb0 + st * kLogitStage;
+    // 32 rows x 128 experts = 1024 x 16 bytes, 8 per thread
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 8; ++i) {
       const int idx = tid + i * kLogitThreads;
-      const int row = idx >> 3, c4 = (idx & 7) * 4;
+      const int row = idx >> 5, c4 = (idx & 31) * 4;
       const int e = e0 + c4;
       const float* src = Wr + (size_t)(h0 + row) * E + e;
       const uint32_t dst = (uint32_t)__cvta_generic_to_shared(&ws[buf][row][c4]);
@@ -77,94 +92,77 @@ __global__ void __launch_bounds__(kLogitThreads) router_logits_kernel(
         for (int j = 0; j < 4; ++j) cp_async4(dst + 4 * j, e + j < E ? src + j : Wr, e + j < E);
       }
     }
-    // x: 32 tokens x 32 h (bf16) = 128 x 16 bytes, 2 per thread
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int idx = tid + i * kLogitThreads;
-      const int tok = idx >> 2, h8 = (idx & 3) * 8;
-      const int t = t0 + tok;
-      const uint32_t dst = (uint32_t)__cvta_generic_to_shared(&xraw[buf][tok][h8]);
-      cp_async16(dst, t < T ? (const void*)(x + (size_t)t * H + h0 + h8) : (const void*)x, t < T);
-    }
+  };
+  auto load_x = [&](int st, uint4 (&r)[2]) {
+    const int hv = (hb0 + st * kLogitStage + xh) / 8;  // 16-byte vector index in the row
+    r[0] = xok ? __ldg(xrow + hv) : make_uint4(0, 0, 0, 0);
+    r[1] = xok ? __ldg(xrow + hv + 1) : make_uint4(0, 0, 0, 0);
   };
 
-  float p[4][4], run[4][4];
+  float p[8][8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      p[i][j] = 0.f;
-      run[i][j] = 0.f;
-    }
+    for (int j = 0; j < 8; ++j) p[i][j] = 0.f;
+
+  uint4 xr[2];
+  load_x(0, xr);
 #pragma unroll
   for (int st = 0; st < kLogitDepth - 1; ++st) {
-    if (st < nstage) issue(st);
+    if (st < nstage) issue_w(st);
     cp_async_commit();
   }
   for (int st = 0; st < nstage; ++st) {
-    const int buf = st % kLogitDepth;
-    cp_async_wait<kLogitDepth - 2>();
-    __syncthreads();  // stage st landed for every thread; stage st-1 fully consumed
-    // widen x: thread converts 16 values [tok][h..h+15] -> xs[h][tok]
-    {
-      const int tok = tid >> 1, hh0 = (tid & 1) * 16;
-      const uint4* src = reinterpret_cast<const uint4*>(&xraw[buf][tok][hh0]);
+    const int xb = st & 1;
+    {  // widen this stage's x into xs[xb][h][token]
+      const uint32_t w8[8] = {xr[0].x, xr[0].y, xr[0].z, xr[0].w, xr[1].x, xr[1].y, xr[1].z, xr[1].w};
 #pragma unroll
-      for (int v = 0; v < 2; ++v) {
-        const uint4 q = src[v];
-        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          xs[hh0 + 8 * v + 2 * i][tok] = bf16lo(w4[i]);
-          xs[hh0 + 8 * v + 2 * i + 1][tok] = bf16hi(w4[i]);
-        }
+      for (int i = 0; i < 8; ++i) {
+        xs[xb][xh + 2 * i][xt] = bf16lo(w8[i]);
+        xs[xb][xh + 2 * i + 1][xt] = bf16hi(w8[i]);
       }
     }
-    if (st + kLogitDepth - 1 < nstage) issue(st + kLogitDepth - 1);
+    cp_async_wait<kLogitDepth - 2>();
+    __syncthreads();  // xs[xb], W stage st visible; stage st-1 fully consumed
+    if (st + kLogitDepth - 1 < nstage) issue_w(st + kLogitDepth - 1);
     cp_async_commit();
-    __syncthreads();
-#pragma unroll 8
+    if (st + 1 < nstage) load_x(st + 1, xr);
+    const int buf = st % kLogitDepth;
+#pragma unroll 4
     for (int hh = 0; hh < kLogitStage; ++hh) {
-      const float4 xv = *reinterpret_cast<const float4*>(&xs[hh][my_tok]);
-      const float4 wv = *reinterpret_cast<const float4*>(&ws[buf][hh][my_exp]);
-      const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
-      const float wa[4] = {wv.x, wv.y, wv.z, wv.w};
+      const float4 xa = *reinterpret_cast<const float4*>(&xs[xb][hh][4 * tg]);
+      const float4 xb4 = *reinterpret_cast<const float4*>(&xs[xb][hh][32 + 4 * tg]);
+      const float4 wa = *reinterpret_cast<const float4*>(&ws[buf][hh][8 * eg]);
+      const float4 wb = *reinterpret_cast<const float4*>(&ws[buf][hh][8 * eg + 4]);
+      const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb4.x, xb4.y, xb4.z, xb4.w};
+      const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) p[i][j] = __fmaf_rn(xa[i], wa[j], p[i][j]);
-    }
-    const int h_end = (st + 1) * kLogitStage;
-    if (h_end % kLogitBlockH == 0 || h_end == H) {
-      const bool first = h_end <= kLogitBlockH;
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          run[i][j] = first ? p[i][j] : __fadd_rn(run[i][j], p[i][j]);
-          p[i][j] = 0.f;
-        }
+        for (int j = 0; j < 8; ++j) p[i][j] = __fmaf_rn(xv[i], wv[j], p[i][j]);
     }
   }
   cp_async_wait<0>();
+  float* out = part + (size_t)blk * T * E;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = t0 + my_tok + i;
+  for (int i = 0; i < 8; ++i) {
+    const int t = t0 + (i < 4 ? 4 * tg + i : 32 + 4 * tg + i - 4);
     if (t >= T) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = e0 + my_exp + j;
-      if (e < E) logits[(size_t)t * E + e] = bias ? __fadd_rn(run[i][j], __ldg(bias + e)) : run[i][j];
+    for (int j = 0; j < 8; ++j) {
+      const int e = e0 + 8 * eg + j;
+      if (e < E) out[(size_t)t * E + e] = p[i][j];
     }
   }
 }
 
 // -------------------------------------------------------------- top-k kernel
 //
-// One warp per token: the token's logits sit in registers (lane l holds
-// experts l, l+32, ...; kNQ registers per lane); k rounds of a warp-wide
-// arg-max over (logit descending, id ascending) pick the slots in order.
-// Slot counts go to counts[] with integer atomics (order-independent).
+// One warp per token: the token's logits are assembled in registers (lane l
+// holds experts l, l+32, ...; kNQ registers per lane) from the h-block
+// partials, added left to right, bias last; k rounds of a warp-wide arg-max
+// over (logit descending, id ascending) pick the slots in order.  Slot
+// counts go to counts[] with integer atomics (order-independent).
 constexpr int kTopkWarps = 8;
 constexpr int kTopkTokPerWarp = 2;
 constexpr int kTopkTokPerBlock = kTopkWarps * kTopkTokPerWarp;
@@ -174,7 +172,8 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
 }
 
 template <int kNQ>
-__global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ logits, int T,
+__global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ part, int nblk,
+                                                          const float* __restrict__ bias, int T,
                                                           int E, int k, int32_t* __restrict__ topk_idx,
                                                           float* __restrict__ topk_w,
                                                           int32_t* __restrict__ counts) {
@@ -186,7 +185,14 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
 #pragma unroll
     for (int q = 0; q < kNQ; ++q) {
       const int e = lane + 32 * q;
-      v[q] = (e < E) ? __ldg(logits + (size_t)t * E + e) : 0.f;
+      float acc = 0.f;
+      if (e < E) {
+        const float* pp = part + (size_t)t * E + e;
+        acc = __ldg(pp);
+        for (int b = 1; b < nblk; ++b) acc = __fadd_rn(acc, __ldg(pp + (size_t)b * T * E));
+        if (bias) acc = __fadd_rn(acc, __ldg(bias + e));
+      }
+      v[q] = acc;
     }
     uint32_t taken = 0;
 #pragma unroll
@@ -374,11 +380,10 @@ __global__ void router_bwd_reduce_kernel(const float* __restrict__ P, int S, int
 
 size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
-int route_ws_layout(int T, int E, size_t* logits_bytes, size_t* hist_bytes) {
-  const size_t nblk = (size_t)((T + kTopkTokPerBlock - 1) / kTopkTokPerBlock);
-  *logits_bytes = align256(sizeof(float) * (size_t)(T > 0 ? T : 1) * E);
-  *hist_bytes = 0;
-  return (int)nblk;
+// Route workspace: the h-block partials of the logits, fp32 [nblk_h][T][E].
+size_t route_ws_bytes(int T, int H, int E) {
+  const size_t nblk_h = (size_t)((H + kLogitBlockH - 1) / kLogitBlockH);
+  return align256(sizeof(float) * nblk_h * (size_t)(T > 0 ? T : 1) * E);
 }
 
 struct BwdLayout {
@@ -415,11 +420,8 @@ using namespace moe;
 extern "C" {
 
 size_t moe_route_topk_workspace_size(int T, int H, int E) {
-  (void)H;
-  if (T < 0 || E <= 0) return 0;
-  size_t a, b;
-  route_ws_layout(T, E, &a, &b);
-  return a + b;
+  if (T < 0 || H <= 0 || E <= 0) return 0;
+  return route_ws_bytes(T, H, E);
 }
 
 int moe_route_topk(const void* x, const float* Wr, const float* bias, int T, int H, int E, int k,
@@ -440,36 +442,49 @@ int moe_route_topk(const void* x, const float* Wr, const float* bias, int T, int
     return fail(MOE_ERR_INVALID_ARG, "moe_route_topk: NULL pointer argument");
   if (!aligned16(x) || !aligned16(Wr) || !aligned16(ws) || (bias && !aligned16(bias)))
     return fail(MOE_ERR_ALIGNMENT, "moe_route_topk: x, Wr, bias and ws must be 16-byte aligned");
-  size_t lb, hb;
-  const int nblk = route_ws_layout(T, E, &lb, &hb);
-  if (ws_bytes < lb + hb)
-    return fail(MOE_ERR_WORKSPACE, "moe_route_topk: workspace %zu < %zu bytes", ws_bytes, lb + hb);
+  const size_t need = route_ws_bytes(T, H, E);
+  if (ws_bytes < need)
+    return fail(MOE_ERR_WORKSPACE, "moe_route_topk: workspace %zu < %zu bytes", ws_bytes, need);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  float* logits = static_cast<float*>(ws);
+  float* part = static_cast<float*>(ws);
   zero_counts_kernel<<<1, 256, 0, s>>>(counts, E);
   if (int rc = check_launch("moe_route_topk: zero counts")) return rc;
   if (T > 0) {
-    dim3 grid((T + kLogitTok - 1) / kLogitTok, (E + kLogitExp - 1) / kLogitExp);
+    static bool attr_set[64] = {};
+    const int dev = current_device();
+    if (dev < 0 || dev >= 64) return fail(MOE_ERR_CUDA, "moe_route_topk: no usable current device");
+    if (!attr_set[dev]) {
+      cudaError_t e1 = cudaFuncSetAttribute(router_partials_kernel<true>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLogitSmem);
+      cudaError_t e2 = cudaFuncSetAttribute(router_partials_kernel<false>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLogitSmem);
+      if (e1 != cudaSuccess || e2 != cudaSuccess)
+        return fail(MOE_ERR_CUDA, "moe_route_topk: %s", cudaGetErrorString(e1 != cudaSuccess ? e1 : e2));
+      attr_set[dev] = true;
+    }
+    const int nblk_h = (H + kLogitBlockH - 1) / kLogitBlockH;
+    dim3 grid((T + kLogitTok - 1) / kLogitTok, nblk_h, (E + kLogitExp - 1) / kLogitExp);
     if (E % 4 == 0)
-      router_logits_kernel<true><<<grid, kLogitThreads, 0, s>>>(
-          static_cast<const __nv_bfloat16*>(x), Wr, bias, T, H, E, logits);
+      router_partials_kernel<true><<<grid, kLogitThreads, kLogitSmem, s>>>(
+          static_cast<const __nv_bfloat16*>(x), Wr, T, H, E, part);
     else
-      router_logits_kernel<false><<<grid, kLogitThreads, 0, s>>>(
-          static_cast<const __nv_bfloat16*>(x), Wr, bias, T, H, E, logits);
+      router_partials_kernel<false><<<grid, kLogitThreads, kLogitSmem, s>>>(
+          static_cast<const __nv_bfloat16*>(x), Wr, T, H, E, part);
     if (int rc = check_launch("moe_route_topk: logits kernel")) return rc;
+    const int nblk = (T + kTopkTokPerBlock - 1) / kTopkTokPerBlock;
     const int nq = (E + 31) / 32;
     if (nq <= 1)
-      router_topk_kernel<1><<<nblk, 256, 0, s>>>(logits, T, E, k, topk_idx, topk_w, counts);
+      router_topk_kernel<1><<<nblk, 256, 0, s>>>(part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
     else if (nq <= 2)
-      router_topk_kernel<2><<<nblk, 256, 0, s>>>(logits, T, E, k, topk_idx, topk_w, counts);
+      router_topk_kernel<2><<<nblk, 256, 0, s>>>(part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
     else if (nq <= 4)
-      router_topk_kernel<4><<<nblk, 256, 0, s>>>(logits, T, E, k, topk_idx, topk_w, counts);
+      router_topk_kernel<4><<<nblk, 256, 0, s>>>(part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
     else if (nq <= 8)
-      router_topk_kernel<8><<<nblk, 256, 0, s>>>(logits, T, E, k, topk_idx, topk_w, counts);
+      router_topk_kernel<8><<<nblk, 256, 0, s>>>(part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
     else if (nq <= 16)
-      router_topk_kernel<16><<<nblk, 256, 0, s>>>(logits, T, E, k, topk_idx, topk_w, counts);
+      router_topk_kernel<16><<<nblk, 256, 0, s>>>(part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
     else
-      router_topk_kernel<32><<<nblk, 256, 0, s>>>(logits, T, E, k, topk_idx, topk_w, counts);
+      router_topk_kernel<32><<<nblk, 256, 0, s>>>(part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
     if (int rc = check_launch("moe_route_topk: top-k kernel")) return rc;
   }
   router_offsets_kernel<<<1, 1024, 0, s>>>(counts, E, ep_size, offsets, rank_offsets);
