@@ -21,7 +21,7 @@ namespace {
 constexpr int kChunkTok = 32;  // tokens per ranking chunk
 
 // --------------------------------------------------------------- histogram
-// blk_hist[c][e] = number of slots of chunk c routed to expert e.
+// chunk_base[e][c] = number of slots of chunk c routed to expert e.
 __global__ void __launch_bounds__(256) chunk_hist_kernel(const int32_t* __restrict__ topk_idx,
                                                          int T, int E, int k, int nchunk,
                                                          int32_t* __restrict__ chunk_base,
@@ -43,35 +43,34 @@ __global__ void __launch_bounds__(256) chunk_hist_kernel(const int32_t* __restri
         set_status(status, MOE_STATUS_BAD_INDEX);
     }
     __syncwarp();
-    for (int e = lane; e < E; e += 32) chunk_base[(size_t)c * E + e] = h[e];
+    for (int e = lane; e < E; e += 32) chunk_base[(size_t)e * nchunk + c] = h[e];
   }
 }
 
-// chunk_base[c][e] <- offsets[e] + sum_{c' < c} hist[c'][e]  (in place).
-// One warp per expert: lane l owns a contiguous run of chunks; a warp scan of
-// the per-lane sums gives each lane its starting row.
+// chunk_base[e][c] <- offsets[e] + sum_{c' < c} hist[e][c']  (in place).
+// One warp per expert walks its row of chunks 32 at a time (coalesced): a
+// warp scan of each batch plus the running carry gives every chunk its
+// starting row.
 __global__ void __launch_bounds__(256) chunk_scan_kernel(int32_t* __restrict__ chunk_base,
                                                          const int32_t* __restrict__ offsets,
                                                          int nchunk, int E, int* status) {
   const int e = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (e >= E) return;
-  const int per = (nchunk + 31) / 32;
-  const int c0 = min(nchunk, lane * per), c1 = min(nchunk, c0 + per);
-  int local = 0;
-  for (int c = c0; c < c1; ++c) local += chunk_base[(size_t)c * E + e];
-  int incl = local;
+  int32_t* row = chunk_base + (size_t)e * nchunk;
+  int carry = offsets[e];
+  for (int c0 = 0; c0 < nchunk; c0 += 32) {
+    const int c = c0 + lane;
+    const int v = c < nchunk ? row[c] : 0;
+    int incl = v;
 #pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int o = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += o;
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    if (c < nchunk) row[c] = carry + incl - v;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
   }
-  int run = offsets[e] + incl - local;
-  for (int c = c0; c < c1; ++c) {
-    const int v = chunk_base[(size_t)c * E + e];
-    chunk_base[(size_t)c * E + e] = run;
-    run += v;
-  }
-  if (lane == 31 && run != offsets[e + 1]) set_status(status, MOE_STATUS_COUNT_MISMATCH);
+  if (lane == 0 && carry != offsets[e + 1]) set_status(status, MOE_STATUS_COUNT_MISMATCH);
 }
 
 // ------------------------------------------------------- rank and row copy
@@ -79,7 +78,8 @@ __global__ void __launch_bounds__(256) chunk_scan_kernel(int32_t* __restrict__ c
 // (token, slot) order: lanes that hold the same expert in one batch of 32
 // slots get consecutive rows in lane order (= token order, since a token
 // picks an expert at most once).  Then all 8 warps copy the chunk's token
-// rows to their k destinations.
+// rows to their k destinations; the first row of every copying warp is
+// loaded while warp 0 is still ranking.
 __global__ void __launch_bounds__(256) dispatch_kernel(
     const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ topk_idx,
     const int32_t* __restrict__ chunk_base, int T, int H, int E, int k,
@@ -94,7 +94,20 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
   const int nt = min(kChunkTok, T - t0);
   const int nslot = nt * k;
   const int R = T * k;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = chunk_base[(size_t)c * E + e];
+  const int nchunk = gridDim.x;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = chunk_base[(size_t)e * nchunk + c];
+  const int nvec = H / 8;  // 16-byte vectors per row
+  // the first 8 vectors per lane of this warp's first token, in flight during the ranking
+  uint4 pre[8];
+  const bool prefetch = x_perm != nullptr && warp > 0 && warp < nt;
+  if (prefetch) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(t0 + warp) * H);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int v = u * 32 + lane;
+      if (v < nvec) pre[u] = __ldg(src + v);
+    }
+  }
   __syncthreads();
   if (warp == 0) {
     for (int b = 0; b < nslot; b += 32) {
@@ -124,16 +137,20 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
   }
   __syncthreads();
   if (!x_perm) return;
-  const int nvec = H / 8;  // 16-byte vectors per row
   for (int i = warp; i < nt; i += 8) {
     const int t = t0 + i;
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
     for (int v0 = 0; v0 < nvec; v0 += 32 * 8) {
       uint4 buf[8];
+      if (prefetch && i == warp && v0 == 0) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int v = v0 + u * 32 + lane;
-        if (v < nvec) buf[u] = __ldg(src + v);
+        for (int u = 0; u < 8; ++u) buf[u] = pre[u];
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int v = v0 + u * 32 + lane;
+          if (v < nvec) buf[u] = __ldg(src + v);
+        }
       }
       for (int j = 0; j < k; ++j) {
         const int row = rows[i * k + j];
