@@ -233,73 +233,63 @@ __global__ void __launch_bounds__(256) gather_sum_kernel(const __nv_bfloat16* __
 }
 
 // ------------------------------------------------------------ combine bwd
-// CTA per token: for every slot the CTA writes dy_perm[row] = w * dy[t] and
-// reduces the dot product dy[t] . y_perm[row] (per-thread partials, then a
-// fixed-order warp and block reduction).  Slots go in batches of 8 so that
-// eight independent row loads per thread are in flight.
+// Warp per token (grid-stride over tokens): the token's dy row sits in
+// registers (8 vectors of 8 bf16 columns per lane at a time); for every slot
+// the warp writes dy_perm[row] = w * dy[t] and reduces dy[t] . y_perm[row]
+// (per-lane fp32 partial, then a fixed butterfly); lane j keeps d_w[t,j].
 __global__ void __launch_bounds__(256) combine_bwd_kernel(
     const __nv_bfloat16* __restrict__ dy, const __nv_bfloat16* __restrict__ y_perm,
     const float* __restrict__ topk_w, const int32_t* __restrict__ row_of_slot, int T, int H, int k,
     int R, __nv_bfloat16* __restrict__ dy_perm, float* __restrict__ d_w, int* status) {
-  __shared__ float red[8][kMaxTopK];
-  const int t = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31;
   const int nvec = H / 8;
-  for (int j0 = 0; j0 < k; j0 += 8) {
-    int rows[8];
-    float wv[8], part[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int j = j0 + u;
-      rows[u] = -1;
-      wv[u] = 0.f;
-      part[u] = 0.f;
-      if (j < k) {
-        const int row = __ldg(row_of_slot + (size_t)t * k + j);
-        if (row >= 0 && row < R) {
-          rows[u] = row;
-          wv[u] = __ldg(topk_w + (size_t)t * k + j);
-        } else {
-          set_status(status, MOE_STATUS_BAD_INDEX);
-        }
-      }
+  const int nw = (int)((gridDim.x * blockDim.x) >> 5);
+  for (int t = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); t < T; t += nw) {
+    int my_row = lane < k ? __ldg(row_of_slot + (size_t)t * k + lane) : -1;
+    const float my_w = lane < k ? __ldg(topk_w + (size_t)t * k + lane) : 0.f;
+    if (lane < k && (my_row < 0 || my_row >= R)) {
+      set_status(status, MOE_STATUS_BAD_INDEX);
+      my_row = -1;
     }
-    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
-      float g[8];
-      unpack8(__ldg(reinterpret_cast<const uint4*>(dy + (size_t)t * H) + v), g);
-      uint4 yb[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        yb[u] = rows[u] >= 0 ? __ldg(reinterpret_cast<const uint4*>(y_perm + (size_t)rows[u] * H) + v)
-                             : make_uint4(0, 0, 0, 0);
+    float my_dw = 0.f;
+    for (int v0 = 0; v0 < nvec; v0 += 256) {
+      uint4 gp[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        if (rows[u] < 0) continue;
-        float yv[8], o[8];
-        unpack8(yb[u], yv);
+        const int v = v0 + u * 32 + lane;
+        gp[u] = v < nvec ? __ldg(reinterpret_cast<const uint4*>(dy + (size_t)t * H) + v) : make_uint4(0, 0, 0, 0);
+      }
+      for (int j = 0; j < k; ++j) {
+        const int row = __shfl_sync(0xffffffffu, my_row, j);
+        const float w = __shfl_sync(0xffffffffu, my_w, j);
+        if (row < 0) continue;  // uniform across the warp
+        uint4 yb[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int v = v0 + u * 32 + lane;
+          yb[u] = v < nvec ? __ldg(reinterpret_cast<const uint4*>(y_perm + (size_t)row * H) + v)
+                           : make_uint4(0, 0, 0, 0);
+        }
         float p = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          o[i] = wv[u] * g[i];
-          p = __fmaf_rn(g[i], yv[i], p);
+        for (int u = 0; u < 8; ++u) {
+          const int v = v0 + u * 32 + lane;
+          float g[8], yv[8], o[8];
+          unpack8(gp[u], g);
+          unpack8(yb[u], yv);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            o[i] = w * g[i];
+            p = __fmaf_rn(g[i], yv[i], p);
+          }
+          if (v < nvec) reinterpret_cast<uint4*>(dy_perm + (size_t)row * H)[v] = pack8(o);
         }
-        reinterpret_cast<uint4*>(dy_perm + (size_t)rows[u] * H)[v] = pack8(o);
-        part[u] += p;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+        if (lane == j) my_dw += p;
       }
     }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      float p = part[u];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
-      if (lane == 0 && j0 + u < k) red[warp][j0 + u] = p;
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x < k) {
-    float s = 0.f;
-    for (int w = 0; w < 8; ++w) s += red[w][threadIdx.x];
-    d_w[(size_t)t * k + threadIdx.x] = s;
+    if (lane < k) d_w[(size_t)t * k + lane] = my_dw;
   }
 }
 
@@ -407,7 +397,7 @@ int moe_combine_bwd(const void* dy, const void* y_perm, const float* topk_w,
   if (!aligned16(dy) || !aligned16(y_perm) || !aligned16(dy_perm))
     return fail(MOE_ERR_ALIGNMENT, "moe_combine_bwd: dy, y_perm and dy_perm must be 16-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  combine_bwd_kernel<<<T, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(dy),
+  combine_bwd_kernel<<<grid_for((size_t)T * 32, 256), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(dy),
                                        static_cast<const __nv_bfloat16*>(y_perm), topk_w,
                                        row_of_slot, T, H, k, T * k,
                                        static_cast<__nv_bfloat16*>(dy_perm), d_w, status_word());
