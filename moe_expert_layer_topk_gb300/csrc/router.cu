@@ -28,7 +28,7 @@ namespace {
 // tokens 4tg..4tg+3 and 32+4tg..32+4tg+3 (so the eight tg of a warp read 128
 // contiguous bytes of xs per load, free of bank conflicts), experts
 // 8eg..8eg+7.
-// h advances in stages of 32: a 3-deep cp.async pipeline brings the Wr tile
+// h advances in stages of 32: a double-buffered cp.async pipeline brings the Wr tile
 // [32 h][128 e] (fp32) into shared memory; the x tile [64 tokens][32 h]
 // (bf16) is read into registers one stage ahead, widened and stored
 // transposed as xs[32 h][64 tokens] (two buffers).
@@ -37,7 +37,7 @@ constexpr int kLogitExp = 128;
 constexpr int kLogitThreads = 128;
 constexpr int kLogitStage = 32;   // h per stage
 constexpr int kLogitBlockH = 256; // h per summation block
-constexpr int kLogitDepth = 3;    // W stages in flight
+constexpr int kLogitDepth = 2;    // W stages in flight (4 CTAs per SM)
 constexpr size_t kLogitSmem = sizeof(float) * (kLogitDepth * kLogitStage * kLogitExp + 2 * kLogitStage * kLogitTok);
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
