@@ -149,8 +149,8 @@ int moe_dispatch(const void* x, const int32_t* topk_idx, const int32_t* offsets,
  * device allocation allowed afterwards), or a thin C caller with no device
  * allocator of its own.  Its scratch is a 1 MiB array built into the library;
  * every GPU that loads the library holds it until the process exits.
- *   - Limit: ceil(T/32) * E <= moe_dispatch_no_alloc_max_scratch() (262144),
- *     e.g. T <= 65536 tokens at E = 128; larger sizes return
+ *   - Limit: ceil(T/16) * E <= moe_dispatch_no_alloc_max_scratch() (262144),
+ *     e.g. T <= 32768 tokens at E = 128; larger sizes return
  *     MOE_ERR_WORKSPACE without launching anything (use moe_dispatch).
  *   - The first call on a device looks the array's device address up
  *     (cudaGetSymbolAddress) with that device current; make that first call

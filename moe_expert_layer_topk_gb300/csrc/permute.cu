@@ -18,7 +18,7 @@
 namespace moe {
 namespace {
 
-constexpr int kChunkTok = 32;  // tokens per ranking chunk
+constexpr int kChunkTok = 16;  // tokens per ranking chunk
 
 // --------------------------------------------------------------- histogram
 // chunk_base[e][c] = number of slots of chunk c routed to expert e.
@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(256) chunk_scan_kernel(int32_t* __restrict__ c
 }
 
 // ------------------------------------------------------- rank and row copy
-// One CTA per chunk of 32 tokens.  Warp 0 hands out rows slot by slot in
+// One CTA per chunk of 16 tokens.  Warp 0 hands out rows slot by slot in
 // (token, slot) order: lanes that hold the same expert in one batch of 32
 // slots get consecutive rows in lane order (= token order, since a token
 // picks an expert at most once).  Then all 8 warps copy the chunk's token
@@ -463,7 +463,7 @@ int moe_dispatch_no_alloc(const void* x, const int32_t* topk_idx, const int32_t*
   const size_t nchunk = (size_t)((T + kChunkTok - 1) / kChunkTok);
   if (nchunk * (size_t)E > kNoAllocScratchInts)
     return fail(MOE_ERR_WORKSPACE,
-                "moe_dispatch_no_alloc: ceil(T/32)*E = %zu exceeds the built-in scratch of %zu "
+                "moe_dispatch_no_alloc: ceil(T/16)*E = %zu exceeds the built-in scratch of %zu "
                 "entries (use moe_dispatch with a workspace)",
                 nchunk * (size_t)E, kNoAllocScratchInts);
   int32_t* chunk_base = nullptr;

@@ -51,7 +51,7 @@ def test_no_alloc_dispatch_refuses_sizes_beyond_its_scratch():
     L = m.lib()
     cap = L.moe_dispatch_no_alloc_max_scratch()
     E = 1024
-    T = (cap // E + 1) * 32          # one chunk more than fits
+    T = (cap // E + 1) * 16          # one chunk more than fits
     P = 0x10000                      # never dereferenced: refused before any launch
     assert L.moe_dispatch_no_alloc(P, P, P, T, 128, E, 2, P, P, P, None) == -4
     assert "scratch" in L.moe_last_error_string().decode()
