@@ -114,6 +114,33 @@ class ClockSampler:
                 "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
 
 
+# ------------------------------------------------------------ ncu traffic
+
+def recorded_traffic():
+    """DRAM bytes per launch of the forward gate/up GEMM as recorded from ncu
+    in profiles/traffic_gate_up_fwd_T8192.md, or None once the kernel's
+    sources no longer hash to the values recorded there."""
+    import hashlib
+    prof = ROOT / "profiles" / "traffic_gate_up_fwd_T8192.md"
+    if not prof.exists():
+        return None
+    value, hashes = None, {}
+    for line in prof.read_text().splitlines():
+        if line.startswith("traffic_bytes_per_launch:"):
+            value = int(line.split(":")[1])
+        elif line.startswith("source_sha256 "):
+            name, digest = line[len("source_sha256 "):].split(":")
+            hashes[name.strip()] = digest.strip()
+    csrc = ROOT / "moe_expert_layer_topk_gb300" / "csrc"
+    if value is None or not hashes:
+        return None
+    for name, digest in hashes.items():
+        f = csrc / name
+        if not f.exists() or hashlib.sha256(f.read_bytes()).hexdigest() != digest:
+            return None
+    return value
+
+
 # --------------------------------------------------------------- multi-rank
 
 def dist_setup(n_gpus):
@@ -355,13 +382,7 @@ def run_ours(args, shape, inp):
     dom_tflops = gemm_fl[dom] / (per_call[dom] * 1e-3) / 1e12
     step_ms = ms / args.steps
     value = world * T / (step_ms * 1e-3)
-    prof = ROOT / "profiles" / "traffic.json"
-    traffic = None
-    if prof.exists():
-        try:
-            traffic = json.loads(prof.read_text()).get("grouped_gemm_gate_up_fwd_T4096x8_bytes_per_launch")
-        except Exception:
-            traffic = None
+    traffic = recorded_traffic()
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
