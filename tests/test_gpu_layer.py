@@ -25,6 +25,10 @@ CASES = {
     "odd_tiles": (300, 192, 192, 6, 2, 3, None),
     "zipf_bias": (500, 128, 128, 16, 4, 4, "zipf"),
     "many_experts": (160, 512, 256, 40, 5, 8, None),
+    # more than 128 experts: two router expert tiles and the separate top-k
+    # kernel; E % 4 != 0 takes the scalar Wr loads
+    "router_e130": (96, 256, 64, 130, 4, 2, None),
+    "router_e256": (64, 320, 64, 256, 8, 8, None),
 }
 
 
