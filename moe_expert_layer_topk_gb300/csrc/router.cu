@@ -166,6 +166,9 @@ __global__ void __launch_bounds__(kLogitThreads) router_partials_kernel(
 constexpr int kTopkWarps = 8;
 constexpr int kTopkTokPerWarp = 2;
 constexpr int kTopkTokPerBlock = kTopkWarps * kTopkTokPerWarp;
+// h-block partials loaded per batch (kNQ * batch <= 32 values per lane)
+template <int kNQ>
+__host__ __device__ constexpr int sum_batch() { return kNQ >= 32 ? 1 : (kNQ >= 16 ? 2 : (kNQ >= 8 ? 4 : 8)); }
 
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
@@ -181,18 +184,33 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
   for (int it = 0; it < kTopkTokPerWarp; ++it) {
     const int t = blockIdx.x * kTopkTokPerBlock + warp * kTopkTokPerWarp + it;
     if (t >= T) break;
+    // the partials of up to kSumBatch blocks are loaded together (independent
+    // loads in flight), then added in block order
+    constexpr int kSumBatch = sum_batch<kNQ>();
     float v[kNQ];
 #pragma unroll
-    for (int q = 0; q < kNQ; ++q) {
-      const int e = lane + 32 * q;
-      float acc = 0.f;
-      if (e < E) {
-        const float* pp = part + (size_t)t * E + e;
-        acc = __ldg(pp);
-        for (int b = 1; b < nblk; ++b) acc = __fadd_rn(acc, __ldg(pp + (size_t)b * T * E));
-        if (bias) acc = __fadd_rn(acc, __ldg(bias + e));
+    for (int q = 0; q < kNQ; ++q) v[q] = 0.f;
+    for (int b0 = 0; b0 < nblk; b0 += kSumBatch) {
+      float pv[kNQ][kSumBatch];
+#pragma unroll
+      for (int q = 0; q < kNQ; ++q) {
+        const int e = lane + 32 * q;
+#pragma unroll
+        for (int u = 0; u < kSumBatch; ++u)
+          pv[q][u] = (e < E && b0 + u < nblk) ? __ldg(part + ((size_t)(b0 + u) * T + t) * E + e) : 0.f;
       }
-      v[q] = acc;
+#pragma unroll
+      for (int q = 0; q < kNQ; ++q)
+#pragma unroll
+        for (int u = 0; u < kSumBatch; ++u)
+          if (b0 + u < nblk) v[q] = (b0 + u == 0) ? pv[q][u] : __fadd_rn(v[q], pv[q][u]);
+    }
+    if (bias) {
+#pragma unroll
+      for (int q = 0; q < kNQ; ++q) {
+        const int e = lane + 32 * q;
+        if (e < E) v[q] = __fadd_rn(v[q], __ldg(bias + e));
+      }
     }
     uint32_t taken = 0;
 #pragma unroll
