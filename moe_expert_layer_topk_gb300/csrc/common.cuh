@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moe_topk.h"
 
 namespace moe {
@@ -23,6 +25,26 @@ int sm_count();
 int current_device();
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launches `kern` on `s` with programmatic dependent launch allowed: the
+// kernel may be scheduled while its predecessor in the stream is finishing;
+// every kernel of this library starts with pdl_wait(), which returns once
+// the predecessor has completed and its memory is visible.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 inline int check_launch(const char* what) {
   cudaError_t e = cudaGetLastError();
@@ -57,6 +79,11 @@ int launch_dw_split(const void* A, const void* B, int K_rows, int M, int N,
                     cudaStream_t stream);
 
 // ---------------------------------------------------------------- device side
+
+// Programmatic dependent launch: wait for the predecessor grid (its writes
+// visible), then let the successor grid be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }

@@ -208,6 +208,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const __grid_constant__ CUtensorMap tmB1,
                         const __grid_constant__ CUtensorMap tmO0,
                         const __grid_constant__ CUtensorMap tmO1, const Params p) {
+  pdl_wait();
+  pdl_trigger();
   using C = Cfg<KIND, CTAS, DEEP>;
   constexpr int STG = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -716,6 +718,8 @@ __global__ void dw_segment_maps_kernel(const __grid_constant__ CUtensorMap tplA,
                                        const int32_t* seg_offsets, int num_seg, int rows,
                                        const uint8_t* baseA, size_t pitchA, const uint8_t* baseB,
                                        size_t pitchB, CUtensorMap* maps) {
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= 2 * num_seg) return;
   const int s = i >> 1;
@@ -795,14 +799,17 @@ int launch(Params p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensor
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // the kernel starts with pdl_wait()
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (CTAS == 2) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
   }
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, b0, b1, o0, o1, p);
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -838,7 +845,7 @@ int run_dw(bool pair, Params p, const void* A, const void* B, const CUtensorMap&
   if (int rc = make_tmap_mn(&ta, A, p.M, p.K, BM / 64)) return rc;
   if (int rc = make_tmap_mn(&tb, B, p.N, p.K, nckB)) return rc;
   const int nmaps = 2 * p.num_seg;
-  dw_segment_maps_kernel<<<(nmaps + 127) / 128, 128, 0, s>>>(
+  launch_pdl(dw_segment_maps_kernel, (nmaps + 127) / 128, 128, 0, s, 
       ta, tb, p.seg_offsets, p.num_seg, p.K, static_cast<const uint8_t*>(A), (size_t)p.M * 2,
       static_cast<const uint8_t*>(B), (size_t)p.N * 2, static_cast<CUtensorMap*>(maps));
   if (int rc = check_launch(what)) return rc;

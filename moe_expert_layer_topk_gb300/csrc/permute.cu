@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(256) chunk_hist_kernel(const int32_t* __restri
                                                          int T, int E, int k, int nchunk,
                                                          int32_t* __restrict__ chunk_base,
                                                          int* status) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int hist[];  // [8 warps][E]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * 8 + warp;
@@ -54,6 +56,8 @@ __global__ void __launch_bounds__(256) chunk_hist_kernel(const int32_t* __restri
 __global__ void __launch_bounds__(256) chunk_scan_kernel(int32_t* __restrict__ chunk_base,
                                                          const int32_t* __restrict__ offsets,
                                                          int nchunk, int E, int* status) {
+  pdl_wait();
+  pdl_trigger();
   const int e = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (e >= E) return;
   int32_t* row = chunk_base + (size_t)e * nchunk;
@@ -85,6 +89,8 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
     const int32_t* __restrict__ chunk_base, int T, int H, int E, int k,
     __nv_bfloat16* __restrict__ x_perm, int32_t* __restrict__ row_of_slot,
     int32_t* __restrict__ token_of_row, int* status) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int sm[];
   int* cnt = sm;                // [E]
   int* rows = sm + E;           // [kChunkTok * k]
@@ -185,6 +191,8 @@ __global__ void __launch_bounds__(256) gather_sum_kernel(const __nv_bfloat16* __
                                                          const int32_t* __restrict__ row_of_slot,
                                                          int T, int H, int k, int R,
                                                          void* __restrict__ out, int* status) {
+  pdl_wait();
+  pdl_trigger();
   const int nvec = H / 8;
   const size_t total = (size_t)T * nvec;
   for (size_t gid = blockIdx.x * (size_t)blockDim.x + threadIdx.x; gid < total;
@@ -241,6 +249,8 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(
     const __nv_bfloat16* __restrict__ dy, const __nv_bfloat16* __restrict__ y_perm,
     const float* __restrict__ topk_w, const int32_t* __restrict__ row_of_slot, int T, int H, int k,
     int R, __nv_bfloat16* __restrict__ dy_perm, float* __restrict__ d_w, int* status) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int nvec = H / 8;
   const int nw = (int)((gridDim.x * blockDim.x) >> 5);
@@ -341,12 +351,12 @@ int moe_dispatch(const void* x, const int32_t* topk_idx, const int32_t* offsets,
   int* status = status_word();
   const int nchunk = (T + kChunkTok - 1) / kChunkTok;
   int32_t* chunk_base = static_cast<int32_t*>(ws);
-  chunk_hist_kernel<<<(nchunk + 7) / 8, 256, sizeof(int) * 8 * E, s>>>(topk_idx, T, E, k, nchunk,
+  launch_pdl(chunk_hist_kernel, (nchunk + 7) / 8, 256, sizeof(int) * 8 * E, s, topk_idx, T, E, k, nchunk,
                                                                        chunk_base, status);
   if (int rc = check_launch("moe_dispatch: histogram kernel")) return rc;
-  chunk_scan_kernel<<<(E + 7) / 8, 256, 0, s>>>(chunk_base, offsets, nchunk, E, status);
+  launch_pdl(chunk_scan_kernel, (E + 7) / 8, 256, 0, s, chunk_base, offsets, nchunk, E, status);
   if (int rc = check_launch("moe_dispatch: scan kernel")) return rc;
-  dispatch_kernel<<<nchunk, 256, sizeof(int) * (E + kChunkTok * k), s>>>(
+  launch_pdl(dispatch_kernel, nchunk, 256, sizeof(int) * (E + kChunkTok * k), s, 
       static_cast<const __nv_bfloat16*>(x), topk_idx, chunk_base, T, H, E, k,
       static_cast<__nv_bfloat16*>(x_perm), row_of_slot, token_of_row, status);
   return check_launch("moe_dispatch: row kernel");
@@ -363,7 +373,7 @@ int moe_combine(const void* y_perm, const float* topk_w, const int32_t* row_of_s
     return fail(MOE_ERR_ALIGNMENT, "moe_combine: y_perm and y must be 16-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t work = (size_t)T * (H / 8);
-  gather_sum_kernel<true, false><<<grid_for(work, 256), 256, 0, s>>>(
+  launch_pdl(gather_sum_kernel<true, false>, grid_for(work, 256), 256, 0, s, 
       static_cast<const __nv_bfloat16*>(y_perm), topk_w, row_of_slot, T, H, k, T * k, y,
       status_word());
   return check_launch("moe_combine");
@@ -380,7 +390,7 @@ int moe_dispatch_bwd(const void* dx_perm, const int32_t* row_of_slot, int T, int
     return fail(MOE_ERR_ALIGNMENT, "moe_dispatch_bwd: dx_perm and dx_acc must be 16-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t work = (size_t)T * (H / 8);
-  gather_sum_kernel<false, true><<<grid_for(work, 256), 256, 0, s>>>(
+  launch_pdl(gather_sum_kernel<false, true>, grid_for(work, 256), 256, 0, s, 
       static_cast<const __nv_bfloat16*>(dx_perm), nullptr, row_of_slot, T, H, k, T * k, dx_acc,
       status_word());
   return check_launch("moe_dispatch_bwd");
@@ -397,7 +407,7 @@ int moe_combine_bwd(const void* dy, const void* y_perm, const float* topk_w,
   if (!aligned16(dy) || !aligned16(y_perm) || !aligned16(dy_perm))
     return fail(MOE_ERR_ALIGNMENT, "moe_combine_bwd: dy, y_perm and dy_perm must be 16-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  combine_bwd_kernel<<<grid_for((size_t)T * 32, 256), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(dy),
+  launch_pdl(combine_bwd_kernel, grid_for((size_t)T * 32, 256), 256, 0, s, static_cast<const __nv_bfloat16*>(dy),
                                        static_cast<const __nv_bfloat16*>(y_perm), topk_w,
                                        row_of_slot, T, H, k, T * k,
                                        static_cast<__nv_bfloat16*>(dy_perm), d_w, status_word());
@@ -472,12 +482,12 @@ int moe_dispatch_no_alloc(const void* x, const int32_t* topk_idx, const int32_t*
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* status = status_word();
   const int nc = (int)nchunk;
-  chunk_hist_kernel<<<(nc + 7) / 8, 256, sizeof(int) * 8 * E, s>>>(topk_idx, T, E, k, nc,
+  launch_pdl(chunk_hist_kernel, (nc + 7) / 8, 256, sizeof(int) * 8 * E, s, topk_idx, T, E, k, nc,
                                                                    chunk_base, status);
   if (int rc = check_launch("moe_dispatch_no_alloc: histogram kernel")) return rc;
-  chunk_scan_kernel<<<(E + 7) / 8, 256, 0, s>>>(chunk_base, offsets, nc, E, status);
+  launch_pdl(chunk_scan_kernel, (E + 7) / 8, 256, 0, s, chunk_base, offsets, nc, E, status);
   if (int rc = check_launch("moe_dispatch_no_alloc: scan kernel")) return rc;
-  dispatch_kernel<<<nc, 256, sizeof(int) * (E + kChunkTok * k), s>>>(
+  launch_pdl(dispatch_kernel, nc, 256, sizeof(int) * (E + kChunkTok * k), s, 
       static_cast<const __nv_bfloat16*>(x), topk_idx, chunk_base, T, H, E, k,
       static_cast<__nv_bfloat16*>(x_perm), row_of_slot, token_of_row, status);
   return check_launch("moe_dispatch_no_alloc: row kernel");

@@ -59,6 +59,8 @@ template <bool kVec>
 __global__ void __launch_bounds__(kLogitThreads) router_partials_kernel(
     const __nv_bfloat16* __restrict__ x, const float* __restrict__ Wr, int T, int H, int E,
     float* __restrict__ part) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(16) float lsm[];
   float(*ws)[kLogitStage][kLogitExp] = reinterpret_cast<float(*)[kLogitStage][kLogitExp]>(lsm);
   float(*xs)[kLogitStage][kLogitTok] =
@@ -180,6 +182,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
                                                           int E, int k, int32_t* __restrict__ topk_idx,
                                                           float* __restrict__ topk_w,
                                                           int32_t* __restrict__ counts) {
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int it = 0; it < kTopkTokPerWarp; ++it) {
     const int t = blockIdx.x * kTopkTokPerBlock + warp * kTopkTokPerWarp + it;
@@ -258,6 +262,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
 }
 
 __global__ void zero_counts_kernel(int32_t* __restrict__ counts, int E) {
+  pdl_wait();
+  pdl_trigger();
   for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = 0;
 }
 
@@ -267,6 +273,8 @@ __global__ void __launch_bounds__(1024) router_offsets_kernel(const int32_t* __r
                                                               int E, int ep_size,
                                                               int32_t* __restrict__ offsets,
                                                               int32_t* __restrict__ rank_offsets) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int warp_sum[32];
   __shared__ int excl[kMaxExperts + 1];
   const int e = threadIdx.x;
@@ -324,6 +332,8 @@ __global__ void __launch_bounds__(256) router_bwd_dl_kernel(
     const float* __restrict__ d_w, const float* __restrict__ topk_w,
     const int32_t* __restrict__ topk_idx, int T, int E, int Ep, int k,
     __nv_bfloat16* __restrict__ dl2, __nv_bfloat16* __restrict__ dl3, int* status) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ float rowbuf[];  // [8 warps][Ep]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
@@ -359,6 +369,8 @@ __global__ void __launch_bounds__(256) router_bwd_dl_kernel(
 
 __global__ void router_bwd_wr_kernel(const float* __restrict__ Wr, int H, int E, int Ep,
                                      __nv_bfloat16* __restrict__ wr3) {
+  pdl_wait();
+  pdl_trigger();
   const size_t n = (size_t)H * Ep;
   for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n;
        q += (size_t)gridDim.x * blockDim.x) {
@@ -374,6 +386,8 @@ __global__ void router_bwd_wr_kernel(const float* __restrict__ Wr, int H, int E,
 }
 
 __global__ void split_table_kernel(int32_t* __restrict__ seg, int S, int T) {
+  pdl_wait();
+  pdl_trigger();
   const int s = threadIdx.x;
   if (s <= S) seg[s] = (int)(((long long)s * T) / S);
 }
@@ -381,6 +395,8 @@ __global__ void split_table_kernel(int32_t* __restrict__ seg, int S, int T) {
 // dWr[h,e] (+)= sum_s (P[s][h][e] + P[s][h][Ep+e]), splits in order.
 __global__ void router_bwd_reduce_kernel(const float* __restrict__ P, int S, int H, int E, int Ep,
                                          float* __restrict__ dWr, int accumulate) {
+  pdl_wait();
+  pdl_trigger();
   const size_t n = (size_t)H * E;
   for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n;
        q += (size_t)gridDim.x * blockDim.x) {
@@ -465,7 +481,7 @@ int moe_route_topk(const void* x, const float* Wr, const float* bias, int T, int
     return fail(MOE_ERR_WORKSPACE, "moe_route_topk: workspace %zu < %zu bytes", ws_bytes, need);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* part = static_cast<float*>(ws);
-  zero_counts_kernel<<<1, 256, 0, s>>>(counts, E);
+  launch_pdl(zero_counts_kernel, 1, 256, 0, s, counts, E);
   if (int rc = check_launch("moe_route_topk: zero counts")) return rc;
   if (T > 0) {
     static bool attr_set[64] = {};
@@ -483,29 +499,29 @@ int moe_route_topk(const void* x, const float* Wr, const float* bias, int T, int
     const int nblk_h = (H + kLogitBlockH - 1) / kLogitBlockH;
     dim3 grid((T + kLogitTok - 1) / kLogitTok, nblk_h, (E + kLogitExp - 1) / kLogitExp);
     if (E % 4 == 0)
-      router_partials_kernel<true><<<grid, kLogitThreads, kLogitSmem, s>>>(
+      launch_pdl(router_partials_kernel<true>, grid, kLogitThreads, kLogitSmem, s, 
           static_cast<const __nv_bfloat16*>(x), Wr, T, H, E, part);
     else
-      router_partials_kernel<false><<<grid, kLogitThreads, kLogitSmem, s>>>(
+      launch_pdl(router_partials_kernel<false>, grid, kLogitThreads, kLogitSmem, s, 
           static_cast<const __nv_bfloat16*>(x), Wr, T, H, E, part);
     if (int rc = check_launch("moe_route_topk: logits kernel")) return rc;
     const int nblk = (T + kTopkTokPerBlock - 1) / kTopkTokPerBlock;
     const int nq = (E + 31) / 32;
     if (nq <= 1)
-      router_topk_kernel<1><<<nblk, 256, 0, s>>>(part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
+      launch_pdl(router_topk_kernel<1>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
     else if (nq <= 2)
-      router_topk_kernel<2><<<nblk, 256, 0, s>>>(part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
+      launch_pdl(router_topk_kernel<2>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
     else if (nq <= 4)
-      router_topk_kernel<4><<<nblk, 256, 0, s>>>(part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
+      launch_pdl(router_topk_kernel<4>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
     else if (nq <= 8)
-      router_topk_kernel<8><<<nblk, 256, 0, s>>>(part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
+      launch_pdl(router_topk_kernel<8>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
     else if (nq <= 16)
-      router_topk_kernel<16><<<nblk, 256, 0, s>>>(part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
+      launch_pdl(router_topk_kernel<16>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
     else
-      router_topk_kernel<32><<<nblk, 256, 0, s>>>(part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
+      launch_pdl(router_topk_kernel<32>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
     if (int rc = check_launch("moe_route_topk: top-k kernel")) return rc;
   }
-  router_offsets_kernel<<<1, 1024, 0, s>>>(counts, E, ep_size, offsets, rank_offsets);
+  launch_pdl(router_offsets_kernel, 1, 1024, 0, s, counts, E, ep_size, offsets, rank_offsets);
   return check_launch("moe_route_topk: offsets kernel");
 }
 
@@ -549,22 +565,21 @@ int moe_route_topk_bwd(const float* d_w, const float* topk_w, const int32_t* top
     }
     return MOE_OK;
   }
-  router_bwd_dl_kernel<<<(T + 7) / 8, 256, sizeof(float) * 8 * L.Ep, s>>>(
+  launch_pdl(router_bwd_dl_kernel, (T + 7) / 8, 256, sizeof(float) * 8 * L.Ep, s, 
       d_w, topk_w, topk_idx, T, E, L.Ep, k, dl2, dl3, status);
   if (int rc = check_launch("moe_route_topk_bwd: dl kernel")) return rc;
   const size_t nwr = (size_t)H * L.Ep;
-  router_bwd_wr_kernel<<<(int)((nwr + 255) / 256 < 4096 ? (nwr + 255) / 256 : 4096), 256, 0, s>>>(
+  launch_pdl(router_bwd_wr_kernel, (int)((nwr + 255) / 256 < 4096 ? (nwr + 255) / 256 : 4096), 256, 0, s, 
       Wr, H, E, L.Ep, wr3);
   if (int rc = check_launch("moe_route_topk_bwd: Wr split kernel")) return rc;
-  split_table_kernel<<<1, 128, 0, s>>>(seg, L.S, T);
+  launch_pdl(split_table_kernel, 1, 128, 0, s, seg, L.S, T);
   if (int rc = check_launch("moe_route_topk_bwd: split table")) return rc;
   // dx = bf16(dx_acc + dl . Wr^T)
   if (int rc = launch_dense_add_bf16(dl3, wr3, dx_acc, dx, T, H, 3 * L.Ep, s)) return rc;
   // split-K partials of x^T . [dl_hi | dl_lo]
   if (int rc = launch_dw_split(x, dl2, T, H, 2 * L.Ep, seg, L.S, part, base + L.maps, s)) return rc;
   const size_t nred = (size_t)H * E;
-  router_bwd_reduce_kernel<<<(int)((nred + 255) / 256 < 4096 ? (nred + 255) / 256 : 4096), 256, 0,
-                             s>>>(part, L.S, H, E, L.Ep, dWr, accumulate);
+  launch_pdl(router_bwd_reduce_kernel, (int)((nred + 255) / 256 < 4096 ? (nred + 255) / 256 : 4096), 256, 0, s, part, L.S, H, E, L.Ep, dWr, accumulate);
   return check_launch("moe_route_topk_bwd: reduce kernel");
 }
 
