@@ -125,8 +125,14 @@ struct Cfg {
   static constexpr int B_BYTES = B_BYTES_MAX / CTAS;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TILE_M = BM * CTAS;
-  static constexpr int EP_WARP = gu_tma ? EP_BOX_BYTES * 2 * GU_SETS : EP_WARP_BYTES;
-  static constexpr int EP_TOTAL = 4 * EP_WARP;
+  // The weight-gradient kind (fp32 output, short reductions) runs eight
+  // epilogue warps, two per TMEM lane quadrant, each on half the columns,
+  // with a one-box store ring each.
+  static constexpr int EPW = KIND == DW ? 8 : 4;
+  static constexpr int NTHREADS = 64 + 32 * EPW;
+  static constexpr int RING = KIND == DW ? 1 : EP_SLOTS;
+  static constexpr int EP_WARP = gu_tma ? EP_BOX_BYTES * 2 * GU_SETS : EP_BOX_BYTES * RING;
+  static constexpr int EP_TOTAL = EPW * EP_WARP;
   // without the segment tables
   static constexpr size_t SMEM_FIXED = 1024 + (size_t)STAGES * STAGE_BYTES + EP_TOTAL + sizeof(Ctl);
 };
@@ -202,7 +208,7 @@ __device__ __forceinline__ void for_each_kblock(const Tile& t, const Params& p, 
 }
 
 template <int KIND, int CTAS, bool DEEP>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(Cfg<KIND, CTAS, DEEP>::NTHREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB0,
                         const __grid_constant__ CUtensorMap tmB1,
@@ -234,7 +240,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncthreads();
   }
-  for (int s = threadIdx.x; s <= p.num_seg; s += THREADS) {
+  for (int s = threadIdx.x; s <= p.num_seg; s += C::NTHREADS) {
     // a null table means one segment covering every row
     int o = p.seg_offsets ? p.seg_offsets[s] : (s == 0 ? 0 : limit);
     if (o < 0 || o > limit) {
@@ -244,7 +250,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     ctl->seg_off[s] = o;
   }
   __syncthreads();
-  for (int s = threadIdx.x; s < p.num_seg; s += THREADS) {
+  for (int s = threadIdx.x; s < p.num_seg; s += C::NTHREADS) {
     int e = p.seg_expert ? p.seg_expert[s] : s;
     if (e < 0 || e >= p.num_groups) {
       set_status(p.status, MOE_STATUS_BAD_SEGMENTS);
@@ -257,10 +263,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     ctl->seg_exp[s] = e;
   }
   if (!Traits<KIND>::rows)
-    for (int g = threadIdx.x; g < p.num_groups; g += THREADS) ctl->grp_rows[g] = 0;
+    for (int g = threadIdx.x; g < p.num_groups; g += C::NTHREADS) ctl->grp_rows[g] = 0;
   __syncthreads();
   if (!Traits<KIND>::rows)
-    for (int s = threadIdx.x; s < p.num_seg; s += THREADS)
+    for (int s = threadIdx.x; s < p.num_seg; s += C::NTHREADS)
       if (ctl->seg_exp[s] >= 0) atomicAdd(&ctl->grp_rows[ctl->seg_exp[s]], ctl->seg_off[s + 1] - ctl->seg_off[s]);
   if (warp == 0) {
     if constexpr (Traits<KIND>::rows) {
@@ -295,7 +301,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       for (int i = 0; i < 2; ++i) {
         mbar_init(smem_u32(&ctl->tfull[i]), 1);
-        mbar_init(smem_u32(&ctl->tempty[i]), 4 * CTAS);
+        mbar_init(smem_u32(&ctl->tempty[i]), C::EPW * CTAS);
       }
       mbar_init(smem_u32(&ctl->drain), 1);
       for (int w = 0; w < 4; ++w)
@@ -487,7 +493,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // Full boxes of the fp32 weight gradients and of the down projection go
     // out through TMA bulk stores instead (measured faster for those two).
     constexpr bool kTmaOut = KIND == DW || KIND == DOWN_FWD;
-    EpRing ring{ep_base, 0, lane};
+    EpRing<C::RING> ring{ep_base, 0, lane};
     int gu_ctr = 0;  // DOWN_BWD_DX, DENSE_ADD: running count of this warp's 32-column chunks
     const uint32_t tempty_leader[2] = {
         CTAS == 2 ? map_to_rank(smem_u32(&ctl->tempty[0]), 0) : smem_u32(&ctl->tempty[0]),
@@ -507,7 +513,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // rows x 16 columns).  They arrive by TMA into set (chunk counter mod
       // 4) of the warp's staging, two chunks ahead; the first two are
       // requested before waiting for the MMAs.
-      const uint32_t gu_bar0 = smem_u32(&ctl->ep_bar[warp - 2][0]);
+      const uint32_t gu_bar0 = C::gu_tma ? smem_u32(&ctl->ep_bar[warp - 2][0]) : 0u;
       auto gu_load = [&](int c, int ctr) {
         if (C::gu_tma && any && c < p.BN && lane == 0) {
           const int set = ctr & (C::GU_SETS - 1);
@@ -664,7 +670,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           const bool second = p.split_m > 0 && rb >= p.split_m;
           const int y = p.split_m > 0 ? t.group * p.split_m + (second ? rb - p.split_m : rb)
                                       : t.group * p.M + rb;
-          for (int c = 0; c < p.BN; c += 32) {
+          // with eight epilogue warps, warps 2..5 take the first half of the
+          // columns and warps 6..9 the second
+          const int cspan = p.BN / (C::EPW / 4);
+          const int cbeg = ((warp - 2) >> 2) * cspan;
+          for (int c = cbeg; c < cbeg + cspan; c += 32) {
             uint32_t a[32];
             if (nonempty) {
               tmem_ld32(taddr + c, a);
@@ -796,7 +806,7 @@ int launch(Params p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensor
   if (units < 1) units = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(units * CTAS));
-  cfg.blockDim = dim3(THREADS);
+  cfg.blockDim = dim3(Cfg<KIND, CTAS, DEEP>::NTHREADS);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];

@@ -113,13 +113,14 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32
 }
 
 // One epilogue warp's staging ring (see EP_*).  Lane i holds row i of a box.
+template <int SLOTS = EP_SLOTS>
 struct EpRing {
   uint8_t* base;
   int slot;
   int lane;
   __device__ __forceinline__ uint8_t* acquire() {
-    // the store issued from this slot EP_SLOTS boxes ago must have read it
-    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+    // the store issued from this slot SLOTS boxes ago must have read it
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(SLOTS - 1) : "memory");
     __syncwarp();
     return base + slot * EP_BOX_BYTES;
   }
@@ -138,7 +139,7 @@ struct EpRing {
         tma_store_2d(map, smem_u32(box), x, y);
       asm volatile("cp.async.bulk.commit_group;" ::: "memory");
     }
-    slot = (slot + 1) & (EP_SLOTS - 1);
+    slot = (slot + 1) & (SLOTS - 1);
   }
   __device__ __forceinline__ void drain() {
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
