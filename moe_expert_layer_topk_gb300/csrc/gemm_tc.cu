@@ -40,7 +40,6 @@ namespace tc {
 
 constexpr int A_BYTES = BM * BK * 2;          // 16 KiB
 constexpr int B_BYTES_MAX = 256 * BK * 2;     // 32 KiB
-constexpr int EP_WARP_BYTES = EP_BOX_BYTES * EP_SLOTS;
 // DOWN_BWD_DX also loads the saved g, u boxes by TMA: 4 sets of (g, u) slots.
 constexpr int EP_GU_SETS = 4;
 
@@ -112,39 +111,36 @@ struct Traits {
 // (cluster rank 0) issues the MMAs, which read both CTAs' shared memory and
 // write each CTA's 128 accumulator rows into that CTA's TMEM.
 //
-// The kinds whose epilogue reads a second input tile by TMA (SwiGLU
-// backward: saved g, u; router dX: the fp32 addend) stage GU_SETS sets of
-// it, GU_SETS/2 chunks ahead, and run one pipeline stage fewer.  DEEP (the
-// SwiGLU-backward kind, when the segment tables are small enough) keeps all
-// four stages and stages two sets, one chunk ahead.
-template <int KIND, int CTAS, bool DEEP = false>
+// The router dX kind reads its fp32 addend by TMA into GU_SETS staging
+// sets, GU_SETS/2 chunks ahead, and runs one pipeline stage fewer.
+template <int KIND, int CTAS>
 struct Cfg {
-  static constexpr bool gu_tma = KIND == DOWN_BWD_DX || KIND == DENSE_ADD;
-  static constexpr int GU_SETS = DEEP ? 2 : EP_GU_SETS;
-  static constexpr int STAGES = CTAS == 1 ? ((gu_tma && !DEEP) ? 3 : 4) : (gu_tma ? 4 : 6);
+  static constexpr bool gu_tma = KIND == DENSE_ADD;
+  static constexpr int GU_SETS = EP_GU_SETS;
+  static constexpr int STAGES = CTAS == 1 ? (gu_tma ? 3 : 4) : (gu_tma ? 4 : 6);
   static constexpr int B_BYTES = B_BYTES_MAX / CTAS;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TILE_M = BM * CTAS;
-  // The weight-gradient kind (fp32 output, short reductions) runs eight
-  // epilogue warps, two per TMEM lane quadrant, each on half the columns,
-  // with a one-box store ring each.
-  static constexpr int EPW = KIND == DW ? 8 : 4;
+  // The weight-gradient kind (fp32 output, short reductions) and the
+  // SwiGLU-backward kind (heavy epilogue) run eight epilogue warps, two per
+  // TMEM lane quadrant, each on half the columns (a one-box store ring each).
+  static constexpr int EPW = (KIND == DW || KIND == DOWN_BWD_DX) ? 8 : 4;
   static constexpr int NTHREADS = 64 + 32 * EPW;
-  static constexpr int RING = KIND == DW ? 1 : EP_SLOTS;
+  static constexpr int RING = (KIND == DW || KIND == DOWN_BWD_DX) ? 1 : EP_SLOTS;
   static constexpr int EP_WARP = gu_tma ? EP_BOX_BYTES * 2 * GU_SETS : EP_BOX_BYTES * RING;
   static constexpr int EP_TOTAL = EPW * EP_WARP;
   // without the segment tables
   static constexpr size_t SMEM_FIXED = 1024 + (size_t)STAGES * STAGE_BYTES + EP_TOTAL + sizeof(Ctl);
 };
+// the configurations launched (cluster pairs only for GATE_UP_BWD_DX)
 static_assert(Cfg<GATE_UP_FWD, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
-                  Cfg<GATE_UP_FWD, 2>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
+                  Cfg<DOWN_FWD, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<DOWN_BWD_DX, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
-                  Cfg<DOWN_BWD_DX, 2>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
+                  Cfg<GATE_UP_BWD_DX, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
+                  Cfg<GATE_UP_BWD_DX, 2>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<DENSE_ADD, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<DW, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax,
               "shared memory budget exceeded");
-static_assert(Cfg<DOWN_BWD_DX, 1, true>::SMEM_FIXED + seg_table_bytes(128, 0, false) <= kSmemMax,
-              "the deep SwiGLU-backward configuration must fit 128 segments");
 
 struct Tile {
   int group;   // expert (row kinds) / output group (DW)
@@ -207,8 +203,8 @@ __device__ __forceinline__ void for_each_kblock(const Tile& t, const Params& p, 
   }
 }
 
-template <int KIND, int CTAS, bool DEEP>
-__global__ void __launch_bounds__(Cfg<KIND, CTAS, DEEP>::NTHREADS, 1)
+template <int KIND, int CTAS>
+__global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB0,
                         const __grid_constant__ CUtensorMap tmB1,
@@ -216,7 +212,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS, DEEP>::NTHREADS, 1)
                         const __grid_constant__ CUtensorMap tmO1, const Params p) {
   pdl_wait();
   pdl_trigger();
-  using C = Cfg<KIND, CTAS, DEEP>;
+  using C = Cfg<KIND, CTAS>;
   constexpr int STG = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -494,7 +490,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS, DEEP>::NTHREADS, 1)
     // out through TMA bulk stores instead (measured faster for those two).
     constexpr bool kTmaOut = KIND == DW || KIND == DOWN_FWD;
     EpRing<C::RING> ring{ep_base, 0, lane};
-    int gu_ctr = 0;  // DOWN_BWD_DX, DENSE_ADD: running count of this warp's 32-column chunks
+    int gu_ctr = 0;  // DENSE_ADD: running count of this warp's 32-column chunks
     const uint32_t tempty_leader[2] = {
         CTAS == 2 ? map_to_rank(smem_u32(&ctl->tempty[0]), 0) : smem_u32(&ctl->tempty[0]),
         CTAS == 2 ? map_to_rank(smem_u32(&ctl->tempty[1]), 0) : smem_u32(&ctl->tempty[1])};
@@ -507,12 +503,11 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS, DEEP>::NTHREADS, 1)
       const int lim = Traits<KIND>::rows ? t.row_end : p.M;
       const int nvalid = lim - rb < 0 ? 0 : (lim - rb > 32 ? 32 : lim - rb);
       const bool any = nvalid > 0;
-      // Second input of the epilogue, which does not depend on the
-      // accumulator: SwiGLU backward reads the saved g, u boxes (32 rows x
-      // 32 bf16 columns each), router dX the fp32 addend (two boxes of 32
-      // rows x 16 columns).  They arrive by TMA into set (chunk counter mod
-      // 4) of the warp's staging, two chunks ahead; the first two are
-      // requested before waiting for the MMAs.
+      // Router dX: the fp32 addend, which does not depend on the
+      // accumulator (two boxes of 32 rows x 16 columns per 32-column
+      // chunk), arrives by TMA into set (chunk counter mod GU_SETS) of the
+      // warp's staging, GU_SETS/2 chunks ahead; the first ones are requested
+      // before waiting for the MMAs.
       const uint32_t gu_bar0 = C::gu_tma ? smem_u32(&ctl->ep_bar[warp - 2][0]) : 0u;
       auto gu_load = [&](int c, int ctr) {
         if (C::gu_tma && any && c < p.BN && lane == 0) {
@@ -522,13 +517,33 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS, DEEP>::NTHREADS, 1)
           const uint32_t g_slot = smem_u32(ep_base + (2 * set) * EP_BOX_BYTES);
           mbar_arrive_expect_tx(bar, 2 * EP_BOX_BYTES);
           tma_load_2d(g_slot, &tmB1, bar, t.n0 + c, rb);
-          tma_load_2d(g_slot + EP_BOX_BYTES, &tmB1, bar, (KIND == DENSE_ADD ? 16 : p.I) + t.n0 + c, rb);
+          tma_load_2d(g_slot + EP_BOX_BYTES, &tmB1, bar, 16 + t.n0 + c, rb);
         }
       };
       constexpr int GU_AHEAD = C::GU_SETS / 2;  // chunks requested ahead
       if constexpr (C::gu_tma) {
 #pragma unroll
         for (int a = 0; a < GU_AHEAD; ++a) gu_load(32 * a, gu_ctr + a);
+      }
+      // with eight epilogue warps, warps 2..5 take the first half of the
+      // tile's columns and warps 6..9 the second
+      const int cspan = p.BN / (C::EPW / 4);
+      const int cbeg = ((warp - 2) >> 2) * cspan;
+      // SwiGLU backward: this lane's row of the saved g, u for a 32-column chunk
+      uint4 gq[4], uq[4];
+      auto ld_gu = [&](int c, uint4 (&g4)[4], uint4 (&u4)[4]) {
+        const bool ok = lane < nvalid;
+        const uint4* row = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.aux) +
+                                                          (size_t)(ok ? rb + lane : 0) * p.I * 4);
+        const int v = (t.n0 + c) >> 3, vu = (p.I + t.n0 + c) >> 3;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          g4[i] = ok ? __ldg(row + v + i) : make_uint4(0, 0, 0, 0);
+          u4[i] = ok ? __ldg(row + vu + i) : make_uint4(0, 0, 0, 0);
+        }
+      };
+      if constexpr (KIND == DOWN_BWD_DX) {
+        if (any) ld_gu(cbeg, gq, uq);
       }
       if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&ctl->tfull[buf]), use & 1u, &ctl->abort_flag, p.status))) break;
       tc_fence_after();
@@ -593,7 +608,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS, DEEP>::NTHREADS, 1)
         }
       } else if constexpr (KIND == DENSE_ADD) {
         // out = bf16(acc + add): the addend's two 16-column boxes of this
-        // chunk sit in set (gu_ctr mod 4); the result goes out through the
+        // chunk sit in set (gu_ctr mod GU_SETS); the result goes out through the
         // first box of the set.
         const size_t pitch = (size_t)p.ldo * 2;
         for (int c = 0; any && c < p.BN; c += 32, ++gu_ctr) {
@@ -624,23 +639,21 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS, DEEP>::NTHREADS, 1)
           flush(lo, p.out0, pitch, (size_t)(t.n0 + c) * 2, rb, nvalid, false);
         }
       } else if constexpr (KIND == DOWN_BWD_DX) {
+        // The saved g, u of this lane's row and chunk come from global memory
+        // straight into registers, one chunk ahead; dg and du leave through
+        // the warp's box as coalesced row stores.
         const size_t pitch = (size_t)p.I * 4;
-        for (int c = 0; any && c < p.BN; c += 32, ++gu_ctr) {
-          gu_load(c + 32 * GU_AHEAD, gu_ctr + GU_AHEAD);
+        for (int c = cbeg; any && c < cbeg + cspan; c += 32) {
+          uint4 gn[4], un[4];
+          if (c + 32 < cbeg + cspan) ld_gu(c + 32, gn, un);
           uint32_t a[32];
           tmem_ld32(taddr + c, a);
-          const int set = gu_ctr & (C::GU_SETS - 1);
-          uint8_t* gbox = ep_base + (2 * set) * EP_BOX_BYTES;
-          uint8_t* ubox = gbox + EP_BOX_BYTES;
-          const bool ok = __all_sync(0xffffffffu, wait_bar(gu_bar0 + 8u * (uint32_t)set,
-                                                           (uint32_t)(gu_ctr / C::GU_SETS) & 1u, &ctl->abort_flag, p.status));
           tmem_wait_ld();
-          if (!ok) break;
+          uint4 og4[4], ou4[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const uint4 gv = get(gbox, i), uv = get(ubox, i);
-            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-            const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+            const uint32_t gw[4] = {gq[i].x, gq[i].y, gq[i].z, gq[i].w};
+            const uint32_t uw[4] = {uq[i].x, uq[i].y, uq[i].z, uq[i].w};
             uint32_t og[4], ou[4];
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
@@ -657,12 +670,20 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS, DEEP>::NTHREADS, 1)
               og[jj] = pack_bf16x2(dg2[0], dg2[1]);
               ou[jj] = pack_bf16x2(du2[0], du2[1]);
             }
-            // results overwrite the g, u boxes in place (each lane its own row)
-            put(gbox, i, make_uint4(og[0], og[1], og[2], og[3]));
-            put(ubox, i, make_uint4(ou[0], ou[1], ou[2], ou[3]));
+            og4[i] = make_uint4(og[0], og[1], og[2], og[3]);
+            ou4[i] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
           }
-          flush(gbox, p.out0, pitch, (size_t)(t.n0 + c) * 2, rb, nvalid, false);
-          flush(ubox, p.out0, pitch, (size_t)(p.I + t.n0 + c) * 2, rb, nvalid, false);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) put(ep_base, i, og4[i]);
+          flush(ep_base, p.out0, pitch, (size_t)(t.n0 + c) * 2, rb, nvalid, false);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) put(ep_base, i, ou4[i]);
+          flush(ep_base, p.out0, pitch, (size_t)(p.I + t.n0 + c) * 2, rb, nvalid, false);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            gq[i] = gn[i];
+            uq[i] = un[i];
+          }
         }
       } else {  // DW: fp32 [group, M, N] (optionally split at split_m over two tensors)
         const bool nonempty = ctl->grp_rows[t.group] > 0;
@@ -670,10 +691,6 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS, DEEP>::NTHREADS, 1)
           const bool second = p.split_m > 0 && rb >= p.split_m;
           const int y = p.split_m > 0 ? t.group * p.split_m + (second ? rb - p.split_m : rb)
                                       : t.group * p.M + rb;
-          // with eight epilogue warps, warps 2..5 take the first half of the
-          // columns and warps 6..9 the second
-          const int cspan = p.BN / (C::EPW / 4);
-          const int cbeg = ((warp - 2) >> 2) * cspan;
           for (int c = cbeg; c < cbeg + cspan; c += 32) {
             uint32_t a[32];
             if (nonempty) {
@@ -769,13 +786,13 @@ bool use_pair(int bn) { return bn >= 128; }
 template <int KIND>
 bool pair_for(int bn) { return KIND == GATE_UP_BWD_DX && use_pair(bn); }
 
-bool g_attr[6][2][2][64] = {};
+bool g_attr[6][2][64] = {};
 
-// Launches grouped_gemm_kernel<KIND, CTAS, DEEP>: completes the
-// CTAS-dependent parameters, sizes the shared memory to the segment tables
-// and the persistent grid to the SM count and, for pairs, sets the cluster
+// Launches grouped_gemm_kernel<KIND, CTAS>: completes the CTAS-dependent
+// parameters, sizes the shared memory to the segment tables and the
+// persistent grid to the SM count and, for pairs, sets the cluster
 // dimension.
-template <int KIND, int CTAS, bool DEEP = false>
+template <int KIND, int CTAS>
 int launch(Params p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
            const CUtensorMap& o0, const CUtensorMap& o1, cudaStream_t s, const char* what) {
   constexpr bool a_mn = KIND == DW;
@@ -790,14 +807,14 @@ int launch(Params p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensor
   }
   const int dev = current_device();
   if (dev < 0) return fail(MOE_ERR_CUDA, "%s: no current CUDA device", what);
-  auto kern = grouped_gemm_kernel<KIND, CTAS, DEEP>;
-  const size_t smem_sz = Cfg<KIND, CTAS, DEEP>::SMEM_FIXED + seg_table_bytes(p.num_seg, p.num_groups, KIND == DW);
+  auto kern = grouped_gemm_kernel<KIND, CTAS>;
+  const size_t smem_sz = Cfg<KIND, CTAS>::SMEM_FIXED + seg_table_bytes(p.num_seg, p.num_groups, KIND == DW);
   if (smem_sz > kSmemMax) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "%s: segment tables too large", what);
   const int smem = (int)smem_sz;
-  if (!g_attr[KIND][CTAS - 1][DEEP][dev]) {
+  if (!g_attr[KIND][CTAS - 1][dev]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMax);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
-    g_attr[KIND][CTAS - 1][DEEP][dev] = true;
+    g_attr[KIND][CTAS - 1][dev] = true;
   }
   const int sms = sm_count();
   if (sms <= 0) return fail(MOE_ERR_CUDA, "%s: cannot query the SM count", what);
@@ -806,7 +823,7 @@ int launch(Params p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensor
   if (units < 1) units = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(units * CTAS));
-  cfg.blockDim = dim3(Cfg<KIND, CTAS, DEEP>::NTHREADS);
+  cfg.blockDim = dim3(Cfg<KIND, CTAS>::NTHREADS);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -826,18 +843,12 @@ int launch(Params p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensor
   return check_launch(what);
 }
 
-// Cluster pairs are built only for the gate/up backward dX GEMM; the
-// SwiGLU-backward GEMM runs its deep configuration whenever its segment
-// tables leave room for it.
+// Cluster pairs are built only for the gate/up backward dX GEMM.
 template <int KIND>
 int run(bool pair, const Params& p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
         const CUtensorMap& o0, const CUtensorMap& o1, cudaStream_t s, const char* what) {
   if constexpr (KIND == GATE_UP_BWD_DX) {
     if (pair) return launch<KIND, 2>(p, a, b0, b1, o0, o1, s, what);
-  }
-  if constexpr (KIND == DOWN_BWD_DX) {
-    if (Cfg<KIND, 1, true>::SMEM_FIXED + seg_table_bytes(p.num_seg, p.num_groups, false) <= kSmemMax)
-      return launch<KIND, 1, true>(p, a, b0, b1, o0, o1, s, what);
   }
   return launch<KIND, 1>(p, a, b0, b1, o0, o1, s, what);
 }
@@ -1043,10 +1054,9 @@ int moe_grouped_gemm_down_bwd(const void* dy_perm, const void* h, const void* gu
     CUtensorMap ta, tb;
     if (int rc = make_tmap(&ta, dy_perm, H, R, 64, BM)) return rc;
     if (int rc = make_tmap_mn(&tb, Wd, I, (uint64_t)E * H, p.BN / 64)) return rc;
-    CUtensorMap to, tgu;
+    CUtensorMap to;
     if (int rc = make_out_map(&to, dgu, 2 * I, R, false)) return rc;
-    if (int rc = make_out_map(&tgu, gu_save, 2 * I, R, false)) return rc;  // g,u boxes in
-    if (int rc = run<DOWN_BWD_DX>(false, p, ta, tb, tgu, to, to, s, fn))
+    if (int rc = run<DOWN_BWD_DX>(false, p, ta, tb, tb, to, to, s, fn))
       return rc;
   }
   // dWd[e] = dy_perm[rows of e]^T . h[rows of e]
