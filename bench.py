@@ -297,7 +297,7 @@ def run_ours(args, shape, inp):
     fin = make_layer_inputs(fshape, 0)
     fg = {n: (v.to(dev) if isinstance(v, torch.Tensor) else v) for n, v in fin.items()}
     flayer = m.MoELayer(fshape.T, fshape.H, fshape.I, fshape.E, fshape.k, fshape.ep_size,
-                        training=False, device=dev)
+                        training=False, fused_dispatch=True, device=dev)
     for _ in range(args.warmup):
         flayer.forward(fg["x"], fg["Wr"], fg["bias"], fg["Wg"], fg["Wu"], fg["Wd"])
     fs, fe = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -392,7 +392,8 @@ def run_ours(args, shape, inp):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (1.2 GB of expert weights per step)"},
         "fwd_tokens_per_s": fshape.T / (fwd_ms * 1e-3),
-        "fwd_ms": fwd_ms, "fwd_config": {"workload": FWD_WORKLOAD, "T": fshape.T},
+        "fwd_ms": fwd_ms, "fwd_config": {"workload": FWD_WORKLOAD, "T": fshape.T,
+                       "path": "fused dispatch: rows gathered from x by the gate/up GEMM"},
         "grouped_gemm_tflops": gemm_tflops,
         "per_call_ms": per_call,
         "roofline": {"bound": "tensor", "kernel": "grouped_gemm gate/up + SwiGLU (forward)",

@@ -186,6 +186,20 @@ int moe_grouped_gemm_swiglu(const void* x_perm, const void* Wg, const void* Wu, 
                             int I, int E, void* h, void* gu_save, void* ws, size_t ws_bytes,
                             void* stream);
 
+/* A3 + A4 fused (the first "next" step after the path: the dispatcher the
+ * pages call fused, "FSDPTurbo EP/EFSDP and LlamaFactory FSDP2/CP Design"
+ * section 3, taken one step further): moe_grouped_gemm_swiglu on the rows
+ * x_perm[r] = x[token_of_row[r]] without x_perm in memory -- the GEMM loads
+ * its A rows from x by token id.  Results are bit-identical to
+ * moe_dispatch + moe_grouped_gemm_swiglu.  x bf16 [T,H]; token_of_row int32
+ * [R] from moe_dispatch, which may then be called with x_perm = NULL.  A
+ * token id outside [0,T) inside a segment reads token 0 and sets
+ * MOE_STATUS_BAD_INDEX.  No workspace. */
+int moe_grouped_gemm_swiglu_gather(const void* x, const int32_t* token_of_row, int T,
+                                   const void* Wg, const void* Wu, int num_seg,
+                                   const int32_t* seg_offsets, const int32_t* seg_expert, int R,
+                                   int H, int I, int E, void* h, void* gu_save, void* stream);
+
 /* A5  grouped down GEMM: y_perm[r] = h[r] . Wd[e]^T (fp32 accumulation) -> bf16.
  * h bf16 [R,I]; Wd bf16 [E,H,I]; y_perm bf16 [R,H].  ws may be NULL. */
 int moe_grouped_gemm_down(const void* h, const void* Wd, int num_seg, const int32_t* seg_offsets,

@@ -18,7 +18,8 @@ import torch
 from . import build as _build_mod
 
 __all__ = ["lib", "MoEError", "LIB_PATH", "ENTRY_POINTS",
-           "moe_route_topk", "moe_dispatch", "moe_dispatch_no_alloc", "moe_grouped_gemm_swiglu", "moe_grouped_gemm_down",
+           "moe_route_topk", "moe_dispatch", "moe_dispatch_no_alloc", "moe_grouped_gemm_swiglu",
+           "moe_grouped_gemm_swiglu_gather", "moe_grouped_gemm_down",
            "moe_combine", "moe_combine_bwd", "moe_grouped_gemm_down_bwd",
            "moe_grouped_gemm_swiglu_bwd", "moe_dispatch_bwd", "moe_route_topk_bwd",
            "moe_route_topk_workspace_size", "moe_dispatch_workspace_size",
@@ -41,6 +42,7 @@ ENTRY_POINTS = {
     "moe_dispatch_no_alloc_max_scratch": ([], _Z),
     "moe_dispatch_no_alloc": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
     "moe_grouped_gemm_swiglu": ([_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P], _I),
+    "moe_grouped_gemm_swiglu_gather": ([_P, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_grouped_gemm_down": ([_P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _P], _I),
     "moe_combine": ([_P, _P, _P, _I, _I, _I, _P, _P], _I),
     "moe_combine_bwd": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _P], _I),
@@ -160,6 +162,12 @@ def moe_grouped_gemm_swiglu(x_perm, Wg, Wu, num_seg, seg_offsets, seg_expert, R,
     _call("moe_grouped_gemm_swiglu", _ptr(x_perm), _ptr(Wg), _ptr(Wu), num_seg, _ptr(seg_offsets),
           _ptr(seg_expert), R, H, I, E, _ptr(h), _ptr(gu_save), _ptr(ws), _nbytes(ws),
           _stream(stream))
+
+
+def moe_grouped_gemm_swiglu_gather(x, token_of_row, T, Wg, Wu, num_seg, seg_offsets, seg_expert, R, H,
+                                   I, E, h, gu_save=None, stream=None):
+    _call("moe_grouped_gemm_swiglu_gather", _ptr(x), _ptr(token_of_row), T, _ptr(Wg), _ptr(Wu), num_seg,
+          _ptr(seg_offsets), _ptr(seg_expert), R, H, I, E, _ptr(h), _ptr(gu_save), _stream(stream))
 
 
 def moe_grouped_gemm_down(h, Wd, num_seg, seg_offsets, seg_expert, R, H, I, E, y_perm, ws=None,

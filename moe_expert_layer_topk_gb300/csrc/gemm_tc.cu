@@ -66,6 +66,8 @@ struct Params {
   void* out0;
   void* out1;
   const void* aux;
+  const int32_t* gather_rows;   // GATE_UP_FWD: A row r is x[gather_rows[r]] (token_of_row), else null
+  int gather_limit;             // tokens in x
   const CUtensorMap* seg_maps;  // DW: per segment s, the A map (2s) and the B map (2s+1)
   int* status;
 };
@@ -125,7 +127,9 @@ struct Cfg {
   // SwiGLU-backward kind (heavy epilogue) run eight epilogue warps, two per
   // TMEM lane quadrant, each on half the columns (a one-box store ring each).
   static constexpr int EPW = (KIND == DW || KIND == DOWN_BWD_DX) ? 8 : 4;
-  static constexpr int NTHREADS = 64 + 32 * EPW;
+  // GATE_UP_FWD: four more warps share the row gather (when A rows come from x)
+  static constexpr int GW = KIND == GATE_UP_FWD ? 4 : 0;
+  static constexpr int NTHREADS = 64 + 32 * (EPW + GW);
   static constexpr int RING = (KIND == DW || KIND == DOWN_BWD_DX) ? 1 : EP_SLOTS;
   static constexpr int EP_WARP = gu_tma ? EP_BOX_BYTES * 2 * GU_SETS : EP_BOX_BYTES * RING;
   static constexpr int EP_TOTAL = EPW * EP_WARP;
@@ -292,7 +296,8 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
     }
     if (lane == 0) {
       for (int i = 0; i < STG; ++i) {
-        mbar_init(smem_u32(&ctl->full[i]), 1);
+        // gather mode: lane 0's arming arrival plus one cp.async arrival per gathering lane
+        mbar_init(smem_u32(&ctl->full[i]), (KIND == GATE_UP_FWD && p.gather_rows) ? 1 + 32 * (1 + C::GW) : 1);
         mbar_init(smem_u32(&ctl->empty[i]), 1);
       }
       for (int i = 0; i < 2; ++i) {
@@ -321,9 +326,77 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
   const int total = ctl->total_tiles;
   const uint32_t b_bytes = (uint32_t)p.BN * BK * 2 / CTAS;  // this CTA's share of a B stage
 
+  // GATE_UP_FWD with gathered A rows: warp 0 and the GW helper warps copy the
+  // A tile's rows from x by token id with cp.async (per instruction a warp
+  // copies four whole 128-byte rows, 8 lanes per row, into the
+  // 128-byte-swizzled tile) and each lane arrives on the stage's barrier when
+  // its copies land; warp 0's lane 0 also arms the barrier for the gate and
+  // up tiles, which come by TMA.
+  auto gather_loop = [&](int gw) {
+    constexpr int NG = 32 * (1 + C::GW);            // gathering lanes
+    constexpr int PIECES = BM * 8;                   // 16-byte pieces of an A tile
+    constexpr int NI = (PIECES + NG - 1) / NG;
+    const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.aux);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    const int nkb = p.K / BK;
+    const int c = lane & 7;  // 16-byte chunk of a row
+    for (int tile = unit; ok && tile < total; tile += nunits) {
+      const Tile t = decode_tile<KIND, CTAS>(tile, p, ctl, rank);
+      int tok[NI];
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        const int piece = i * NG + gw * 32 + lane;
+        const int r = t.m0 + piece / 8;
+        int v = (piece < PIECES && r < p.M) ? p.gather_rows[r] : 0;
+        if (v < 0 || v >= p.gather_limit) {
+          if (r < t.row_end && c == 0) set_status(p.status, MOE_STATUS_BAD_INDEX);
+          v = 0;
+        }
+        tok[i] = v;
+      }
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&ctl->empty[stage]), phase ^ 1u, &ctl->abort_flag,
+                                              p.status))) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = smem_u32(&ctl->full[stage]);
+        const uint32_t sA = smem_u32(smem + (size_t)stage * C::STAGE_BYTES);
+        const int k0 = kb * BK;
+        if (gw == 0 && lane == 0) {
+          const uint32_t sB = sA + A_BYTES;
+          mbar_arrive_expect_tx(fb, b_bytes);
+          const int brow = t.group * p.b_group_rows + t.n0;
+          tma_load_2d(sB, &tmB0, fb, k0, brow);
+          tma_load_2d(sB + (uint32_t)p.NH * BK * 2, &tmB1, fb, k0, brow);
+        }
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+          const int piece = i * NG + gw * 32 + lane;
+          if (piece < PIECES) {
+            const int row = piece / 8;
+            const __nv_bfloat16* src = xg + (size_t)tok[i] * p.K + k0 + 8 * c;
+            const uint32_t dst = sA + (uint32_t)row * 128 + (uint32_t)((c ^ (row & 7)) << 4);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+          }
+        }
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(fb) : "memory");
+        if (++stage == STG) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  };
+
   if (warp == 0) {
     // ============================ TMA producer ============================
-    if (lane == 0) {
+    if (KIND == GATE_UP_FWD && p.gather_rows != nullptr) {
+      gather_loop(0);
+    } else if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -412,6 +485,8 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
           // only the 16-deep MMA steps that hold valid rows are issued.
           const int nkk = KIND == DW ? (valid + 15) / 16 : BK / 16;
           tc_fence_after();
+          if (KIND == GATE_UP_FWD && p.gather_rows)  // A was written by cp.async (generic proxy)
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           if (lane == 0) {
             const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
 #pragma unroll
@@ -446,6 +521,9 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
         }
       }
     }
+  } else if (warp >= 2 + C::EPW) {
+    // ======================= row-gather helper warps ========================
+    if (KIND == GATE_UP_FWD && p.gather_rows != nullptr) gather_loop(warp - (1 + C::EPW));
   } else {
     // ============================ epilogue ================================
     // Each warp owns 32 accumulator rows of the tile (TMEM lanes
@@ -956,6 +1034,45 @@ int launch_dw_split(const void* A, const void* B, int K_rows, int M, int N,
 using namespace moe;
 using namespace moe::tc;
 
+namespace moe {
+namespace tc {
+
+// Gate/up GEMM + SwiGLU on A rows x_perm[r] (gather_rows == nullptr) or
+// x[gather_rows[r]] (rows copied by cp.async in the producer warp).
+int swiglu_impl(const void* a_src, const int32_t* gather_rows, int T, const void* Wg, const void* Wu,
+                int num_seg, const int32_t* seg_offsets, const int32_t* seg_expert, int R, int H,
+                int I, int E, void* h, void* gu_save, cudaStream_t s, const char* fn) {
+  Params p = base_params(num_seg, seg_offsets, seg_expert, E);
+  p.M = R;
+  p.N = I;
+  p.K = H;
+  p.NH = (I % 128 == 0) ? 128 : 64;
+  p.BN = 2 * p.NH;
+  p.n_tiles = I / p.NH;
+  p.b_group_rows = I;
+  p.I = I;
+  p.out0 = h;
+  p.out1 = gu_save;
+  p.gather_rows = gather_rows;
+  p.gather_limit = T;
+  CUtensorMap ta, tg, tu;
+  if (gather_rows) {
+    p.aux = a_src;  // x rows are copied by cp.async; the A map is unused
+    if (int rc = make_tmap(&ta, a_src, H, T, 64, 64)) return rc;
+  } else {
+    if (int rc = make_tmap(&ta, a_src, H, R, 64, BM)) return rc;
+  }
+  if (int rc = make_tmap(&tg, Wg, H, (uint64_t)E * I, 64, p.NH)) return rc;
+  if (int rc = make_tmap(&tu, Wu, H, (uint64_t)E * I, 64, p.NH)) return rc;
+  CUtensorMap th, tgu;
+  if (int rc = make_out_map(&th, h, I, R, false)) return rc;
+  if (int rc = make_out_map(&tgu, gu_save ? gu_save : h, gu_save ? 2 * I : I, R, false)) return rc;
+  return run<GATE_UP_FWD>(false, p, ta, tg, tu, th, tgu, s, fn);
+}
+
+}  // namespace tc
+}  // namespace moe
+
 extern "C" {
 
 size_t moe_grouped_gemm_bwd_workspace_size(int num_seg) {
@@ -975,25 +1092,26 @@ int moe_grouped_gemm_swiglu(const void* x_perm, const void* Wg, const void* Wu, 
       (gu_save && !aligned16(gu_save)))
     return fail(MOE_ERR_ALIGNMENT, "%s: tensors must be 16-byte aligned", fn);
   if (R == 0 || num_seg == 0) return MOE_OK;
-  Params p = base_params(num_seg, seg_offsets, seg_expert, E);
-  p.M = R;
-  p.N = I;
-  p.K = H;
-  p.NH = (I % 128 == 0) ? 128 : 64;
-  p.BN = 2 * p.NH;
-  p.n_tiles = I / p.NH;
-  p.b_group_rows = I;
-  p.I = I;
-  p.out0 = h;
-  p.out1 = gu_save;
-  CUtensorMap ta, tg, tu;
-  if (int rc = make_tmap(&ta, x_perm, H, R, 64, BM)) return rc;
-  if (int rc = make_tmap(&tg, Wg, H, (uint64_t)E * I, 64, p.NH)) return rc;
-  if (int rc = make_tmap(&tu, Wu, H, (uint64_t)E * I, 64, p.NH)) return rc;
-  CUtensorMap th, tgu;
-  if (int rc = make_out_map(&th, h, I, R, false)) return rc;
-  if (int rc = make_out_map(&tgu, gu_save ? gu_save : h, gu_save ? 2 * I : I, R, false)) return rc;
-  return run<GATE_UP_FWD>(false, p, ta, tg, tu, th, tgu, static_cast<cudaStream_t>(stream), fn);
+  return swiglu_impl(x_perm, nullptr, 0, Wg, Wu, num_seg, seg_offsets, seg_expert, R, H, I, E, h,
+                     gu_save, static_cast<cudaStream_t>(stream), fn);
+}
+
+int moe_grouped_gemm_swiglu_gather(const void* x, const int32_t* token_of_row, int T,
+                                   const void* Wg, const void* Wu, int num_seg,
+                                   const int32_t* seg_offsets, const int32_t* seg_expert, int R,
+                                   int H, int I, int E, void* h, void* gu_save, void* stream) {
+  clear_error();
+  const char* fn = "moe_grouped_gemm_swiglu_gather";
+  if (int rc = check_grouped(fn, num_seg, seg_offsets, R, H, I, E)) return rc;
+  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "%s: need T>=0", fn);
+  if (R > 0 && num_seg > 0 && (!x || !token_of_row || !Wg || !Wu || !h || T == 0))
+    return fail(MOE_ERR_INVALID_ARG, "%s: NULL pointer argument or no tokens", fn);
+  if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(h) ||
+      (gu_save && !aligned16(gu_save)))
+    return fail(MOE_ERR_ALIGNMENT, "%s: tensors must be 16-byte aligned", fn);
+  if (R == 0 || num_seg == 0) return MOE_OK;
+  return swiglu_impl(x, token_of_row, T, Wg, Wu, num_seg, seg_offsets, seg_expert, R, H, I, E, h,
+                     gu_save, static_cast<cudaStream_t>(stream), fn);
 }
 
 int moe_grouped_gemm_down(const void* h, const void* Wd, int num_seg, const int32_t* seg_offsets,

@@ -12,7 +12,8 @@ import torch
 from . import (moe_combine, moe_combine_bwd, moe_dispatch, moe_dispatch_bwd,
                moe_dispatch_workspace_size, moe_grouped_gemm_bwd_workspace_size,
                moe_grouped_gemm_down, moe_grouped_gemm_down_bwd,
-               moe_grouped_gemm_swiglu, moe_grouped_gemm_swiglu_bwd, moe_route_topk,
+               moe_grouped_gemm_swiglu, moe_grouped_gemm_swiglu_bwd,
+               moe_grouped_gemm_swiglu_gather, moe_route_topk,
                moe_route_topk_bwd, moe_route_topk_bwd_workspace_size,
                moe_route_topk_workspace_size)
 
@@ -22,13 +23,22 @@ def _ws(nbytes: int, device) -> torch.Tensor:
 
 
 class MoELayer:
-    """One layer's buffers for T tokens of hidden size H, E experts of size I, top-k."""
+    """One layer's buffers for T tokens of hidden size H, E experts of size I, top-k.
+
+    fused_dispatch (forward only): dispatch only ranks the slots and the
+    gate/up GEMM reads its rows straight from x by token id, so x_perm is
+    never written (moe_grouped_gemm_swiglu_gather)."""
 
     def __init__(self, T: int, H: int, I: int, E: int, k: int, ep_size: int = 1, *,
-                 training: bool = True, device: str | torch.device = "cuda"):
+                 training: bool = True, fused_dispatch: bool = False,
+                 device: str | torch.device = "cuda"):
+        if fused_dispatch and training:
+            raise ValueError("fused_dispatch keeps no x_perm, which the backward pass needs")
         self.T, self.H, self.I, self.E, self.k, self.ep_size = T, H, I, E, k, ep_size
         self.R = R = T * k
         self.training = training
+        self.fused_dispatch = fused_dispatch
+        self._x = None
         dev = torch.device(device)
         i32, f32, bf = torch.int32, torch.float32, torch.bfloat16
         e = lambda *s, dt: torch.empty(*s, dtype=dt, device=dev)  # noqa: E731
@@ -39,7 +49,7 @@ class MoELayer:
         self.rank_offsets = e(ep_size + 1, dt=i32)
         self.ws_route = _ws(moe_route_topk_workspace_size(T, H, E), dev)
         self.ws_dispatch = _ws(moe_dispatch_workspace_size(T, E, k), dev)
-        self.x_perm = e(R, H, dt=bf)
+        self.x_perm = None if fused_dispatch else e(R, H, dt=bf)
         self.row_of_slot = e(T, k, dt=i32)
         self.token_of_row = e(R, dt=i32)
         self.h = e(R, I, dt=bf)
@@ -67,12 +77,18 @@ class MoELayer:
                        stream)
 
     def dispatch(self, x, stream=None):
+        self._x = x  # the fused gate/up GEMM reads the rows from here
         moe_dispatch(x, self.topk_idx, self.offsets, self.T, self.H, self.E, self.k, self.x_perm,
                      self.row_of_slot, self.token_of_row, self.ws_dispatch, stream)
 
     def experts(self, Wg, Wu, Wd, stream=None):
-        moe_grouped_gemm_swiglu(self.x_perm, Wg, Wu, self.E, self.offsets, None, self.R, self.H,
-                                self.I, self.E, self.h, self.gu, None, stream)
+        if self.fused_dispatch:
+            moe_grouped_gemm_swiglu_gather(self._x, self.token_of_row, self.T, Wg, Wu, self.E,
+                                           self.offsets, None, self.R, self.H, self.I, self.E, self.h,
+                                           None, stream)
+        else:
+            moe_grouped_gemm_swiglu(self.x_perm, Wg, Wu, self.E, self.offsets, None, self.R, self.H,
+                                    self.I, self.E, self.h, self.gu, None, stream)
         moe_grouped_gemm_down(self.h, Wd, self.E, self.offsets, None, self.R, self.H, self.I,
                               self.E, self.y_perm, None, stream)
 

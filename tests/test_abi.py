@@ -76,6 +76,12 @@ def test_grouped_gemm_rejects_bad_shapes(L):
                                        None) == INVALID
     assert L.moe_grouped_gemm_swiglu_bwd(P, P, P, P, 8, P, None, 64, 128, 96, 8, P, P, P, 0, None, 0,
                                          None) == SHAPE
+    # the gathering gate/up GEMM: needs x and token ids when there is work
+    assert L.moe_grouped_gemm_swiglu_gather(None, None, 16, P, P, 8, P, None, 64, 128, 64, 8, P, None,
+                                            None) == INVALID
+    assert L.moe_grouped_gemm_swiglu_gather(P, P, 16, P, P, 8, P, None, 64, 100, 64, 8, P, None, None) == SHAPE
+    assert L.moe_grouped_gemm_swiglu_gather(P + 8, P, 16, P, P, 8, P, None, 64, 128, 64, 8, P, None,
+                                            None) == ALIGN
     # the backward GEMMs need 256 bytes of 128-byte aligned workspace per segment
     assert L.moe_grouped_gemm_bwd_workspace_size(8) == 8 * 256
     assert L.moe_grouped_gemm_bwd_workspace_size(0) == 0
