@@ -19,14 +19,20 @@
 //   DW             dW[g] = sum over group g's rows of A^T B (fp32) A, B MN-major
 //   DENSE_ADD      out = bf16(A B^T + add)  (router backward)     A, B K-major
 //
-// CTA layout (192 threads, one CTA per SM, persistent over tiles):
+// CTA layout (one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer (one lane issues)
 //   warp 1      TMEM allocator + MMA issuer (one lane issues)
-//   warps 2..5  epilogue: TMEM -> registers -> global (warp w reads TMEM
-//               lanes 32*(w%4)..+31, i.e. accumulator rows)
+//   warps 2..   epilogue: TMEM -> registers -> global (warp w reads TMEM
+//               lanes 32*(w%4)..+31, i.e. accumulator rows); four warps, or
+//               eight (two per lane quadrant, half the columns each) for the
+//               weight-gradient and SwiGLU-backward kinds
+//   last 4      GATE_UP_FWD only: with A rows gathered from x by token id,
+//               they and warp 0 copy the rows with cp.async
 // Tile: 128 rows x BN columns (BN <= 256), k-block 64 (one 128-byte swizzle
-// row of bf16), 4-stage shared-memory ring, two 256-column accumulators in
-// TMEM so the epilogue of tile i overlaps the MMAs of tile i+1.
+// row of bf16), 4-stage shared-memory ring (3 for the router dX kind, whose
+// epilogue stages its addend), two 256-column accumulators in TMEM so the
+// epilogue of tile i overlaps the MMAs of tile i+1.  GATE_UP_BWD_DX runs as
+// cluster pairs (tcgen05 cta_group::2, 256-row tiles).
 //
 // Every wait on an mbarrier is bounded (globaltimer): on timeout the CTA
 // records MOE_STATUS_TIMEOUT, all roles leave their loops, outstanding MMAs
