@@ -527,7 +527,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
         }
       }
     }
-  } else if (warp >= 2 + C::EPW) {
+  } else if (C::GW > 0 && warp >= 2 + C::EPW) {
     // ======================= row-gather helper warps ========================
     if (KIND == GATE_UP_FWD && p.gather_rows != nullptr) gather_loop(warp - (1 + C::EPW));
   } else {
