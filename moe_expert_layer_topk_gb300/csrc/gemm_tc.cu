@@ -64,7 +64,10 @@ struct Params {
   const int32_t* seg_expert;
   int num_groups;    // experts (B row groups) / DW output groups
   int b_group_rows;  // rows of the 2-D view of B per expert
-  int split_m;       // DW: rows m < split_m -> out0, else out1 (0: all out0)
+  union {
+    int split_m;       // DW: rows m < split_m -> out0, else out1 (0: all out0)
+    int gather_limit;  // GATE_UP_FWD with gathered rows: tokens in x
+  };
   int ldo;           // leading dimension of out0/out1 (elements)
   int I;             // intermediate size (gu / dgu layouts)
   uint32_t idesc;
@@ -72,9 +75,10 @@ struct Params {
   void* out0;
   void* out1;
   const void* aux;
-  const int32_t* gather_rows;   // GATE_UP_FWD: A row r is x[gather_rows[r]] (token_of_row), else null
-  int gather_limit;             // tokens in x
-  const CUtensorMap* seg_maps;  // DW: per segment s, the A map (2s) and the B map (2s+1)
+  union {
+    const CUtensorMap* seg_maps;  // DW: per segment s, the A map (2s) and the B map (2s+1)
+    const int32_t* gather_rows;   // GATE_UP_FWD: A row r is x[gather_rows[r]] (token_of_row), else null
+  };
   int* status;
 };
 
