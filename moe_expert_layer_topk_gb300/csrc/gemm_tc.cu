@@ -11,8 +11,9 @@
 // [E,I,H], down [E,H,I]).  fp32 weight gradients: "TorchTitan FSDP2 完全指南",
 // mixed-precision section.
 //
-// One kernel template serves six GEMM shapes (`Kind`):
+// One kernel template serves seven GEMM shapes (`Kind`):
 //   GATE_UP_FWD    h = silu(A Wg^T) * (A Wu^T)  (+ save g, u)     A, B K-major
+//   GATE_UP_GATHER the same with A row r = x[token_of_row[r]]
 //   DOWN_FWD       y = A Wd^T                                     A, B K-major
 //   DOWN_BWD_DX    dh = A Wd; SwiGLU backward in the epilogue     B MN-major
 //   GATE_UP_BWD_DX dx = dg Wg + du Wu (K = 2I, two B tensors)      B MN-major
@@ -26,8 +27,8 @@
 //               lanes 32*(w%4)..+31, i.e. accumulator rows); four warps, or
 //               eight (two per lane quadrant, half the columns each) for the
 //               weight-gradient and SwiGLU-backward kinds
-//   last 4      GATE_UP_FWD only: with A rows gathered from x by token id,
-//               they and warp 0 copy the rows with cp.async
+//   last 4      GATE_UP_GATHER only: they and warp 0 copy the A rows from x
+//               by token id with cp.async
 // Tile: 128 rows x BN columns (BN <= 256), k-block 64 (one 128-byte swizzle
 // row of bf16), 4-stage shared-memory ring (3 for the router dX kind, whose
 // epilogue stages its addend), two 256-column accumulators in TMEM so the
@@ -49,14 +50,25 @@ constexpr int B_BYTES_MAX = 256 * BK * 2;     // 32 KiB
 // DOWN_BWD_DX also loads the saved g, u boxes by TMA: 4 sets of (g, u) slots.
 constexpr int EP_GU_SETS = 4;
 
-enum Kind : int { GATE_UP_FWD = 0, DOWN_FWD = 1, DOWN_BWD_DX = 2, GATE_UP_BWD_DX = 3, DW = 4, DENSE_ADD = 5 };
+enum Kind : int {
+  GATE_UP_FWD = 0,
+  DOWN_FWD = 1,
+  DOWN_BWD_DX = 2,
+  GATE_UP_BWD_DX = 3,
+  DW = 4,
+  DENSE_ADD = 5,
+  GATE_UP_GATHER = 6
+};
+constexpr int kNumKinds = 7;
+// the gate/up forward kinds (same tiles and epilogue; they differ in how A arrives)
+__host__ __device__ constexpr bool is_gate_up(int k) { return k == GATE_UP_FWD || k == GATE_UP_GATHER; }
 
 struct Params {
   int M;             // row kinds: rows of A (R).  DW: output rows per group.
   int N;             // output columns
   int K;             // row kinds: reduction length.  DW: rows of the K-indexed operands.
   int BN;            // MMA N
-  int NH;            // GATE_UP_FWD: width of each of the g and u halves
+  int NH;            // gate/up forward: width of each of the g and u halves
   int n_tiles;
   int m_tiles;       // DW: m-tiles per group
   int num_seg;
@@ -66,7 +78,7 @@ struct Params {
   int b_group_rows;  // rows of the 2-D view of B per expert
   union {
     int split_m;       // DW: rows m < split_m -> out0, else out1 (0: all out0)
-    int gather_limit;  // GATE_UP_FWD with gathered rows: tokens in x
+    int gather_limit;  // GATE_UP_GATHER: tokens in x
   };
   int ldo;           // leading dimension of out0/out1 (elements)
   int I;             // intermediate size (gu / dgu layouts)
@@ -77,7 +89,7 @@ struct Params {
   const void* aux;
   union {
     const CUtensorMap* seg_maps;  // DW: per segment s, the A map (2s) and the B map (2s+1)
-    const int32_t* gather_rows;   // GATE_UP_FWD: A row r is x[gather_rows[r]] (token_of_row), else null
+    const int32_t* gather_rows;   // GATE_UP_GATHER: A row r is x[gather_rows[r]] (token_of_row)
   };
   int* status;
 };
@@ -137,8 +149,8 @@ struct Cfg {
   // SwiGLU-backward kind (heavy epilogue) run eight epilogue warps, two per
   // TMEM lane quadrant, each on half the columns (a one-box store ring each).
   static constexpr int EPW = (KIND == DW || KIND == DOWN_BWD_DX) ? 8 : 4;
-  // GATE_UP_FWD: four more warps share the row gather (when A rows come from x)
-  static constexpr int GW = KIND == GATE_UP_FWD ? 4 : 0;
+  // GATE_UP_GATHER: four more warps share the row gather
+  static constexpr int GW = KIND == GATE_UP_GATHER ? 4 : 0;
   static constexpr int NTHREADS = 64 + 32 * (EPW + GW);
   static constexpr int RING = (KIND == DW || KIND == DOWN_BWD_DX) ? 1 : EP_SLOTS;
   static constexpr int EP_WARP = gu_tma ? EP_BOX_BYTES * 2 * GU_SETS : EP_BOX_BYTES * RING;
@@ -148,6 +160,7 @@ struct Cfg {
 };
 // the configurations launched (cluster pairs only for GATE_UP_BWD_DX)
 static_assert(Cfg<GATE_UP_FWD, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
+                  Cfg<GATE_UP_GATHER, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<DOWN_FWD, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<DOWN_BWD_DX, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<GATE_UP_BWD_DX, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
@@ -178,7 +191,7 @@ __device__ __forceinline__ Tile decode_tile(int tile, const Params& p, const Ctl
     t.group = ctl->seg_exp[lo];
     t.m0 = ctl->seg_off[lo] + (gm - ctl->seg_tiles[lo]) * Cfg<KIND, CTAS>::TILE_M + BM * rank;
     t.row_end = ctl->seg_off[lo + 1];
-    t.n0 = nt * (KIND == GATE_UP_FWD ? p.NH : p.BN);
+    t.n0 = nt * (is_gate_up(KIND) ? p.NH : p.BN);
   } else {
     const int per = p.m_tiles * p.n_tiles;
     t.group = tile / per;
@@ -307,7 +320,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
     if (lane == 0) {
       for (int i = 0; i < STG; ++i) {
         // gather mode: lane 0's arming arrival plus one cp.async arrival per gathering lane
-        mbar_init(smem_u32(&ctl->full[i]), (KIND == GATE_UP_FWD && p.gather_rows) ? 1 + 32 * (1 + C::GW) : 1);
+        mbar_init(smem_u32(&ctl->full[i]), KIND == GATE_UP_GATHER ? 1 + 32 * (1 + C::GW) : 1);
         mbar_init(smem_u32(&ctl->empty[i]), 1);
       }
       for (int i = 0; i < 2; ++i) {
@@ -336,7 +349,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
   const int total = ctl->total_tiles;
   const uint32_t b_bytes = (uint32_t)p.BN * BK * 2 / CTAS;  // this CTA's share of a B stage
 
-  // GATE_UP_FWD with gathered A rows: warp 0 and the GW helper warps copy the
+  // GATE_UP_GATHER: warp 0 and the GW helper warps copy the
   // A tile's rows from x by token id with cp.async (per instruction a warp
   // copies four whole 128-byte rows, 8 lanes per row, into the
   // 128-byte-swizzled tile) and each lane arrives on the stage's barrier when
@@ -404,7 +417,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
 
   if (warp == 0) {
     // ============================ TMA producer ============================
-    if (KIND == GATE_UP_FWD && p.gather_rows != nullptr) {
+    if constexpr (KIND == GATE_UP_GATHER) {
       gather_loop(0);
     } else if (lane == 0) {
       int stage = 0;
@@ -437,7 +450,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
             tma_load_mn<CTAS>(sB, ma + 1, fb, row0, t.n0 / 64 + ck0);
           } else {
             tma_load<CTAS>(sA, &tmA, fb, row0, t.m0);
-            if constexpr (KIND == GATE_UP_FWD) {
+            if constexpr (is_gate_up(KIND)) {
               const int brow = t.group * p.b_group_rows + t.n0;
               if (CTAS == 1) {
                 tma_load<CTAS>(sB, &tmB0, fb, row0, brow);
@@ -495,7 +508,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
           // only the 16-deep MMA steps that hold valid rows are issued.
           const int nkk = KIND == DW ? (valid + 15) / 16 : BK / 16;
           tc_fence_after();
-          if (KIND == GATE_UP_FWD && p.gather_rows)  // A was written by cp.async (generic proxy)
+          if (KIND == GATE_UP_GATHER)  // A was written by cp.async (generic proxy)
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           if (lane == 0) {
             const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
@@ -533,7 +546,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
     }
   } else if (C::GW > 0 && warp >= 2 + C::EPW) {
     // ======================= row-gather helper warps ========================
-    if (KIND == GATE_UP_FWD && p.gather_rows != nullptr) gather_loop(warp - (1 + C::EPW));
+    if constexpr (KIND == GATE_UP_GATHER) gather_loop(warp - (1 + C::EPW));
   } else {
     // ============================ epilogue ================================
     // Each warp owns 32 accumulator rows of the tile (TMEM lanes
@@ -637,7 +650,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * ACC_COLS);
 
-      if constexpr (KIND == GATE_UP_FWD) {
+      if constexpr (is_gate_up(KIND)) {
         const size_t hp_pitch = (size_t)p.I * 2, gu_pitch = (size_t)p.I * 4;
         for (int c = 0; any && c < p.NH; c += 32) {
           uint32_t g[32], u[32];
@@ -874,7 +887,7 @@ bool use_pair(int bn) { return bn >= 128; }
 template <int KIND>
 bool pair_for(int bn) { return KIND == GATE_UP_BWD_DX && use_pair(bn); }
 
-bool g_attr[6][2][64] = {};
+bool g_attr[kNumKinds][2][64] = {};
 
 // Launches grouped_gemm_kernel<KIND, CTAS>: completes the CTAS-dependent
 // parameters, sizes the shared memory to the segment tables and the
@@ -1077,6 +1090,7 @@ int swiglu_impl(const void* a_src, const int32_t* gather_rows, int T, const void
   CUtensorMap th, tgu;
   if (int rc = make_out_map(&th, h, I, R, false)) return rc;
   if (int rc = make_out_map(&tgu, gu_save ? gu_save : h, gu_save ? 2 * I : I, R, false)) return rc;
+  if (gather_rows) return run<GATE_UP_GATHER>(false, p, ta, tg, tu, th, tgu, s, fn);
   return run<GATE_UP_FWD>(false, p, ta, tg, tu, th, tgu, s, fn);
 }
 
