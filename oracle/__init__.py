@@ -52,7 +52,7 @@ class _Ptr:
         return ctypes.c_void_p(a.ctypes.data)
 
 
-U16, I32, F32 = _Ptr(np.uint16), _Ptr(np.int32), _Ptr(np.float32)
+U8, U16, I32, F32 = _Ptr(np.uint8), _Ptr(np.uint16), _Ptr(np.int32), _Ptr(np.float32)
 C_INT = ctypes.c_int
 
 _SIGS = {
@@ -69,6 +69,12 @@ _SIGS = {
                                        F32, F32, F32, C_INT],
     "oracle_dispatch_bwd": [F32, I32, C_INT, C_INT, C_INT, F32],
     "oracle_route_topk_bwd": [F32, F32, I32, U16, F32, F32, C_INT, C_INT, C_INT, C_INT, F32, F32, C_INT],
+    "oracle_e4m3_decode": [U8, C_INT, F32],
+    "oracle_e4m3_encode": [F32, C_INT, U8],
+    "oracle_quantize_rows_e4m3": [F32, C_INT, C_INT, U8, F32],
+    "oracle_grouped_gemm_swiglu_fp8": [U8, F32, U8, F32, U8, F32, C_INT, I32, I32, C_INT, C_INT, C_INT,
+                                       C_INT, F32],
+    "oracle_grouped_gemm_down_fp8": [U8, F32, U8, F32, C_INT, I32, I32, C_INT, C_INT, C_INT, C_INT, F32],
 }
 
 def load(path) -> ctypes.CDLL:
@@ -252,3 +258,57 @@ def route_topk_bwd(d_w, topk_w, topk_idx, x, Wr, dx_acc, dWr=None):
     _ok(lib().oracle_route_topk_bwd(d_w, topk_w, topk_idx, x, Wr, dx_acc, T, H, E, k, out, dx,
                                     int(acc)), "oracle_route_topk_bwd")
     return out, dx
+
+
+# ------------------------------------------------------------ FP8 (e4m3)
+
+
+def e4m3_decode(q):
+    q = _c(q, np.uint8)
+    out = np.empty(q.shape, np.float32)
+    _ok(lib().oracle_e4m3_decode(q.reshape(-1), q.size, out.reshape(-1)), "oracle_e4m3_decode")
+    return out
+
+
+def e4m3_encode(v):
+    v = _c(v, np.float32)
+    q = np.empty(v.shape, np.uint8)
+    _ok(lib().oracle_e4m3_encode(v.reshape(-1), v.size, q.reshape(-1)), "oracle_e4m3_encode")
+    return q
+
+
+def quantize_rows_e4m3(a):
+    """Per-row e4m3 codes and fp32 scales of a 2-D fp32 array (or [..., cols])."""
+    a = _c(a, np.float32)
+    cols = a.shape[-1]
+    rows = a.size // cols
+    q = np.empty(a.shape, np.uint8)
+    s = np.empty(a.shape[:-1], np.float32)
+    _ok(lib().oracle_quantize_rows_e4m3(a.reshape(rows, cols), rows, cols, q.reshape(rows, cols),
+                                        s.reshape(rows)), "oracle_quantize_rows_e4m3")
+    return q, s
+
+
+def grouped_gemm_swiglu_fp8(aq, a_scale, Wgq, Wg_scale, Wuq, Wu_scale, seg_offsets, seg_expert=None):
+    aq = _c(aq, np.uint8); a_scale = _c(a_scale, np.float32)
+    Wgq = _c(Wgq, np.uint8); Wuq = _c(Wuq, np.uint8)
+    Wg_scale = _c(Wg_scale, np.float32); Wu_scale = _c(Wu_scale, np.float32)
+    so, se = _segs(None, seg_offsets, seg_expert)
+    R, H = aq.shape
+    E, I, _ = Wgq.shape
+    h = np.zeros((R, I), np.float32)
+    _ok(lib().oracle_grouped_gemm_swiglu_fp8(aq, a_scale, Wgq, Wg_scale, Wuq, Wu_scale, len(so) - 1, so,
+                                             se, R, H, I, E, h), "oracle_grouped_gemm_swiglu_fp8")
+    return h
+
+
+def grouped_gemm_down_fp8(hq, h_scale, Wdq, Wd_scale, seg_offsets, seg_expert=None):
+    hq = _c(hq, np.uint8); h_scale = _c(h_scale, np.float32)
+    Wdq = _c(Wdq, np.uint8); Wd_scale = _c(Wd_scale, np.float32)
+    so, se = _segs(None, seg_offsets, seg_expert)
+    R, I = hq.shape
+    E, H, _ = Wdq.shape
+    y = np.zeros((R, H), np.float32)
+    _ok(lib().oracle_grouped_gemm_down_fp8(hq, h_scale, Wdq, Wd_scale, len(so) - 1, so, se, R, H, I, E,
+                                           y), "oracle_grouped_gemm_down_fp8")
+    return y

@@ -44,6 +44,19 @@
  *      Wu, Wd; the routing indices and the bias get no gradient; weight
  *      gradients are fp32, overwritten unless `accumulate` is set (then the
  *      freshly computed sum is added to what the buffer holds).
+ *  R7. FP8 forward.  "TorchTitan FSDP2 完全指南", performance table, reports
+ *      the gain of FP8 matmuls in training but gives no recipe.  Reading:
+ *      e4m3 codes (1 sign bit, 4 exponent bits with bias 7, 3 mantissa
+ *      bits, no infinities, largest finite magnitude 448) with one fp32
+ *      scale per row of the operand as stored: a token row of x, a
+ *      permuted row of h, an output channel of one expert's weight (a row
+ *      of Wg/Wu/Wd seen as [E*out, in]).  A row a[0..n) gets
+ *      s = amax/448 (fp32 division; s = 1 for an all-zero row) and
+ *      q[j] = e4m3(a[j] / s) (fp32 division; round to nearest, ties to
+ *      even; magnitudes at or above 448 give 448; the sign is kept, also
+ *      on a zero).  The FP8 GEMMs compute
+ *      g[r,n] = s_a[r] * s_w[e,n] * sum_k dec(a[r,k]) * dec(w[e,n,k]),
+ *      the sum taken in double (every product of two e4m3 values is exact).
  */
 #include "moe_oracle.h"
 
@@ -445,5 +458,122 @@ int oracle_route_topk_bwd(const float* d_w, const float* topk_w, const int32_t* 
       dx[(size_t)t * H + c] = acc;
     }
   free(dl); free(sum);
+  return 0;
+}
+
+/* ------------------------------------------------------------ R7 FP8 e4m3 */
+
+/* Value of an e4m3 code: exponent field 0 is subnormal (m * 2^-9); fields
+ * 1..15 are (1 + m/8) * 2^(field-7); magnitude code 0x7F is NaN. */
+static double e4m3_value(uint8_t c) {
+  const int field = (c >> 3) & 15, m = c & 7;
+  double v;
+  if (field == 15 && m == 7) return NAN;
+  if (field == 0)
+    v = ldexp((double)m, -9);
+  else
+    v = ldexp(1.0 + m / 8.0, field - 7);
+  return (c & 0x80) ? -v : v;
+}
+
+/* Round-to-nearest-even of |v| onto the e4m3 grid, saturating at 448. */
+static uint8_t e4m3_code(float v) {
+  const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+  const double m = fabs((double)v);
+  if (m >= 448.0) return sign | 0x7E;
+  int field, q;
+  if (m < ldexp(1.0, -6)) {
+    /* subnormal quantum 2^-9; q = 8 lands on the smallest normal (field 1) */
+    q = (int)nearbyint(m / ldexp(1.0, -9));
+    return sign | (uint8_t)q;
+  }
+  int e2;
+  (void)frexp(m, &e2);  /* m = f * 2^e2, f in [0.5, 1): leading bit at 2^(e2-1) */
+  const int e = e2 - 1;
+  q = (int)nearbyint(m / ldexp(1.0, e - 3)); /* 8..16 quanta of 2^(e-3) */
+  if (q == 16) {
+    q = 8;
+    field = e + 1 + 7;
+  } else {
+    field = e + 7;
+  }
+  if (field > 15 || (field == 15 && q - 8 > 6)) return sign | 0x7E;
+  return sign | (uint8_t)((field << 3) | (q - 8));
+}
+
+int oracle_e4m3_decode(const uint8_t* q, int n, float* out) {
+  if (n < 0 || (n > 0 && (!q || !out))) return -1;
+  for (int i = 0; i < n; ++i) out[i] = (float)e4m3_value(q[i]);
+  return 0;
+}
+
+int oracle_e4m3_encode(const float* v, int n, uint8_t* q) {
+  if (n < 0 || (n > 0 && (!v || !q))) return -1;
+  for (int i = 0; i < n; ++i) q[i] = e4m3_code(v[i]);
+  return 0;
+}
+
+int oracle_quantize_rows_e4m3(const float* a, int rows, int cols, uint8_t* q, float* scale) {
+  if (rows < 0 || cols <= 0 || (rows > 0 && (!a || !q || !scale))) return -1;
+  for (int r = 0; r < rows; ++r) {
+    const float* row = a + (size_t)r * cols;
+    float amax = 0.0f;
+    for (int j = 0; j < cols; ++j) amax = fmaxf(amax, fabsf(row[j]));
+    const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+    scale[r] = s;
+    for (int j = 0; j < cols; ++j) q[(size_t)r * cols + j] = e4m3_code(row[j] / s);
+  }
+  return 0;
+}
+
+/* R7 with R4: h = silu(g) * u on e4m3 rows of x_perm and e4m3 weights. */
+int oracle_grouped_gemm_swiglu_fp8(const uint8_t* aq, const float* a_scale, const uint8_t* Wgq,
+                                   const float* Wg_scale, const uint8_t* Wuq, const float* Wu_scale,
+                                   int num_seg, const int32_t* seg_offsets,
+                                   const int32_t* seg_expert, int R, int H, int I, int E, float* h) {
+  if (H <= 0 || I <= 0 || E <= 0 || !aq || !a_scale || !Wgq || !Wg_scale || !Wuq || !Wu_scale || !h)
+    return -1;
+  if (check_segments(num_seg, seg_offsets, seg_expert, R, E)) return -1;
+  for (int s = 0; s < num_seg; ++s) {
+    int e = seg_expert_of(seg_expert, s);
+    for (int r = seg_offsets[s]; r < seg_offsets[s + 1]; ++r) {
+      const uint8_t* a = aq + (size_t)r * H;
+      for (int i = 0; i < I; ++i) {
+        const uint8_t* wg = Wgq + ((size_t)e * I + i) * H;
+        const uint8_t* wu = Wuq + ((size_t)e * I + i) * H;
+        double sg = 0.0, su = 0.0;
+        for (int c = 0; c < H; ++c) {
+          const double av = e4m3_value(a[c]);
+          sg += av * e4m3_value(wg[c]);
+          su += av * e4m3_value(wu[c]);
+        }
+        const double g = (double)a_scale[r] * Wg_scale[(size_t)e * I + i] * sg;
+        const double u = (double)a_scale[r] * Wu_scale[(size_t)e * I + i] * su;
+        h[(size_t)r * I + i] = (float)(g / (1.0 + exp(-g)) * u);
+      }
+    }
+  }
+  return 0;
+}
+
+/* R7 with R4: y_perm = h . Wd^T on e4m3 rows of h and e4m3 weights. */
+int oracle_grouped_gemm_down_fp8(const uint8_t* hq, const float* h_scale, const uint8_t* Wdq,
+                                 const float* Wd_scale, int num_seg, const int32_t* seg_offsets,
+                                 const int32_t* seg_expert, int R, int H, int I, int E,
+                                 float* y_perm) {
+  if (H <= 0 || I <= 0 || E <= 0 || !hq || !h_scale || !Wdq || !Wd_scale || !y_perm) return -1;
+  if (check_segments(num_seg, seg_offsets, seg_expert, R, E)) return -1;
+  for (int s = 0; s < num_seg; ++s) {
+    int e = seg_expert_of(seg_expert, s);
+    for (int r = seg_offsets[s]; r < seg_offsets[s + 1]; ++r) {
+      const uint8_t* a = hq + (size_t)r * I;
+      for (int n = 0; n < H; ++n) {
+        const uint8_t* w = Wdq + ((size_t)e * H + n) * I;
+        double acc = 0.0;
+        for (int i = 0; i < I; ++i) acc += e4m3_value(a[i]) * e4m3_value(w[i]);
+        y_perm[(size_t)r * H + n] = (float)((double)h_scale[r] * Wd_scale[(size_t)e * H + n] * acc);
+      }
+    }
+  }
   return 0;
 }

@@ -5,7 +5,8 @@
  * may load this library.  The product (the CUDA library and its Python
  * binding) never calls it and shares no code with it.
  *
- * Every function takes host pointers, runs single-threaded in fp32 and
+ * Every function takes host pointers, runs single-threaded in fp32 (the FP8
+ * GEMMs sum their exact e4m3 products in double) and
  * returns 0 on success, -1 on a bad argument, -2 when a host allocation
  * fails.  bf16 tensors are passed as uint16_t bit patterns and widened
  * exactly to fp32.  Activations that the CUDA path stores in bf16 between
@@ -70,6 +71,19 @@ int oracle_dispatch_bwd(const float* dx_perm, const int32_t* row_of_slot, int T,
 int oracle_route_topk_bwd(const float* d_w, const float* topk_w, const int32_t* topk_idx,
                           const uint16_t* x, const float* Wr, const float* dx_acc,
                           int T, int H, int E, int k, float* dWr, float* dx, int accumulate);
+
+/* e4m3 (R7): codes <-> values, per-row quantisation, FP8 grouped GEMMs. */
+int oracle_e4m3_decode(const uint8_t* q, int n, float* out);
+int oracle_e4m3_encode(const float* v, int n, uint8_t* q);
+int oracle_quantize_rows_e4m3(const float* a, int rows, int cols, uint8_t* q, float* scale);
+int oracle_grouped_gemm_swiglu_fp8(const uint8_t* aq, const float* a_scale, const uint8_t* Wgq,
+                                   const float* Wg_scale, const uint8_t* Wuq, const float* Wu_scale,
+                                   int num_seg, const int32_t* seg_offsets,
+                                   const int32_t* seg_expert, int R, int H, int I, int E, float* h);
+int oracle_grouped_gemm_down_fp8(const uint8_t* hq, const float* h_scale, const uint8_t* Wdq,
+                                 const float* Wd_scale, int num_seg, const int32_t* seg_offsets,
+                                 const int32_t* seg_expert, int R, int H, int I, int E,
+                                 float* y_perm);
 
 #ifdef __cplusplus
 }

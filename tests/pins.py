@@ -394,7 +394,145 @@ def pin_accumulate_and_empty():
     assert np.array_equal(accr, prev_r + b["dWr"])
 
 
+# ------------------------------------------------------------ FP8 (e4m3)
+#
+# Format: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits, no
+# infinities, 0x7F/0xFF NaN, largest finite 448 (torch.float8_e4m3fn is the
+# same format).  Scaling reading: one fp32 scale per stored row (token row,
+# permuted row, expert output channel), s = amax / 448.
+
+
+def _torch_e4m3_codes(v):
+    return torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _finite_codes():
+    c = np.arange(256, dtype=np.uint8)
+    return c[(c & 0x7F) != 0x7F]
+
+
+def pin_e4m3_decode():
+    """Every finite code decodes as torch's float8_e4m3fn does; closed forms."""
+    c = _finite_codes()
+    dec = oracle.e4m3_decode(c)
+    ref = torch.from_numpy(c.copy()).view(torch.float8_e4m3fn).float().numpy()
+    assert np.array_equal(dec.view(np.uint32), ref.view(np.uint32))
+    closed = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0, 0x3C: 1.5,
+              0x7E: 448.0, 0xB8: -1.0, 0xFE: -448.0}
+    got = oracle.e4m3_decode(np.array(list(closed), np.uint8))
+    assert np.array_equal(got, np.array(list(closed.values()), np.float32))
+
+
+def pin_e4m3_encode():
+    """Round to nearest even: every midpoint between neighbouring codes, one
+    fp32 ulp either side of it, and seeded values over eight decades give
+    torch's conversion; magnitudes at or above 448 saturate to 448."""
+    c = _finite_codes()
+    pos = np.sort(oracle.e4m3_decode(c[c < 0x80]).astype(np.float64))
+    mids = ((pos[1:] + pos[:-1]) / 2).astype(np.float32)
+    probes = np.concatenate([mids, np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(np.inf)),
+                             pos.astype(np.float32)])
+    rng = np.random.default_rng(60)
+    seeded = np.concatenate([(rng.standard_normal(20000) * sc).astype(np.float32)
+                             for sc in (1e-4, 1e-3, 1e-2, 0.1, 1.0, 10.0, 100.0)])
+    v = np.concatenate([probes, -probes, seeded, np.array([0.0, -0.0], np.float32)])
+    v = v[np.abs(v) < 464]
+    assert np.array_equal(oracle.e4m3_encode(v), _torch_e4m3_codes(v))
+    big = np.array([448, 463.9, 464, 500, 1e30, -448, -1e10], np.float32)
+    assert np.array_equal(oracle.e4m3_encode(big), np.array([0x7E] * 5 + [0xFE] * 2, np.uint8))
+
+
+def pin_quantize_rows():
+    """Per-row scaling: the largest magnitude of each row maps to code 448,
+    dequantised values are within half a quantum (2^-4 relative, 2^-10 * s
+    absolute in the subnormal range), signs are kept, an all-zero row gets
+    scale 1 and zero codes."""
+    rng = np.random.default_rng(61)
+    a = (rng.standard_normal((40, 96)) * np.exp(rng.uniform(-8, 8, (40, 1)))).astype(np.float32)
+    a[3] = 0.0
+    a[5, :] = 0.0
+    a[5, 17] = -3.5
+    a[7, ::2] *= 1e-6                     # many values in the subnormal range of that row
+    q, s = oracle.quantize_rows_e4m3(a)
+    dec = oracle.e4m3_decode(q).astype(np.float64)
+    for r in range(a.shape[0]):
+        amax = np.abs(a[r]).max()
+        if amax == 0:
+            assert s[r] == 1.0 and not (q[r] & 0x7F).any()
+            continue
+        assert np.abs(dec[r]).max() == 448.0
+        assert abs(s[r] * 448.0 - amax) <= 2 * U * amax
+        err = np.abs(dec[r] * s[r] - a[r].astype(np.float64))
+        assert np.all(err <= np.maximum(2.0 ** -4 * np.abs(a[r]), 2.0 ** -10 * s[r]) * (1 + 4 * U) + 1e-45)
+        nz = dec[r] != 0
+        assert np.array_equal(np.sign(dec[r][nz]), np.sign(a[r][nz]))
+    assert np.abs(dec[5]).max() == 448.0 and q[5, 17] == 0xFE
+
+
+def _int_codes(rng, shape, lo=-8, hi=8):
+    """e4m3 codes of random small integers (exactly representable)."""
+    v = rng.integers(lo, hi + 1, shape).astype(np.float32)
+    return oracle.e4m3_encode(v), v.astype(np.int64)
+
+
+def pin_fp8_gemms_integer_case():
+    """Integer-valued codes and power-of-two scales: g, u and y_perm are
+    exact (integer matmul in numpy, per segment, with empty and reordered
+    segments); h = silu(g) * u against torch fp64."""
+    rng = np.random.default_rng(62)
+    R, H, I, E = 70, 64, 32, 4
+    aq, av = _int_codes(rng, (R, H))
+    Wgq, wg = _int_codes(rng, (E, I, H)); Wuq, wu = _int_codes(rng, (E, I, H))
+    Wdq, wd = _int_codes(rng, (E, H, I))
+    sa = (2.0 ** rng.integers(-6, 4, R)).astype(np.float32)
+    sg = (2.0 ** rng.integers(-6, 4, (E, I))).astype(np.float32)
+    su = (2.0 ** rng.integers(-6, 4, (E, I))).astype(np.float32)
+    sd = (2.0 ** rng.integers(-6, 4, (E, H))).astype(np.float32)
+    so = np.array([0, 20, 20, 45, 70], np.int32); se = np.array([2, 0, 3, 1], np.int32)
+    h = oracle.grouped_gemm_swiglu_fp8(aq, sa, Wgq, sg, Wuq, su, so, se)
+    hq, _ = _int_codes(rng, (R, I))
+    hs = (2.0 ** rng.integers(-6, 4, R)).astype(np.float32)
+    y = oracle.grouped_gemm_down_fp8(hq, hs, Wdq, sd, so, se)
+    for q in range(4):
+        a, b, e = so[q], so[q + 1], se[q]
+        if a == b:
+            continue
+        g = (av[a:b] @ wg[e].T).astype(np.float64) * sa[a:b, None] * sg[e][None, :]
+        u = (av[a:b] @ wu[e].T).astype(np.float64) * sa[a:b, None] * su[e][None, :]
+        ref_h = (F.silu(torch.from_numpy(g)) * torch.from_numpy(u)).numpy()
+        assert np.allclose(h[a:b], ref_h, rtol=1e-6, atol=1e-30)
+        ref_y = (_decode_int(hq[a:b]) @ wd[e].T).astype(np.float64) * hs[a:b, None] * sd[e][None, :]
+        assert np.array_equal(y[a:b], ref_y.astype(np.float32))
+
+
+def _decode_int(q):
+    return oracle.e4m3_decode(q).astype(np.int64)
+
+
+def pin_fp8_reduces_to_bf16_oracle():
+    """Scale 1 and e4m3-representable inputs (every e4m3 value is a bf16
+    value): the FP8 GEMMs equal the pinned bf16 oracle GEMMs up to the
+    latter's fp32 summation error."""
+    rng = np.random.default_rng(63)
+    R, H, I, E = 48, 128, 64, 3
+    codes = lambda shape: oracle.e4m3_encode(rng.standard_normal(shape).astype(np.float32))
+    aq, Wgq, Wuq, Wdq = codes((R, H)), codes((E, I, H)), codes((E, I, H)), codes((E, H, I))
+    as_bf16 = lambda q: (oracle.e4m3_decode(q).view(np.uint32) >> 16).astype(np.uint16)
+    so = np.array([0, 10, 30, 48], np.int32)
+    one = lambda n: np.ones(n, np.float32)
+    h8 = oracle.grouped_gemm_swiglu_fp8(aq, one(R), Wgq, one((E, I)), Wuq, one((E, I)), so)
+    h16 = oracle.grouped_gemm_swiglu(oracle.e4m3_decode(aq), as_bf16(Wgq), as_bf16(Wuq), so)
+    assert rel_l2(h8, h16) < 1e-6
+    hq = codes((R, I))
+    y8 = oracle.grouped_gemm_down_fp8(hq, one(R), Wdq, one((E, H)), so)
+    y16 = oracle.grouped_gemm_down(oracle.e4m3_decode(hq), as_bf16(Wdq), so)
+    assert rel_l2(y8, y16) < 1e-6
+
+
+FP8_PINS = [pin_e4m3_decode, pin_e4m3_encode, pin_quantize_rows, pin_fp8_gemms_integer_case,
+            pin_fp8_reduces_to_bf16_oracle]
+
 ALL_PINS = [pin_logit_block_order, pin_logits_error_bound, pin_topk_bruteforce, pin_topk_ties,
             pin_weights_closed_form, pin_counts_offsets, pin_permutation, pin_forward_dense_fp64,
             pin_dense_mlp_special_case, pin_identity_experts, pin_segments_dense,
-            pin_backward_autograd, pin_accumulate_and_empty]
+            pin_backward_autograd, pin_accumulate_and_empty] + FP8_PINS
