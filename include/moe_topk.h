@@ -206,6 +206,52 @@ int moe_grouped_gemm_down(const void* h, const void* Wd, int num_seg, const int3
                           const int32_t* seg_expert, int R, int H, int I, int E, void* y_perm,
                           void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------------
+ * FP8 (e4m3) forward GEMMs -- the second "next" step after the path.
+ *
+ * "TorchTitan FSDP2 完全指南", performance table: FP8 matmuls raise training
+ * throughput; the page gives no recipe.  Reading taken here: one fp32 scale
+ * per stored row (a token row of x, a permuted row of h, an output channel
+ * of one expert's weight, i.e. a row of Wg/Wu/Wd seen as [E*out, in]),
+ *   s = amax(|row|) / 448   (s = 1 for an all-zero row)
+ *   q = e4m3(row / s)       (IEEE fp32 division, round to nearest even,
+ *                            saturated to +-448; e4m3 = 1 sign, 4 exponent
+ *                            bits with bias 7, 3 mantissa bits, no infinity)
+ * and the GEMMs multiply e4m3 codes on the tensor cores with fp32
+ * accumulation, the two row scales applied to the accumulator:
+ *   g[r,n] = s_a[r] * s_w[e,n] * sum_k dec(a[r,k]) * dec(w[e,n,k]).
+ * H and I must be multiples of 128.  Forward only (no g,u save).
+ * ---------------------------------------------------------------------- */
+
+/* Per-row e4m3 quantisation of a bf16 matrix a [rows, cols] (cols % 8 == 0):
+ * q uint8 [rows, cols] (8-byte aligned), scale fp32 [rows].  Bit-exact:
+ * codes and scales are a pure function of the input bits. */
+int moe_quantize_rows_e4m3(const void* a, int rows, int cols, void* q, float* scale, void* stream);
+
+/* A4 on e4m3 operands: h[r] = silu(g) * u -> bf16 [R,I], with g and u the
+ * scaled e4m3 GEMMs above.  Wg, Wu: uint8 [E,I,H] codes with fp32 scales
+ * Wg_scale, Wu_scale [E*I] (16-byte aligned).
+ *   token_of_row == NULL: a is x_perm's codes uint8 [R,H], a_scale fp32 [R].
+ *   token_of_row != NULL: a is x's codes uint8 [T,H] and a_scale fp32 [T]
+ *     (one scale per token); row r reads token token_of_row[r] (the fused
+ *     dispatch of moe_grouped_gemm_swiglu_gather; a token id outside [0,T)
+ *     reads token 0 and sets MOE_STATUS_BAD_INDEX).
+ * No workspace. */
+int moe_grouped_gemm_swiglu_fp8(const void* a, const float* a_scale, const int32_t* token_of_row,
+                                int T, const void* Wg, const float* Wg_scale, const void* Wu,
+                                const float* Wu_scale, int num_seg, const int32_t* seg_offsets,
+                                const int32_t* seg_expert, int R, int H, int I, int E, void* h,
+                                void* stream);
+
+/* A5 on e4m3 operands: y_perm[r,n] = s_h[r] * s_w[e,n] * sum_i dec(h[r,i]) * dec(Wd[e,n,i])
+ * -> bf16 [R,H].  h: uint8 [R,I] codes with h_scale fp32 [R] (from
+ * moe_quantize_rows_e4m3 of the bf16 h); Wd: uint8 [E,H,I] with Wd_scale
+ * fp32 [E*H] (16-byte aligned).  No workspace. */
+int moe_grouped_gemm_down_fp8(const void* h, const float* h_scale, const void* Wd,
+                              const float* Wd_scale, int num_seg, const int32_t* seg_offsets,
+                              const int32_t* seg_expert, int R, int H, int I, int E, void* y_perm,
+                              void* stream);
+
 /* A6  combine (unpermute): y[t] = sum_{j=0..k-1} topk_w[t,j] * y_perm[row_of_slot[t,j]],
  * accumulated in fp32 in increasing j, rounded once to bf16.
  * y_perm bf16 [R,H]; topk_w fp32 [T,k]; row_of_slot int32 [T,k]; y bf16 [T,H]. */

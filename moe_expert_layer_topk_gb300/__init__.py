@@ -20,6 +20,7 @@ from . import build as _build_mod
 __all__ = ["lib", "MoEError", "LIB_PATH", "ENTRY_POINTS",
            "moe_route_topk", "moe_dispatch", "moe_dispatch_no_alloc", "moe_grouped_gemm_swiglu",
            "moe_grouped_gemm_swiglu_gather", "moe_grouped_gemm_down",
+           "moe_quantize_rows_e4m3", "moe_grouped_gemm_swiglu_fp8", "moe_grouped_gemm_down_fp8",
            "moe_combine", "moe_combine_bwd", "moe_grouped_gemm_down_bwd",
            "moe_grouped_gemm_swiglu_bwd", "moe_dispatch_bwd", "moe_route_topk_bwd",
            "moe_route_topk_workspace_size", "moe_dispatch_workspace_size",
@@ -44,6 +45,9 @@ ENTRY_POINTS = {
     "moe_grouped_gemm_swiglu": ([_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P], _I),
     "moe_grouped_gemm_swiglu_gather": ([_P, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_grouped_gemm_down": ([_P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _P], _I),
+    "moe_quantize_rows_e4m3": ([_P, _I, _I, _P, _P, _P], _I),
+    "moe_grouped_gemm_swiglu_fp8": ([_P, _P, _P, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P], _I),
+    "moe_grouped_gemm_down_fp8": ([_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P], _I),
     "moe_combine": ([_P, _P, _P, _I, _I, _I, _P, _P], _I),
     "moe_combine_bwd": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _P], _I),
     "moe_grouped_gemm_bwd_workspace_size": ([_I], _Z),
@@ -174,6 +178,23 @@ def moe_grouped_gemm_down(h, Wd, num_seg, seg_offsets, seg_expert, R, H, I, E, y
                           stream=None):
     _call("moe_grouped_gemm_down", _ptr(h), _ptr(Wd), num_seg, _ptr(seg_offsets),
           _ptr(seg_expert), R, H, I, E, _ptr(y_perm), _ptr(ws), _nbytes(ws), _stream(stream))
+
+
+def moe_quantize_rows_e4m3(a, rows, cols, q, scale, stream=None):
+    _call("moe_quantize_rows_e4m3", _ptr(a), rows, cols, _ptr(q), _ptr(scale), _stream(stream))
+
+
+def moe_grouped_gemm_swiglu_fp8(a, a_scale, token_of_row, T, Wg, Wg_scale, Wu, Wu_scale, num_seg,
+                                seg_offsets, seg_expert, R, H, I, E, h, stream=None):
+    _call("moe_grouped_gemm_swiglu_fp8", _ptr(a), _ptr(a_scale), _ptr(token_of_row), T, _ptr(Wg),
+          _ptr(Wg_scale), _ptr(Wu), _ptr(Wu_scale), num_seg, _ptr(seg_offsets), _ptr(seg_expert), R, H,
+          I, E, _ptr(h), _stream(stream))
+
+
+def moe_grouped_gemm_down_fp8(h, h_scale, Wd, Wd_scale, num_seg, seg_offsets, seg_expert, R, H, I, E,
+                              y_perm, stream=None):
+    _call("moe_grouped_gemm_down_fp8", _ptr(h), _ptr(h_scale), _ptr(Wd), _ptr(Wd_scale), num_seg,
+          _ptr(seg_offsets), _ptr(seg_expert), R, H, I, E, _ptr(y_perm), _stream(stream))
 
 
 def moe_combine(y_perm, topk_w, row_of_slot, T, H, k, y, stream=None):

@@ -72,7 +72,7 @@ int sm_count() {
 
 extern "C" {
 
-int moe_abi_version(void) { return 101; }
+int moe_abi_version(void) { return 102; }
 
 const char* moe_last_error_string(void) { return g_err; }
 

@@ -11,9 +11,13 @@
 // [E,I,H], down [E,H,I]).  fp32 weight gradients: "TorchTitan FSDP2 完全指南",
 // mixed-precision section.
 //
-// One kernel template serves seven GEMM shapes (`Kind`):
+// One kernel template serves ten GEMM shapes (`Kind`):
 //   GATE_UP_FWD    h = silu(A Wg^T) * (A Wu^T)  (+ save g, u)     A, B K-major
 //   GATE_UP_GATHER the same with A row r = x[token_of_row[r]]
+//   GATE_UP_FP8, GATE_UP_GATHER_FP8, DOWN_FP8: the forward kinds on e4m3
+//                  operands (tcgen05 kind::f8f6f4, fp32 accumulation) with
+//                  one fp32 scale per A row and per B row (output channel),
+//                  applied to the accumulator in the epilogue
 //   DOWN_FWD       y = A Wd^T                                     A, B K-major
 //   DOWN_BWD_DX    dh = A Wd; SwiGLU backward in the epilogue     B MN-major
 //   GATE_UP_BWD_DX dx = dg Wg + du Wu (K = 2I, two B tensors)      B MN-major
@@ -27,10 +31,10 @@
 //               lanes 32*(w%4)..+31, i.e. accumulator rows); four warps, or
 //               eight (two per lane quadrant, half the columns each) for the
 //               weight-gradient and SwiGLU-backward kinds
-//   last 4      GATE_UP_GATHER only: they and warp 0 copy the A rows from x
-//               by token id with cp.async
-// Tile: 128 rows x BN columns (BN <= 256), k-block 64 (one 128-byte swizzle
-// row of bf16), 4-stage shared-memory ring (3 for the router dX kind, whose
+//   last 4      row-gathering kinds only: they and warp 0 copy the A rows
+//               from x by token id with cp.async
+// Tile: 128 rows x BN columns (BN <= 256), k-block of one 128-byte swizzle
+// row (64 bf16 or 128 e4m3 elements), 4-stage shared-memory ring (3 for the router dX kind, whose
 // epilogue stages its addend), two 256-column accumulators in TMEM so the
 // epilogue of tile i overlaps the MMAs of tile i+1.  GATE_UP_BWD_DX runs as
 // cluster pairs (tcgen05 cta_group::2, 256-row tiles).
@@ -57,11 +61,24 @@ enum Kind : int {
   GATE_UP_BWD_DX = 3,
   DW = 4,
   DENSE_ADD = 5,
-  GATE_UP_GATHER = 6
+  GATE_UP_GATHER = 6,
+  GATE_UP_FP8 = 7,
+  GATE_UP_GATHER_FP8 = 8,
+  DOWN_FP8 = 9
 };
-constexpr int kNumKinds = 7;
-// the gate/up forward kinds (same tiles and epilogue; they differ in how A arrives)
-__host__ __device__ constexpr bool is_gate_up(int k) { return k == GATE_UP_FWD || k == GATE_UP_GATHER; }
+constexpr int kNumKinds = 10;
+__host__ __device__ constexpr bool is_fp8(int k) {
+  return k == GATE_UP_FP8 || k == GATE_UP_GATHER_FP8 || k == DOWN_FP8;
+}
+// the gate/up forward kinds (same tiles and epilogue; they differ in how A
+// arrives and in the operand type)
+__host__ __device__ constexpr bool is_gate_up(int k) {
+  return k == GATE_UP_FWD || k == GATE_UP_GATHER || k == GATE_UP_FP8 || k == GATE_UP_GATHER_FP8;
+}
+__host__ __device__ constexpr bool is_gather(int k) { return k == GATE_UP_GATHER || k == GATE_UP_GATHER_FP8; }
+__host__ __device__ constexpr bool is_down_fwd(int k) { return k == DOWN_FWD || k == DOWN_FP8; }
+// reduction elements per k-block: one 128-byte row of the operand type
+__host__ __device__ constexpr int kblock_elems(int k) { return is_fp8(k) ? 128 : BK; }
 
 struct Params {
   int M;             // row kinds: rows of A (R).  DW: output rows per group.
@@ -76,10 +93,7 @@ struct Params {
   const int32_t* seg_expert;
   int num_groups;    // experts (B row groups) / DW output groups
   int b_group_rows;  // rows of the 2-D view of B per expert
-  union {
-    int split_m;       // DW: rows m < split_m -> out0, else out1 (0: all out0)
-    int gather_limit;  // GATE_UP_GATHER: tokens in x
-  };
+  int split_m;       // DW: rows m < split_m -> out0, else out1 (0: all out0)
   int ldo;           // leading dimension of out0/out1 (elements)
   int I;             // intermediate size (gu / dgu layouts)
   uint32_t idesc;
@@ -89,7 +103,13 @@ struct Params {
   const void* aux;
   union {
     const CUtensorMap* seg_maps;  // DW: per segment s, the A map (2s) and the B map (2s+1)
-    const int32_t* gather_rows;   // GATE_UP_GATHER: A row r is x[gather_rows[r]] (token_of_row)
+    struct {
+      const int32_t* gather_rows;  // row-gathering kinds: A row r is x[gather_rows[r]] (token_of_row)
+      const float* a_scale;        // FP8 kinds: per A row (gathering: per token of x)
+      const float* b_scale0;       // FP8 kinds: per row of B0 ([E * N] output channels)
+      const float* b_scale1;       // GATE_UP FP8 kinds: per row of B1
+      int gather_limit;            // row-gathering kinds: tokens in x
+    };
   };
   int* status;
 };
@@ -149,8 +169,8 @@ struct Cfg {
   // SwiGLU-backward kind (heavy epilogue) run eight epilogue warps, two per
   // TMEM lane quadrant, each on half the columns (a one-box store ring each).
   static constexpr int EPW = (KIND == DW || KIND == DOWN_BWD_DX) ? 8 : 4;
-  // GATE_UP_GATHER: four more warps share the row gather
-  static constexpr int GW = KIND == GATE_UP_GATHER ? 4 : 0;
+  // row-gathering kinds: four more warps share the row gather
+  static constexpr int GW = is_gather(KIND) ? 4 : 0;
   static constexpr int NTHREADS = 64 + 32 * (EPW + GW);
   static constexpr int RING = (KIND == DW || KIND == DOWN_BWD_DX) ? 1 : EP_SLOTS;
   static constexpr int EP_WARP = gu_tma ? EP_BOX_BYTES * 2 * GU_SETS : EP_BOX_BYTES * RING;
@@ -161,6 +181,9 @@ struct Cfg {
 // the configurations launched (cluster pairs only for GATE_UP_BWD_DX)
 static_assert(Cfg<GATE_UP_FWD, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<GATE_UP_GATHER, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
+                  Cfg<GATE_UP_FP8, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
+                  Cfg<GATE_UP_GATHER_FP8, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
+                  Cfg<DOWN_FP8, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<DOWN_FWD, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<DOWN_BWD_DX, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<GATE_UP_BWD_DX, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
@@ -211,9 +234,10 @@ __device__ __forceinline__ Tile decode_tile(int tile, const Params& p, const Ctl
 template <int KIND, class F>
 __device__ __forceinline__ void for_each_kblock(const Tile& t, const Params& p, const Ctl* ctl, F&& f) {
   if constexpr (Traits<KIND>::rows) {
-    const int nkb = p.K / BK;
+    constexpr int KB = kblock_elems(KIND);
+    const int nkb = p.K / KB;
     for (int kb = 0; kb < nkb; ++kb)
-      if (!f(kb * BK, BK, t.seg)) return;
+      if (!f(kb * KB, KB, t.seg)) return;
   } else if (p.seg_expert == nullptr) {
     // identity table: group g owns exactly segment g
     const int len = ctl->seg_off[t.group + 1] - ctl->seg_off[t.group];
@@ -320,7 +344,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
     if (lane == 0) {
       for (int i = 0; i < STG; ++i) {
         // gather mode: lane 0's arming arrival plus one cp.async arrival per gathering lane
-        mbar_init(smem_u32(&ctl->full[i]), KIND == GATE_UP_GATHER ? 1 + 32 * (1 + C::GW) : 1);
+        mbar_init(smem_u32(&ctl->full[i]), is_gather(KIND) ? 1 + 32 * (1 + C::GW) : 1);
         mbar_init(smem_u32(&ctl->empty[i]), 1);
       }
       for (int i = 0; i < 2; ++i) {
@@ -349,7 +373,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
   const int total = ctl->total_tiles;
   const uint32_t b_bytes = (uint32_t)p.BN * BK * 2 / CTAS;  // this CTA's share of a B stage
 
-  // GATE_UP_GATHER: warp 0 and the GW helper warps copy the
+  // Row-gathering kinds: warp 0 and the GW helper warps copy the
   // A tile's rows from x by token id with cp.async (per instruction a warp
   // copies four whole 128-byte rows, 8 lanes per row, into the
   // 128-byte-swizzled tile) and each lane arrives on the stage's barrier when
@@ -359,11 +383,13 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
     constexpr int NG = 32 * (1 + C::GW);            // gathering lanes
     constexpr int PIECES = BM * 8;                   // 16-byte pieces of an A tile
     constexpr int NI = (PIECES + NG - 1) / NG;
-    const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.aux);
+    constexpr int KB = kblock_elems(KIND);
+    const uint8_t* xg = static_cast<const uint8_t*>(p.aux);
+    const size_t row_bytes = (size_t)p.K * (is_fp8(KIND) ? 1 : 2);
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    const int nkb = p.K / BK;
+    const int nkb = p.K / KB;
     const int c = lane & 7;  // 16-byte chunk of a row
     for (int tile = unit; ok && tile < total; tile += nunits) {
       const Tile t = decode_tile<KIND, CTAS>(tile, p, ctl, rank);
@@ -387,7 +413,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
         }
         const uint32_t fb = smem_u32(&ctl->full[stage]);
         const uint32_t sA = smem_u32(smem + (size_t)stage * C::STAGE_BYTES);
-        const int k0 = kb * BK;
+        const int k0 = kb * KB;
         if (gw == 0 && lane == 0) {
           const uint32_t sB = sA + A_BYTES;
           mbar_arrive_expect_tx(fb, b_bytes);
@@ -400,7 +426,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
           const int piece = i * NG + gw * 32 + lane;
           if (piece < PIECES) {
             const int row = piece / 8;
-            const __nv_bfloat16* src = xg + (size_t)tok[i] * p.K + k0 + 8 * c;
+            const uint8_t* src = xg + (size_t)tok[i] * row_bytes + (size_t)kb * 128 + 16 * c;
             const uint32_t dst = sA + (uint32_t)row * 128 + (uint32_t)((c ^ (row & 7)) << 4);
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
           }
@@ -417,7 +443,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
 
   if (warp == 0) {
     // ============================ TMA producer ============================
-    if constexpr (KIND == GATE_UP_GATHER) {
+    if constexpr (is_gather(KIND)) {
       gather_loop(0);
     } else if (lane == 0) {
       int stage = 0;
@@ -459,7 +485,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
                 // pair: the leader holds the gate rows, the peer the up rows
                 tma_load<CTAS>(sB, rank == 0 ? &tmB0 : &tmB1, fb, row0, brow);
               }
-            } else if constexpr (KIND == DOWN_FWD || KIND == DENSE_ADD) {
+            } else if constexpr (is_down_fwd(KIND) || KIND == DENSE_ADD) {
               tma_load<CTAS>(sB, &tmB0, fb, row0,
                              t.group * p.b_group_rows + t.n0 + rank * (p.BN / CTAS));
             } else if constexpr (KIND == DOWN_BWD_DX) {
@@ -508,7 +534,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
           // only the 16-deep MMA steps that hold valid rows are issued.
           const int nkk = KIND == DW ? (valid + 15) / 16 : BK / 16;
           tc_fence_after();
-          if (KIND == GATE_UP_GATHER)  // A was written by cp.async (generic proxy)
+          if (is_gather(KIND))  // A was written by cp.async (generic proxy)
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           if (lane == 0) {
             const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
@@ -519,7 +545,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
                                                      : sdesc(a0 + kk * 32, 16, 1024);
               const uint64_t bd = Traits<KIND>::b_mn ? sdesc(b0 + kk * 2048, CHUNK_BYTES, 1024)
                                                      : sdesc(b0 + kk * 32, 16, 1024);
-              mma_issue<CTAS>(d, ad, bd, p.idesc, (nk > 0 || kk > 0) ? 1u : 0u);
+              mma_issue<CTAS, is_fp8(KIND)>(d, ad, bd, p.idesc, (nk > 0 || kk > 0) ? 1u : 0u);
             }
             mma_commit_to<CTAS>(smem_u32(&ctl->empty[stage]));
           }
@@ -546,7 +572,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
     }
   } else if (C::GW > 0 && warp >= 2 + C::EPW) {
     // ======================= row-gather helper warps ========================
-    if constexpr (KIND == GATE_UP_GATHER) gather_loop(warp - (1 + C::EPW));
+    if constexpr (is_gather(KIND)) gather_loop(warp - (1 + C::EPW));
   } else {
     // ============================ epilogue ================================
     // Each warp owns 32 accumulator rows of the tile (TMEM lanes
@@ -589,7 +615,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
     };
     // Full boxes of the fp32 weight gradients and of the down projection go
     // out through TMA bulk stores instead (measured faster for those two).
-    constexpr bool kTmaOut = KIND == DW || KIND == DOWN_FWD;
+    constexpr bool kTmaOut = KIND == DW || is_down_fwd(KIND);
     EpRing<C::RING> ring{ep_base, 0, lane};
     int gu_ctr = 0;  // DENSE_ADD: running count of this warp's 32-column chunks
     const uint32_t tempty_leader[2] = {
@@ -650,6 +676,21 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * ACC_COLS);
 
+      // FP8 kinds: this lane's row scale (the scale of its token when
+      // gathering) and the expert's output-channel scales
+      float rs = 1.0f;
+      if constexpr (is_fp8(KIND)) {
+        if (lane < nvalid) {
+          int src = rb + lane;
+          if constexpr (is_gather(KIND)) {
+            const int v = p.gather_rows[src];
+            src = (v >= 0 && v < p.gather_limit) ? v : 0;
+          }
+          rs = p.a_scale[src];
+        }
+      }
+      const size_t cs_base = (size_t)(t.group < 0 ? 0 : t.group) * p.b_group_rows + t.n0;
+
       if constexpr (is_gate_up(KIND)) {
         const size_t hp_pitch = (size_t)p.I * 2, gu_pitch = (size_t)p.I * 4;
         for (int c = 0; any && c < p.NH; c += 32) {
@@ -660,8 +701,16 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
           uint32_t hp[16], gp[16], upk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float g0 = f32(g[2 * i]), g1 = f32(g[2 * i + 1]);
-            const float u0 = f32(u[2 * i]), u1 = f32(u[2 * i + 1]);
+            float g0 = f32(g[2 * i]), g1 = f32(g[2 * i + 1]);
+            float u0 = f32(u[2 * i]), u1 = f32(u[2 * i + 1]);
+            if constexpr (is_fp8(KIND)) {
+              const float2 sg = __ldg(reinterpret_cast<const float2*>(p.b_scale0 + cs_base + c) + i);
+              const float2 su = __ldg(reinterpret_cast<const float2*>(p.b_scale1 + cs_base + c) + i);
+              g0 = g0 * rs * sg.x;
+              g1 = g1 * rs * sg.y;
+              u0 = u0 * rs * su.x;
+              u1 = u1 * rs * su.y;
+            }
             const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
             const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
             hp[i] = pack_bf16x2(h0, h1);
@@ -671,7 +720,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) put(ep_base, i, make_uint4(hp[4 * i], hp[4 * i + 1], hp[4 * i + 2], hp[4 * i + 3]));
           flush(ep_base, p.out0, hp_pitch, (size_t)(t.n0 + c) * 2, rb, nvalid, false);
-          if (p.out1) {
+          if (!is_fp8(KIND) && p.out1) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) put(ep_base, i, make_uint4(gp[4 * i], gp[4 * i + 1], gp[4 * i + 2], gp[4 * i + 3]));
             flush(ep_base, p.out1, gu_pitch, (size_t)(t.n0 + c) * 2, rb, nvalid, false);
@@ -680,7 +729,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
             flush(ep_base, p.out1, gu_pitch, (size_t)(p.I + t.n0 + c) * 2, rb, nvalid, false);
           }
         }
-      } else if constexpr (KIND == DOWN_FWD || KIND == GATE_UP_BWD_DX) {
+      } else if constexpr (is_down_fwd(KIND) || KIND == GATE_UP_BWD_DX) {
         const size_t pitch = (size_t)p.ldo * 2;
         for (int c = 0; any && c < p.BN; c += 32) {
           uint32_t a[32];
@@ -689,6 +738,17 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = f32(a[i]);
+          if constexpr (is_fp8(KIND)) {
+            const float4* cs = reinterpret_cast<const float4*>(p.b_scale0 + cs_base + c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 sc = __ldg(cs + i);
+              v[4 * i] = v[4 * i] * rs * sc.x;
+              v[4 * i + 1] = v[4 * i + 1] * rs * sc.y;
+              v[4 * i + 2] = v[4 * i + 2] * rs * sc.z;
+              v[4 * i + 3] = v[4 * i + 3] * rs * sc.w;
+            }
+          }
           uint4 pk[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i)
@@ -898,7 +958,7 @@ int launch(Params p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensor
            const CUtensorMap& o0, const CUtensorMap& o1, cudaStream_t s, const char* what) {
   constexpr bool a_mn = KIND == DW;
   constexpr bool b_mn = KIND == DOWN_BWD_DX || KIND == GATE_UP_BWD_DX || KIND == DW;
-  p.idesc = make_idesc(p.BN, BM * CTAS, a_mn, b_mn);
+  p.idesc = make_idesc(p.BN, BM * CTAS, a_mn, b_mn, is_fp8(KIND));
   long long upper;
   if (KIND == DW) {
     p.m_tiles = (p.M + BM * CTAS - 1) / (BM * CTAS);
@@ -1094,6 +1154,49 @@ int swiglu_impl(const void* a_src, const int32_t* gather_rows, int T, const void
   return run<GATE_UP_FWD>(false, p, ta, tg, tu, th, tgu, s, fn);
 }
 
+// e4m3 operands: H and I must be multiples of 128 (one 128-byte k-block).
+int check_fp8(const char* fn, int H, int I) {
+  if (H % 128 || I % 128)
+    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "%s: e4m3 GEMMs need H%%128==0 and I%%128==0 (H=%d I=%d)", fn, H, I);
+  return MOE_OK;
+}
+
+// Gate/up GEMM + SwiGLU on e4m3 rows (permuted, or gathered from x's token
+// rows by token_of_row) and e4m3 weights, scales applied in the epilogue.
+int swiglu_fp8_impl(const void* a, const float* a_scale, const int32_t* gather_rows, int T,
+                    const void* Wg, const float* Wg_scale, const void* Wu, const float* Wu_scale,
+                    int num_seg, const int32_t* seg_offsets, const int32_t* seg_expert, int R, int H,
+                    int I, int E, void* h, cudaStream_t s, const char* fn) {
+  Params p = base_params(num_seg, seg_offsets, seg_expert, E);
+  p.M = R;
+  p.N = I;
+  p.K = H;
+  p.NH = (I % 128 == 0) ? 128 : 64;
+  p.BN = 2 * p.NH;
+  p.n_tiles = I / p.NH;
+  p.b_group_rows = I;
+  p.I = I;
+  p.out0 = h;
+  p.out1 = nullptr;
+  p.gather_rows = gather_rows;
+  p.gather_limit = T;
+  p.a_scale = a_scale;
+  p.b_scale0 = Wg_scale;
+  p.b_scale1 = Wu_scale;
+  CUtensorMap ta, tg, tu, th;
+  if (gather_rows) {
+    p.aux = a;  // token rows are copied by cp.async; the A map is unused
+    if (int rc = make_tmap_e4m3(&ta, a, H, T, 128, 64)) return rc;
+  } else {
+    if (int rc = make_tmap_e4m3(&ta, a, H, R, 128, BM)) return rc;
+  }
+  if (int rc = make_tmap_e4m3(&tg, Wg, H, (uint64_t)E * I, 128, p.NH)) return rc;
+  if (int rc = make_tmap_e4m3(&tu, Wu, H, (uint64_t)E * I, 128, p.NH)) return rc;
+  if (int rc = make_out_map(&th, h, I, R, false)) return rc;
+  if (gather_rows) return run<GATE_UP_GATHER_FP8>(false, p, ta, tg, tu, th, th, s, fn);
+  return run<GATE_UP_FP8>(false, p, ta, tg, tu, th, th, s, fn);
+}
+
 }  // namespace tc
 }  // namespace moe
 
@@ -1136,6 +1239,57 @@ int moe_grouped_gemm_swiglu_gather(const void* x, const int32_t* token_of_row, i
   if (R == 0 || num_seg == 0) return MOE_OK;
   return swiglu_impl(x, token_of_row, T, Wg, Wu, num_seg, seg_offsets, seg_expert, R, H, I, E, h,
                      gu_save, static_cast<cudaStream_t>(stream), fn);
+}
+
+int moe_grouped_gemm_swiglu_fp8(const void* a, const float* a_scale, const int32_t* token_of_row,
+                                int T, const void* Wg, const float* Wg_scale, const void* Wu,
+                                const float* Wu_scale, int num_seg, const int32_t* seg_offsets,
+                                const int32_t* seg_expert, int R, int H, int I, int E, void* h,
+                                void* stream) {
+  clear_error();
+  const char* fn = "moe_grouped_gemm_swiglu_fp8";
+  if (int rc = check_grouped(fn, num_seg, seg_offsets, R, H, I, E)) return rc;
+  if (int rc = check_fp8(fn, H, I)) return rc;
+  if (token_of_row && T <= 0) return fail(MOE_ERR_INVALID_ARG, "%s: gathering needs T>0", fn);
+  if (R > 0 && num_seg > 0 && (!a || !a_scale || !Wg || !Wg_scale || !Wu || !Wu_scale || !h))
+    return fail(MOE_ERR_INVALID_ARG, "%s: NULL pointer argument", fn);
+  if (!aligned16(a) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(h) || !aligned16(Wg_scale) ||
+      !aligned16(Wu_scale))
+    return fail(MOE_ERR_ALIGNMENT, "%s: tensors and weight scales must be 16-byte aligned", fn);
+  if (R == 0 || num_seg == 0) return MOE_OK;
+  return swiglu_fp8_impl(a, a_scale, token_of_row, T, Wg, Wg_scale, Wu, Wu_scale, num_seg,
+                         seg_offsets, seg_expert, R, H, I, E, h, static_cast<cudaStream_t>(stream), fn);
+}
+
+int moe_grouped_gemm_down_fp8(const void* h, const float* h_scale, const void* Wd,
+                              const float* Wd_scale, int num_seg, const int32_t* seg_offsets,
+                              const int32_t* seg_expert, int R, int H, int I, int E, void* y_perm,
+                              void* stream) {
+  clear_error();
+  const char* fn = "moe_grouped_gemm_down_fp8";
+  if (int rc = check_grouped(fn, num_seg, seg_offsets, R, H, I, E)) return rc;
+  if (int rc = check_fp8(fn, H, I)) return rc;
+  if (R > 0 && num_seg > 0 && (!h || !h_scale || !Wd || !Wd_scale || !y_perm))
+    return fail(MOE_ERR_INVALID_ARG, "%s: NULL pointer argument", fn);
+  if (!aligned16(h) || !aligned16(Wd) || !aligned16(y_perm) || !aligned16(Wd_scale))
+    return fail(MOE_ERR_ALIGNMENT, "%s: tensors and weight scales must be 16-byte aligned", fn);
+  if (R == 0 || num_seg == 0) return MOE_OK;
+  Params p = base_params(num_seg, seg_offsets, seg_expert, E);
+  p.M = R;
+  p.N = H;
+  p.K = I;
+  p.BN = pick_bn(H);
+  p.n_tiles = H / p.BN;
+  p.b_group_rows = H;
+  p.ldo = H;
+  p.out0 = y_perm;
+  p.a_scale = h_scale;
+  p.b_scale0 = Wd_scale;
+  CUtensorMap ta, tb, to;
+  if (int rc = make_tmap_e4m3(&ta, h, I, R, 128, BM)) return rc;
+  if (int rc = make_tmap_e4m3(&tb, Wd, I, (uint64_t)E * H, 128, p.BN)) return rc;
+  if (int rc = make_out_map(&to, y_perm, H, R, false)) return rc;
+  return run<DOWN_FP8>(false, p, ta, tb, tb, to, to, static_cast<cudaStream_t>(stream), fn);
 }
 
 int moe_grouped_gemm_down(const void* h, const void* Wd, int num_seg, const int32_t* seg_offsets,

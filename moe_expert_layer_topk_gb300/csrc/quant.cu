@@ -1,0 +1,98 @@
+// Per-row e4m3 quantisation of bf16 tensors (sm_103a).
+//
+// FP8 reading of "TorchTitan FSDP2 完全指南", performance table (FP8 matmuls
+// in training; the page gives no recipe): one fp32 scale per stored row,
+// s = amax / 448 (1 for an all-zero row), codes e4m3(a / s) rounded to
+// nearest even and saturated at 448.  Rows are token rows of x, permuted
+// rows of h, or output channels of the expert weights ([E * out, in]).
+//
+// HBM-bound: one warp per row reads the row once into registers (rows of
+// up to 2048 elements; longer rows are read twice, the second time from
+// L2), reduces |a| to amax with shuffles, then writes the codes with 8-byte
+// stores and the scale.
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int kQuantWarps = 8;   // rows per 256-thread block
+constexpr int kCachedVecs = 8;   // 16-byte vectors held per lane (8 bf16 each)
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ float amax8(uint4 v, float m) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(bf_lo(w[i])), fabsf(bf_hi(w[i]))));
+  return m;
+}
+
+// Eight bf16 values divided by s (IEEE division) -> eight e4m3 codes.
+__device__ __forceinline__ uint2 codes8(uint4 v, float s) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t out[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float2 a = make_float2(__fdiv_rn(bf_lo(w[2 * h]), s), __fdiv_rn(bf_hi(w[2 * h]), s));
+    const float2 b = make_float2(__fdiv_rn(bf_lo(w[2 * h + 1]), s), __fdiv_rn(bf_hi(w[2 * h + 1]), s));
+    const uint32_t ca = __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
+    const uint32_t cb = __nv_cvt_float2_to_fp8x2(b, __NV_SATFINITE, __NV_E4M3);
+    out[h] = (ca & 0xFFFFu) | (cb << 16);
+  }
+  return make_uint2(out[0], out[1]);
+}
+
+__global__ void __launch_bounds__(32 * kQuantWarps)
+    quantize_rows_e4m3_kernel(const __nv_bfloat16* __restrict__ a, int rows, int cols,
+                              uint8_t* __restrict__ q, float* __restrict__ scale) {
+  moe::pdl_wait();
+  moe::pdl_trigger();
+  const int row = blockIdx.x * kQuantWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const uint4* src = reinterpret_cast<const uint4*>(a + (size_t)row * cols);
+  uint2* dst = reinterpret_cast<uint2*>(q + (size_t)row * cols);
+  const int nv = cols / 8;
+  uint4 cache[kCachedVecs];
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kCachedVecs; ++i) {
+    const int v = lane + 32 * i;
+    cache[i] = v < nv ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+    m = amax8(cache[i], m);
+  }
+  for (int v = lane + 32 * kCachedVecs; v < nv; v += 32) m = amax8(__ldg(src + v), m);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  const float s = m > 0.0f ? __fdiv_rn(m, 448.0f) : 1.0f;
+  if (lane == 0) scale[row] = s;
+#pragma unroll
+  for (int i = 0; i < kCachedVecs; ++i) {
+    const int v = lane + 32 * i;
+    if (v < nv) dst[v] = codes8(cache[i], s);
+  }
+  for (int v = lane + 32 * kCachedVecs; v < nv; v += 32) dst[v] = codes8(__ldg(src + v), s);
+}
+
+}  // namespace
+
+extern "C" int moe_quantize_rows_e4m3(const void* a, int rows, int cols, void* q, float* scale,
+                                      void* stream) {
+  moe::clear_error();
+  const char* fn = "moe_quantize_rows_e4m3";
+  if (rows < 0 || cols <= 0 || cols % 8)
+    return moe::fail(MOE_ERR_INVALID_ARG, "%s: need rows>=0, cols>0, cols%%8==0 (rows=%d cols=%d)", fn,
+                     rows, cols);
+  if (rows == 0) return MOE_OK;
+  if (!a || !q || !scale) return moe::fail(MOE_ERR_INVALID_ARG, "%s: NULL pointer argument", fn);
+  if (!moe::aligned16(a) || (reinterpret_cast<uintptr_t>(q) & 7u) || (reinterpret_cast<uintptr_t>(scale) & 3u))
+    return moe::fail(MOE_ERR_ALIGNMENT, "%s: a must be 16-byte, q 8-byte, scale 4-byte aligned", fn);
+  const int blocks = (rows + kQuantWarps - 1) / kQuantWarps;
+  cudaError_t e = moe::launch_pdl(quantize_rows_e4m3_kernel, dim3(blocks), dim3(32 * kQuantWarps), 0,
+                                  static_cast<cudaStream_t>(stream),
+                                  static_cast<const __nv_bfloat16*>(a), rows, cols,
+                                  static_cast<uint8_t*>(q), scale);
+  if (e != cudaSuccess) return moe::fail(MOE_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+  return MOE_OK;
+}

@@ -271,10 +271,25 @@ __device__ __forceinline__ void tma_load_mn(uint32_t dst, const CUtensorMap* map
   }
 }
 
-template <int CTAS>
+// D[tmem] (+)= A[smem] * B[smem], e4m3 inputs (K = 32 per instruction, the
+// same 32 bytes of each operand row as one bf16 step), fp32 accumulation.
+__device__ __forceinline__ void mma_e4m3(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+template <int CTAS, bool FP8 = false>
 __device__ __forceinline__ void mma_issue(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
                                           uint32_t accumulate) {
-  if constexpr (CTAS == 1) {
+  static_assert(!FP8 || CTAS == 1, "e4m3 GEMMs run one CTA per tile");
+  if constexpr (FP8) {
+    mma_e4m3(d, a, b, idesc, accumulate);
+  } else if constexpr (CTAS == 1) {
     mma_bf16(d, a, b, idesc, accumulate);
   } else {
     asm volatile(
@@ -351,23 +366,37 @@ inline EncodeTiledFn encode_fn() {
 // 2-D tensor [outer, inner] row-major, box {box_inner, box_outer}.  Operand
 // maps are bf16 with the 128-byte swizzle; output maps use 64-byte boxes with
 // the 64-byte swizzle (bf16 or fp32).
-inline int make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
-              uint32_t box_outer, bool fp32 = false,
-              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+inline int make_tmap_typed(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+                           uint32_t box_inner, uint32_t box_outer, CUtensorMapDataType dt, uint64_t esz,
+                           CUtensorMapSwizzle swz) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  const uint64_t esz = fp32 ? 4 : 2;
   cuuint64_t dims[2] = {inner, outer > 0 ? outer : 1};
   cuuint64_t strides[1] = {inner * esz};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+  CUresult r = fn(m, dt, 2,
                   const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%llu x %llu] box %u x %u",
                 (int)r, (unsigned long long)outer, (unsigned long long)inner, box_inner, box_outer);
   return MOE_OK;
+}
+
+inline int make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                     uint32_t box_outer, bool fp32 = false,
+                     CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+  return make_tmap_typed(m, ptr, inner, outer, box_inner, box_outer,
+                         fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         fp32 ? 4 : 2, swz);
+}
+
+// e4m3 operand map (bytes), 128-byte swizzle.
+inline int make_tmap_e4m3(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+                          uint32_t box_inner, uint32_t box_outer) {
+  return make_tmap_typed(m, ptr, inner, outer, box_inner, box_outer, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // MN-major operand map: the bf16 tensor [rows, cols] seen as 3-D
@@ -394,9 +423,9 @@ inline int make_out_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_
   return make_tmap(m, ptr, inner, outer, fp32 ? 16 : 32, 32, fp32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-inline uint32_t make_idesc(int n, int m, bool a_mn, bool b_mn) {
+inline uint32_t make_idesc(int n, int m, bool a_mn, bool b_mn, bool e4m3 = false) {
   return (1u << 4)                    // D fp32
-         | (1u << 7) | (1u << 10)     // A, B bf16
+         | (e4m3 ? 0u : (1u << 7) | (1u << 10))  // A, B bf16 (kind::f16) or e4m3 (kind::f8f6f4: code 0)
          | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
          ((uint32_t)(n >> 3) << 17)   // N / 8
          | ((uint32_t)(m >> 4) << 24);  // M / 16

@@ -11,9 +11,9 @@ import torch
 
 from . import (moe_combine, moe_combine_bwd, moe_dispatch, moe_dispatch_bwd,
                moe_dispatch_workspace_size, moe_grouped_gemm_bwd_workspace_size,
-               moe_grouped_gemm_down, moe_grouped_gemm_down_bwd,
-               moe_grouped_gemm_swiglu, moe_grouped_gemm_swiglu_bwd,
-               moe_grouped_gemm_swiglu_gather, moe_route_topk,
+               moe_grouped_gemm_down, moe_grouped_gemm_down_bwd, moe_grouped_gemm_down_fp8,
+               moe_grouped_gemm_swiglu, moe_grouped_gemm_swiglu_bwd, moe_grouped_gemm_swiglu_fp8,
+               moe_grouped_gemm_swiglu_gather, moe_quantize_rows_e4m3, moe_route_topk,
                moe_route_topk_bwd, moe_route_topk_bwd_workspace_size,
                moe_route_topk_workspace_size)
 
@@ -27,17 +27,24 @@ class MoELayer:
 
     fused_dispatch (forward only): dispatch only ranks the slots and the
     gate/up GEMM reads its rows straight from x by token id, so x_perm is
-    never written (moe_grouped_gemm_swiglu_gather)."""
+    never written (moe_grouped_gemm_swiglu_gather).
+
+    fp8 (forward only, implies fused_dispatch): x is quantised to e4m3 per
+    token, the gate/up GEMM gathers its rows from those codes, h is
+    quantised per row, and both GEMMs run on e4m3 weights prepared once by
+    `quantize_weights` (one scale per output channel)."""
 
     def __init__(self, T: int, H: int, I: int, E: int, k: int, ep_size: int = 1, *,
-                 training: bool = True, fused_dispatch: bool = False,
+                 training: bool = True, fused_dispatch: bool = False, fp8: bool = False,
                  device: str | torch.device = "cuda"):
+        fused_dispatch = fused_dispatch or fp8
         if fused_dispatch and training:
             raise ValueError("fused_dispatch keeps no x_perm, which the backward pass needs")
         self.T, self.H, self.I, self.E, self.k, self.ep_size = T, H, I, E, k, ep_size
         self.R = R = T * k
         self.training = training
         self.fused_dispatch = fused_dispatch
+        self.fp8 = fp8
         self._x = None
         dev = torch.device(device)
         i32, f32, bf = torch.int32, torch.float32, torch.bfloat16
@@ -56,6 +63,10 @@ class MoELayer:
         self.gu = e(R, 2 * I, dt=bf) if training else None
         self.y_perm = e(R, H, dt=bf)
         self.y = e(T, H, dt=bf)
+        if fp8:
+            u8 = torch.uint8
+            self.x_q, self.x_scale = e(T, H, dt=u8), e(T, dt=f32)
+            self.h_q, self.h_scale = e(R, I, dt=u8), e(R, dt=f32)
         if training:
             self.dy_perm = e(R, H, dt=bf)
             self.d_w = e(T, k, dt=f32)
@@ -71,6 +82,17 @@ class MoELayer:
             self.ws_gemm_bwd = _ws(moe_grouped_gemm_bwd_workspace_size(E), dev)
 
     # ---------------------------------------------------------------- forward
+    def quantize_weights(self, Wg, Wu, Wd, stream=None):
+        """e4m3 codes and per-output-channel scales of the expert weights."""
+        E, H, I = self.E, self.H, self.I
+        out = {}
+        for name, W, rows, cols in (("Wg", Wg, E * I, H), ("Wu", Wu, E * I, H), ("Wd", Wd, E * H, I)):
+            q = torch.empty(W.shape, dtype=torch.uint8, device=W.device)
+            sc = torch.empty(rows, dtype=torch.float32, device=W.device)
+            moe_quantize_rows_e4m3(W, rows, cols, q, sc, stream)
+            out[name], out[name + "_scale"] = q, sc
+        return out
+
     def route(self, x, Wr, bias=None, stream=None):
         moe_route_topk(x, Wr, bias, self.T, self.H, self.E, self.k, self.ep_size, self.topk_idx,
                        self.topk_w, self.counts, self.offsets, self.rank_offsets, self.ws_route,
@@ -82,6 +104,19 @@ class MoELayer:
                      self.row_of_slot, self.token_of_row, self.ws_dispatch, stream)
 
     def experts(self, Wg, Wu, Wd, stream=None):
+        """Wg, Wu, Wd: bf16 expert weights, or (fp8 layers) the dict that
+        `quantize_weights` returns, passed as Wg (Wu and Wd unused)."""
+        if self.fp8:
+            w = Wg
+            T, H, I, E, R = self.T, self.H, self.I, self.E, self.R
+            moe_quantize_rows_e4m3(self._x, T, H, self.x_q, self.x_scale, stream)
+            moe_grouped_gemm_swiglu_fp8(self.x_q, self.x_scale, self.token_of_row, T, w["Wg"],
+                                        w["Wg_scale"], w["Wu"], w["Wu_scale"], E, self.offsets, None,
+                                        R, H, I, E, self.h, stream)
+            moe_quantize_rows_e4m3(self.h, R, I, self.h_q, self.h_scale, stream)
+            moe_grouped_gemm_down_fp8(self.h_q, self.h_scale, w["Wd"], w["Wd_scale"], E, self.offsets,
+                                      None, R, H, I, E, self.y_perm, stream)
+            return
         if self.fused_dispatch:
             moe_grouped_gemm_swiglu_gather(self._x, self.token_of_row, self.T, Wg, Wu, self.E,
                                            self.offsets, None, self.R, self.H, self.I, self.E, self.h,
