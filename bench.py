@@ -529,6 +529,25 @@ def run_profile_case(args):
                       "device_status": m.moe_read_device_status(reset=True)}))
 
 
+def run_profile_fp8(args):
+    """Untimed fp8 forward passes of one layer shape (for ncu captures)."""
+    import torch
+
+    import moe_expert_layer_topk_gb300 as m
+    from moe_expert_layer_topk_gb300.synth import LayerShape, make_layer_inputs
+    T, H, I, E, k = (int(v) for v in args.profile_fp8.split(","))
+    shape = LayerShape(T=T, H=H, I=I, E=E, k=k, ep_size=1)
+    inp = make_layer_inputs(shape, 0, with_dy=False)
+    g = {n: (v.cuda() if isinstance(v, torch.Tensor) else v) for n, v in inp.items()}
+    layer = m.MoELayer(T, H, I, E, k, 1, training=False, fp8=True)
+    w8 = layer.quantize_weights(g["Wg"], g["Wu"], g["Wd"])
+    for _ in range(args.steps):
+        layer.forward(g["x"], g["Wr"], None, w8, None, None)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_fp8": [T, H, I, E, k], "passes": args.steps,
+                      "device_status": m.moe_read_device_status(reset=True)}))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -542,11 +561,15 @@ def main(argv=None):
                     help="run --steps untimed forward+backward passes of this shape and exit")
     ap.add_argument("--profile-router", default=None, metavar="T,H,E,k",
                     help="run --steps untimed router passes and exit")
+    ap.add_argument("--profile-fp8", default=None, metavar="T,H,I,E,k",
+                    help="run --steps untimed fp8 forward passes of this shape and exit")
     args = ap.parse_args(argv)
     if args.profile_router:
         return run_profile_router(args)
     if args.profile_case:
         return run_profile_case(args)
+    if args.profile_fp8:
+        return run_profile_fp8(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     from moe_expert_layer_topk_gb300.synth import CONFIGS, make_layer_inputs

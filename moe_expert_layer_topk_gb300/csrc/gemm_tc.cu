@@ -165,14 +165,17 @@ struct Cfg {
   static constexpr int B_BYTES = B_BYTES_MAX / CTAS;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TILE_M = BM * CTAS;
-  // The weight-gradient kind (fp32 output, short reductions) and the
-  // SwiGLU-backward kind (heavy epilogue) run eight epilogue warps, two per
-  // TMEM lane quadrant, each on half the columns (a one-box store ring each).
-  static constexpr int EPW = (KIND == DW || KIND == DOWN_BWD_DX) ? 8 : 4;
+  // The weight-gradient kind (fp32 output, short reductions), the
+  // SwiGLU-backward kind (heavy epilogue) and the down projections (256
+  // output columns per tile from a short reduction, K = I) run eight
+  // epilogue warps, two per TMEM lane quadrant, each on half the columns (a
+  // one-box store ring each).
+  static constexpr bool EP8 = KIND == DW || KIND == DOWN_BWD_DX || is_down_fwd(KIND);
+  static constexpr int EPW = EP8 ? 8 : 4;
   // row-gathering kinds: four more warps share the row gather
   static constexpr int GW = is_gather(KIND) ? 4 : 0;
   static constexpr int NTHREADS = 64 + 32 * (EPW + GW);
-  static constexpr int RING = (KIND == DW || KIND == DOWN_BWD_DX) ? 1 : EP_SLOTS;
+  static constexpr int RING = EP8 ? 1 : EP_SLOTS;
   static constexpr int EP_WARP = gu_tma ? EP_BOX_BYTES * 2 * GU_SETS : EP_BOX_BYTES * RING;
   static constexpr int EP_TOTAL = EPW * EP_WARP;
   // without the segment tables
@@ -672,28 +675,41 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
       if constexpr (KIND == DOWN_BWD_DX) {
         if (any) ld_gu(cbeg, gq, uq);
       }
+      // FP8 kinds: this lane's row scale (the scale of its token when
+      // gathering) and the expert's output-channel scales, lane L holding
+      // column L of the current 32-column chunk (gate in sc0, up in sc1).
+      // Loaded before the accumulator wait, later chunks one chunk ahead.
+      float rs = 1.0f, sc0 = 0.0f, sc1 = 0.0f;
+      const size_t cs_base = (size_t)(t.group < 0 ? 0 : t.group) * p.b_group_rows + t.n0;
+      if constexpr (is_fp8(KIND)) {
+        if (any) {
+          if (lane < nvalid) {
+            int src = rb + lane;
+            if constexpr (is_gather(KIND)) {
+              const int v = p.gather_rows[src];
+              src = (v >= 0 && v < p.gather_limit) ? v : 0;
+            }
+            rs = __ldg(p.a_scale + src);
+          }
+          sc0 = __ldg(p.b_scale0 + cs_base + cbeg + lane);
+          if constexpr (is_gate_up(KIND)) sc1 = __ldg(p.b_scale1 + cs_base + lane);
+        }
+      }
       if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&ctl->tfull[buf]), use & 1u, &ctl->abort_flag, p.status))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * ACC_COLS);
 
-      // FP8 kinds: this lane's row scale (the scale of its token when
-      // gathering) and the expert's output-channel scales
-      float rs = 1.0f;
-      if constexpr (is_fp8(KIND)) {
-        if (lane < nvalid) {
-          int src = rb + lane;
-          if constexpr (is_gather(KIND)) {
-            const int v = p.gather_rows[src];
-            src = (v >= 0 && v < p.gather_limit) ? v : 0;
-          }
-          rs = p.a_scale[src];
-        }
-      }
-      const size_t cs_base = (size_t)(t.group < 0 ? 0 : t.group) * p.b_group_rows + t.n0;
 
       if constexpr (is_gate_up(KIND)) {
         const size_t hp_pitch = (size_t)p.I * 2, gu_pitch = (size_t)p.I * 4;
         for (int c = 0; any && c < p.NH; c += 32) {
+          float nx0 = 0.0f, nx1 = 0.0f;  // FP8: the next chunk's column scales
+          if constexpr (is_fp8(KIND)) {
+            if (c + 32 < p.NH) {
+              nx0 = __ldg(p.b_scale0 + cs_base + c + 32 + lane);
+              nx1 = __ldg(p.b_scale1 + cs_base + c + 32 + lane);
+            }
+          }
           uint32_t g[32], u[32];
           tmem_ld32(taddr + c, g);
           tmem_ld32(taddr + p.NH + c, u);
@@ -704,12 +720,10 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
             float g0 = f32(g[2 * i]), g1 = f32(g[2 * i + 1]);
             float u0 = f32(u[2 * i]), u1 = f32(u[2 * i + 1]);
             if constexpr (is_fp8(KIND)) {
-              const float2 sg = __ldg(reinterpret_cast<const float2*>(p.b_scale0 + cs_base + c) + i);
-              const float2 su = __ldg(reinterpret_cast<const float2*>(p.b_scale1 + cs_base + c) + i);
-              g0 = g0 * rs * sg.x;
-              g1 = g1 * rs * sg.y;
-              u0 = u0 * rs * su.x;
-              u1 = u1 * rs * su.y;
+              g0 = g0 * rs * __shfl_sync(0xffffffffu, sc0, 2 * i);
+              g1 = g1 * rs * __shfl_sync(0xffffffffu, sc0, 2 * i + 1);
+              u0 = u0 * rs * __shfl_sync(0xffffffffu, sc1, 2 * i);
+              u1 = u1 * rs * __shfl_sync(0xffffffffu, sc1, 2 * i + 1);
             }
             const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
             const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
@@ -728,10 +742,16 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
             for (int i = 0; i < 4; ++i) put(ep_base, i, make_uint4(upk[4 * i], upk[4 * i + 1], upk[4 * i + 2], upk[4 * i + 3]));
             flush(ep_base, p.out1, gu_pitch, (size_t)(p.I + t.n0 + c) * 2, rb, nvalid, false);
           }
+          sc0 = nx0;
+          sc1 = nx1;
         }
       } else if constexpr (is_down_fwd(KIND) || KIND == GATE_UP_BWD_DX) {
         const size_t pitch = (size_t)p.ldo * 2;
-        for (int c = 0; any && c < p.BN; c += 32) {
+        for (int c = cbeg; any && c < cbeg + cspan; c += 32) {
+          float nx0 = 0.0f;  // FP8: the next chunk's column scales
+          if constexpr (is_fp8(KIND)) {
+            if (c + 32 < cbeg + cspan) nx0 = __ldg(p.b_scale0 + cs_base + c + 32 + lane);
+          }
           uint32_t a[32];
           tmem_ld32(taddr + c, a);
           tmem_wait_ld();
@@ -739,15 +759,9 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = f32(a[i]);
           if constexpr (is_fp8(KIND)) {
-            const float4* cs = reinterpret_cast<const float4*>(p.b_scale0 + cs_base + c);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 sc = __ldg(cs + i);
-              v[4 * i] = v[4 * i] * rs * sc.x;
-              v[4 * i + 1] = v[4 * i + 1] * rs * sc.y;
-              v[4 * i + 2] = v[4 * i + 2] * rs * sc.z;
-              v[4 * i + 3] = v[4 * i + 3] * rs * sc.w;
-            }
+            for (int i = 0; i < 32; ++i) v[i] = v[i] * rs * __shfl_sync(0xffffffffu, sc0, i);
+            sc0 = nx0;
           }
           uint4 pk[4];
 #pragma unroll

@@ -6,10 +6,11 @@
 // nearest even and saturated at 448.  Rows are token rows of x, permuted
 // rows of h, or output channels of the expert weights ([E * out, in]).
 //
-// HBM-bound: one warp per row reads the row once into registers (rows of
-// up to 2048 elements; longer rows are read twice, the second time from
-// L2), reduces |a| to amax with shuffles, then writes the codes with 8-byte
-// stores and the scale.
+// HBM-bound: one warp per row reads the row once into registers (NC
+// 16-byte vectors per lane, NC picked from the row length so that short
+// rows keep few registers and many warps per SM; rows longer than 2048
+// elements are read twice, the second time from L2), reduces |a| to amax
+// with shuffles, then writes the codes with 8-byte stores and the scale.
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -17,7 +18,6 @@
 namespace {
 
 constexpr int kQuantWarps = 8;   // rows per 256-thread block
-constexpr int kCachedVecs = 8;   // 16-byte vectors held per lane (8 bf16 each)
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -44,7 +44,9 @@ __device__ __forceinline__ uint2 codes8(uint4 v, float s) {
   return make_uint2(out[0], out[1]);
 }
 
-__global__ void __launch_bounds__(32 * kQuantWarps)
+// NC: 16-byte vectors (8 bf16 each) a lane holds in registers.
+template <int NC>
+__global__ void __launch_bounds__(32 * kQuantWarps, NC <= 1 ? 6 : (NC <= 4 ? 4 : 2))
     quantize_rows_e4m3_kernel(const __nv_bfloat16* __restrict__ a, int rows, int cols,
                               uint8_t* __restrict__ q, float* __restrict__ scale) {
   moe::pdl_wait();
@@ -54,25 +56,25 @@ __global__ void __launch_bounds__(32 * kQuantWarps)
   const uint4* src = reinterpret_cast<const uint4*>(a + (size_t)row * cols);
   uint2* dst = reinterpret_cast<uint2*>(q + (size_t)row * cols);
   const int nv = cols / 8;
-  uint4 cache[kCachedVecs];
+  uint4 cache[NC];
   float m = 0.0f;
 #pragma unroll
-  for (int i = 0; i < kCachedVecs; ++i) {
+  for (int i = 0; i < NC; ++i) {
     const int v = lane + 32 * i;
     cache[i] = v < nv ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
     m = amax8(cache[i], m);
   }
-  for (int v = lane + 32 * kCachedVecs; v < nv; v += 32) m = amax8(__ldg(src + v), m);
+  for (int v = lane + 32 * NC; v < nv; v += 32) m = amax8(__ldg(src + v), m);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
   const float s = m > 0.0f ? __fdiv_rn(m, 448.0f) : 1.0f;
   if (lane == 0) scale[row] = s;
 #pragma unroll
-  for (int i = 0; i < kCachedVecs; ++i) {
+  for (int i = 0; i < NC; ++i) {
     const int v = lane + 32 * i;
     if (v < nv) dst[v] = codes8(cache[i], s);
   }
-  for (int v = lane + 32 * kCachedVecs; v < nv; v += 32) dst[v] = codes8(__ldg(src + v), s);
+  for (int v = lane + 32 * NC; v < nv; v += 32) dst[v] = codes8(__ldg(src + v), s);
 }
 
 }  // namespace
@@ -89,7 +91,13 @@ extern "C" int moe_quantize_rows_e4m3(const void* a, int rows, int cols, void* q
   if (!moe::aligned16(a) || (reinterpret_cast<uintptr_t>(q) & 7u) || (reinterpret_cast<uintptr_t>(scale) & 3u))
     return moe::fail(MOE_ERR_ALIGNMENT, "%s: a must be 16-byte, q 8-byte, scale 4-byte aligned", fn);
   const int blocks = (rows + kQuantWarps - 1) / kQuantWarps;
-  cudaError_t e = moe::launch_pdl(quantize_rows_e4m3_kernel, dim3(blocks), dim3(32 * kQuantWarps), 0,
+  const int per_lane = (cols / 8 + 31) / 32;  // 16-byte vectors per lane
+  auto kernel = per_lane <= 1   ? quantize_rows_e4m3_kernel<1>
+                : per_lane <= 2 ? quantize_rows_e4m3_kernel<2>
+                : per_lane <= 3 ? quantize_rows_e4m3_kernel<3>
+                : per_lane <= 4 ? quantize_rows_e4m3_kernel<4>
+                                : quantize_rows_e4m3_kernel<8>;
+  cudaError_t e = moe::launch_pdl(kernel, dim3(blocks), dim3(32 * kQuantWarps), 0,
                                   static_cast<cudaStream_t>(stream),
                                   static_cast<const __nv_bfloat16*>(a), rows, cols,
                                   static_cast<uint8_t*>(q), scale);
