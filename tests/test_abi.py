@@ -111,3 +111,25 @@ def test_zero_tokens_is_a_no_op(L):
     assert L.moe_dispatch_bwd(P, P, 0, 128, 2, P, None) == OK
     assert L.moe_grouped_gemm_swiglu(P, P, P, 8, P, None, 0, 128, 64, 8, P, None, None, 0, None) == OK
     assert L.moe_grouped_gemm_down(P, P, 0, None, None, 64, 128, 64, 8, P, None, 0, None) == OK
+
+
+def test_fp8_entry_points_reject_bad_args(L):
+    P = FAKE
+    # per-row quantiser: cols must be a positive multiple of 8; no rows is a no-op
+    assert L.moe_quantize_rows_e4m3(P, 16, 12, P, P, None) == INVALID
+    assert L.moe_quantize_rows_e4m3(P, 0, 16, P, P, None) == OK
+    assert L.moe_quantize_rows_e4m3(P, 16, 16, None, P, None) == INVALID
+    assert L.moe_quantize_rows_e4m3(P + 8, 16, 16, P, P, None) == ALIGN
+    assert L.moe_quantize_rows_e4m3(P, 16, 16, P + 4, P, None) == ALIGN
+    # e4m3 GEMMs: H and I multiples of 128
+    assert L.moe_grouped_gemm_swiglu_fp8(P, P, None, 0, P, P, P, P, 8, P, None, 64, 128, 64, 8, P, None) == SHAPE
+    assert "128" in _err(L)
+    assert L.moe_grouped_gemm_down_fp8(P, P, P, P, 8, P, None, 64, 192, 128, 8, P, None) == SHAPE
+    assert L.moe_grouped_gemm_swiglu_fp8(P, None, None, 0, P, P, P, P, 8, P, None, 64, 128, 128, 8, P,
+                                         None) == INVALID
+    assert L.moe_grouped_gemm_swiglu_fp8(P, P, P, 0, P, P, P, P, 8, P, None, 64, 128, 128, 8, P,
+                                         None) == INVALID  # gathering needs T > 0
+    assert L.moe_grouped_gemm_down_fp8(P, P, P, P + 4, 8, P, None, 64, 128, 128, 8, P, None) == ALIGN
+    # no rows: nothing to do
+    assert L.moe_grouped_gemm_swiglu_fp8(P, P, None, 0, P, P, P, P, 8, P, None, 0, 128, 128, 8, P, None) == OK
+    assert L.moe_grouped_gemm_down_fp8(P, P, P, P, 8, P, None, 0, 128, 128, 8, P, None) == OK
