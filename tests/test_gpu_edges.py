@@ -9,7 +9,7 @@ import torch.nn.functional as F
 
 import moe_expert_layer_topk_gb300 as m
 import oracle
-from gpu_util import assert_close, bits, f32, inputs, oracle_backward, oracle_chain, to_dev
+from gpu_util import assert_close, inputs, oracle_backward, oracle_chain, to_dev
 from moe_expert_layer_topk_gb300.synth import LayerShape, bf16_bits, make_segment_inputs
 
 pytestmark = pytest.mark.gpu
@@ -122,7 +122,8 @@ def test_segmented_rows(R, H, I, E, S):
     y = torch.zeros(R, H, dtype=torch.bfloat16, device=dev)
     m.moe_grouped_gemm_swiglu(xp, Wg, Wu, nseg, so_d, se_d, R, H, I, E, h, gu)
     m.moe_grouped_gemm_down(h, Wd, nseg, so_d, se_d, R, H, I, E, y)
-    dy = torch.randn(R, H, device=dev).to(torch.bfloat16)
+    dy_host = torch.randn(R, H, generator=torch.Generator().manual_seed(29)).to(torch.bfloat16)
+    dy = dy_host.to(dev)
     dgu = torch.zeros(R, 2 * I, dtype=torch.bfloat16, device=dev)
     dWd = torch.empty(E, H, I, device=dev)
     dx = torch.zeros(R, H, dtype=torch.bfloat16, device=dev)
@@ -139,12 +140,14 @@ def test_segmented_rows(R, H, I, E, S):
                                                save_gu=True)
     covered = slice(int(son[0]), int(son[-1]))
     assert_close(h[covered], h_ref[covered], "h")
-    y_ref = oracle.grouped_gemm_down(f32(h), bf16_bits(s["Wd"]), son, sen)
+    # the oracle's own chain from here on (its fp32 h, g|u and dgu)
+    y_ref = oracle.grouped_gemm_down(h_ref, bf16_bits(s["Wd"]), son, sen)
     assert_close(y[covered], y_ref[covered], "y_perm")
-    dgu_ref, dWd_ref = oracle.grouped_gemm_down_bwd(f32(dy), f32(h), f32(gu), bf16_bits(s["Wd"]), son, sen)
+    dy_ref = oracle.widen_bf16(bf16_bits(dy_host))
+    dgu_ref, dWd_ref = oracle.grouped_gemm_down_bwd(dy_ref, h_ref, gu_ref, bf16_bits(s["Wd"]), son, sen)
     assert_close(dgu[covered], dgu_ref[covered], "dgu")
     assert_close(dWd, dWd_ref, "dWd")
-    dx_ref, dWg_ref, dWu_ref = oracle.grouped_gemm_swiglu_bwd(f32(dgu), xo, bf16_bits(s["Wg"]),
+    dx_ref, dWg_ref, dWu_ref = oracle.grouped_gemm_swiglu_bwd(dgu_ref, xo, bf16_bits(s["Wg"]),
                                                               bf16_bits(s["Wu"]), son, sen)
     assert_close(dx[covered], dx_ref[covered], "dx_perm")
     assert_close(dWg, dWg_ref, "dWg")

@@ -212,3 +212,45 @@ def test_fp8_layer_forward(T, H, I, E, k, ep):
     assert_close(y, y8_ref, "y (fp8 layer vs fp8 oracle)")
     # format check: the e4m3 forward stays within e4m3's error of the bf16 layer
     assert_close(y, f["y"], "y (fp8 layer vs bf16 oracle)", max_frac=0.25, rel=0.1)
+
+
+def test_fp8_layer_full_size_sampled_tokens():
+    """The fp8 forward as bench.py times it (Qwen3-30B-A3B shapes, T=4096):
+    routing bit for bit over every token, the weight codes and scales of the
+    experts the sampled tokens use bit for bit, and those tokens' outputs
+    against the oracle's fp8 chain (x and h quantised per row, weights per
+    output channel, h and y_perm rounded to bf16 where the layer stores them)."""
+    from moe_expert_layer_topk_gb300.synth import CONFIGS, make_layer_inputs
+    shape = CONFIGS["qwen3_30b_fwd"]
+    inp = make_layer_inputs(shape, 0, with_dy=False)
+    g = to_dev(inp)
+    L = m.MoELayer(shape.T, shape.H, shape.I, shape.E, shape.k, shape.ep_size, training=False, fp8=True)
+    w8 = L.quantize_weights(g["Wg"], g["Wu"], g["Wd"])
+    y = L.forward(g["x"], g["Wr"], g["bias"], w8, None, None)
+    torch.cuda.synchronize()
+    assert m.moe_read_device_status(reset=True) == 0
+    rt = oracle.route_topk(bits(inp["x"]), inp["Wr"].numpy(), None, shape.k, shape.ep_size)
+    assert np.array_equal(L.topk_idx.cpu().numpy(), rt["topk_idx"])
+    assert np.array_equal(L.offsets.cpu().numpy(), rt["offsets"])
+    rng = np.random.default_rng(8)
+    toks = sorted(rng.choice(shape.T, 4, replace=False).tolist())
+    sub = dict(inp)
+    sub["x"] = inp["x"][toks].contiguous()
+    sub["T"] = len(toks)
+    f = oracle_chain(sub)
+    # the oracle's fp8 chain over the experts these tokens use only
+    used = sorted(set(f["rt"]["topk_idx"].reshape(-1).tolist()))
+    remap = np.zeros(shape.E, np.int32)
+    remap[used] = np.arange(len(used), dtype=np.int32)
+    W = {n: oracle.quantize_rows_e4m3(oracle.widen_bf16(bits(inp[n][used]))) for n in ("Wg", "Wu", "Wd")}
+    for n in ("Wg", "Wu", "Wd"):
+        assert np.array_equal(w8[n][used].cpu().numpy(), W[n][0])
+        assert np.array_equal(w8[n + "_scale"].view(shape.E, -1)[used].cpu().numpy(), W[n][1])
+    xq, xs = oracle.quantize_rows_e4m3(oracle.widen_bf16(f["x"]))
+    tor, off = f["dp"]["token_of_row"], f["rt"]["offsets"]
+    h = oracle.grouped_gemm_swiglu_fp8(xq[tor], xs[tor], W["Wg"][0], W["Wg"][1], W["Wu"][0], W["Wu"][1], off,
+                                       remap)
+    hq, hs = oracle.quantize_rows_e4m3(rne_bf16(h))
+    yp = oracle.grouped_gemm_down_fp8(hq, hs, W["Wd"][0], W["Wd"][1], off, remap)
+    y_ref = oracle.combine(rne_bf16(yp), f["rt"]["topk_w"], f["dp"]["row_of_slot"])
+    assert_close(y[toks], y_ref, "y (fp8, sampled tokens)")

@@ -2,17 +2,21 @@
 768, 128 experts, top-8), run the way bench.py runs them (MoELayer over the
 C ABI).  Routing, counts, offsets and the permutation are compared bit for
 bit over every token; floating-point outputs are compared on samples the
-oracle can afford: whole per-token chains for sampled tokens (a token's
-routing, rows, output and dX depend on that token alone), and whole weight
-gradients of sampled experts with the GPU's stored bf16 operands fed to the
-oracle."""
+oracle can afford, always computed by the oracle from the seeded inputs
+alone (no value the GPU computed is fed to it): whole per-token chains for
+sampled tokens (a token's routing, rows, output and dX depend on that token
+alone), sampled permuted rows, the whole backward of sampled experts (the
+oracle recomputes every row routed to the expert), and the router weight
+gradient over the whole matrix from a second backward pass whose dY is zero
+outside a token sample (so every contribution comes from tokens the oracle
+evaluates)."""
 import numpy as np
 import pytest
 import torch
 
 import moe_expert_layer_topk_gb300 as m
 import oracle
-from gpu_util import assert_close, bits, f32, oracle_backward, oracle_chain, to_dev
+from gpu_util import assert_close, bits, oracle_backward, oracle_chain, to_dev
 from moe_expert_layer_topk_gb300.synth import CONFIGS, bf16_bits, make_layer_inputs, make_segment_inputs
 
 pytestmark = pytest.mark.gpu
@@ -26,14 +30,14 @@ def subset(inp, toks):
     return sub
 
 
-def rows_check(L, inp, rows, experts):
-    """h and y_perm of chosen rows: the GPU's stored operands through the oracle."""
+def rows_check(L, inp, token_of_row, rows, experts):
+    """h and y_perm of chosen permuted rows, the oracle chained on its own h."""
     so = np.arange(len(rows) + 1, dtype=np.int32)
     se = np.asarray(experts, np.int32)
-    xp = f32(L.x_perm[rows])
+    xp = oracle.widen_bf16(bits(inp["x"][token_of_row[rows]]))
     h = oracle.grouped_gemm_swiglu(xp, bits(inp["Wg"]), bits(inp["Wu"]), so, se)
     assert_close(L.h[rows], h, "h (sampled rows)")
-    y = oracle.grouped_gemm_down(f32(L.h[rows]), bits(inp["Wd"]), so, se)
+    y = oracle.grouped_gemm_down(h, bits(inp["Wd"]), so, se)
     assert_close(L.y_perm[rows], y, "y_perm (sampled rows)")
 
 
@@ -67,6 +71,7 @@ def check_routing_and_dispatch(L, inp):
     xp = L.x_perm.view(torch.int16)
     xg = inp["x"].view(torch.int16).to(xp.device)
     assert torch.equal(xp, xg[L.token_of_row.long()])
+    rt["token_of_row"] = dp["token_of_row"]
     return rt
 
 
@@ -88,7 +93,7 @@ def test_qwen3_fwd_T4096():
     rt = check_routing_and_dispatch(L, inp)
     rng = np.random.default_rng(0)
     rows, experts = sample_rows(rt["offsets"], rng, 12)
-    rows_check(L, inp, rows, experts)
+    rows_check(L, inp, rt["token_of_row"], rows, experts)
     toks = sorted(rng.choice(shape.T, 6, replace=False).tolist())
     f = oracle_chain(subset(inp, toks))
     assert_close(L.y[toks], f["y"], "y (sampled tokens, oracle chain)")
@@ -105,7 +110,7 @@ def test_qwen3_zipf_T16384_empty_experts():
     top = int(np.argmax(counts))
     rows += [int(rt["offsets"][top]) + 129, int(rt["offsets"][top + 1]) - 1]
     experts += [top, top]
-    rows_check(L, inp, rows, experts)
+    rows_check(L, inp, rt["token_of_row"], rows, experts)
     toks = sorted(rng.choice(shape.T, 4, replace=False).tolist())
     f = oracle_chain(subset(inp, toks))
     assert_close(L.y[toks], f["y"], "y (sampled tokens, oracle chain)")
@@ -139,35 +144,65 @@ def test_ep_rank_local_segments():
     href = oracle.grouped_gemm_swiglu(oracle.widen_bf16(bf16_bits(s["x_perm"][rows])), bf16_bits(s["Wg"]),
                                       bf16_bits(s["Wu"]), so2, se2)
     assert_close(h[rows], href, "h (sampled rows)")
-    yref = oracle.grouped_gemm_down(f32(h[rows]), bf16_bits(s["Wd"]), so2, se2)
+    yref = oracle.grouped_gemm_down(href, bf16_bits(s["Wd"]), so2, se2)
     assert_close(y[rows], yref, "y_perm (sampled rows)")
+
+
+def expert_backward_oracle(inp, rt, e):
+    """The oracle's forward and backward over every row routed to expert e,
+    from the seeded inputs: returns its rows [a, b) and h, dgu, dx_perm,
+    dW_down, dW_gate, dW_up of that expert."""
+    a, b = int(rt["offsets"][e]), int(rt["offsets"][e + 1])
+    tok = rt["token_of_row"][a:b]
+    slot = np.argmax(rt["topk_idx"][tok] == e, axis=1)
+    n = b - a
+    so = np.array([0, n], np.int32)
+    xe = oracle.widen_bf16(bits(inp["x"][tok]))
+    Wg, Wu, Wd = (bits(inp[w][e:e + 1]) for w in ("Wg", "Wu", "Wd"))
+    h, gu = oracle.grouped_gemm_swiglu(xe, Wg, Wu, so, save_gu=True)
+    # dy_perm[row] = topk_w[t, j] * dy[t]: combine backward with one slot per row
+    dye = oracle.widen_bf16(bits(inp["dy"][tok]))
+    w = rt["topk_w"][tok, slot][:, None]
+    dyp, _ = oracle.combine_bwd(dye, np.zeros((n, dye.shape[1]), np.float32), w,
+                                np.arange(n, dtype=np.int32)[:, None])
+    dgu, dWd = oracle.grouped_gemm_down_bwd(dyp, h, gu, Wd, so)
+    dxp, dWg, dWu = oracle.grouped_gemm_swiglu_bwd(dgu, xe, Wg, Wu, so)
+    return a, b, dict(h=h, dgu=dgu, dx_perm=dxp, dWd=dWd[0], dWg=dWg[0], dWu=dWu[0])
 
 
 def test_qwen3_fwd_bwd_T8192():
     shape, inp, g, L = run_fwd("qwen3_30b_fwd_bwd", with_bwd=True)
     rt = check_routing_and_dispatch(L, inp)
-    offs = rt["offsets"]
     rng = np.random.default_rng(3)
-    # whole weight gradients of two experts, GPU bf16 operands through the oracle
+    # the whole backward of two experts (every row routed to them)
     for e in rng.choice(shape.E, 2, replace=False):
-        a, b = int(offs[e]), int(offs[e + 1])
-        so = np.array([0, b - a], np.int32)
-        _, dWd = oracle.grouped_gemm_down_bwd(f32(L.dy_perm[a:b]), f32(L.h[a:b]), f32(L.gu[a:b]),
-                                              bits(inp["Wd"][e:e + 1]), so)
-        assert_close(L.dWd[e], dWd[0], f"dWd[{e}]")
-        _, dWg, dWu = oracle.grouped_gemm_swiglu_bwd(f32(L.dgu[a:b]), f32(L.x_perm[a:b]),
-                                                     bits(inp["Wg"][e:e + 1]), bits(inp["Wu"][e:e + 1]), so)
-        assert_close(L.dWg[e], dWg[0], f"dWg[{e}]")
-        assert_close(L.dWu[e], dWu[0], f"dWu[{e}]")
-    # router weight gradient over all tokens from the GPU's d_w and dx_acc
-    dWr, _ = oracle.route_topk_bwd(f32(L.d_w), f32(L.topk_w), rt["topk_idx"], bits(inp["x"]),
-                                   inp["Wr"].numpy(), np.zeros((shape.T, shape.H), np.float32))
-    assert_close(L.dWr, dWr, "dWr", max_frac=1e-3, rel=1e-4)
+        a, b, ref = expert_backward_oracle(inp, rt, int(e))
+        assert_close(L.h[a:b], ref["h"], f"h rows of expert {e}")
+        assert_close(L.dgu[a:b], ref["dgu"], f"dgu rows of expert {e}")
+        assert_close(L.dx_perm[a:b], ref["dx_perm"], f"dx_perm rows of expert {e}")
+        for n in ("dWd", "dWg", "dWu"):
+            assert_close(getattr(L, n)[e], ref[n], f"{n}[{e}]")
     # whole chains (forward and backward) of sampled tokens
     toks = sorted(rng.choice(shape.T, 4, replace=False).tolist())
     sub = subset(inp, toks)
     f = oracle_chain(sub)
-    b = oracle_backward(sub, f)
+    bw = oracle_backward(sub, f)
     assert_close(L.y[toks], f["y"], "y (sampled tokens)")
-    assert_close(L.dx[toks], b["dx"], "dx (sampled tokens)")
-    assert_close(L.d_w[toks], b["d_w"], "d_w (sampled tokens)")
+    assert_close(L.dx[toks], bw["dx"], "dx (sampled tokens)")
+    assert_close(L.d_w[toks], bw["d_w"], "d_w (sampled tokens)")
+    # second backward, dY zero outside the sample: dWr over the whole
+    # matrix, and every weight gradient, come from the sampled tokens alone
+    dy_sparse = torch.zeros_like(g["dy"])
+    dy_sparse[toks] = g["dy"][toks]
+    L.backward(dy_sparse, g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"])
+    torch.cuda.synchronize()
+    assert m.moe_read_device_status(reset=True) == 0
+    assert_close(L.dWr, bw["dWr"], "dWr (sparse dY)")
+    assert_close(L.dx[toks], bw["dx"], "dx (sparse dY)")
+    touched = sorted(set(f["rt"]["topk_idx"].reshape(-1).tolist()))
+    for n in ("dWd", "dWg", "dWu"):
+        assert_close(getattr(L, n)[touched], bw[n][touched], f"{n} of the sampled tokens' experts (sparse dY)")
+    others = torch.ones(shape.E, dtype=torch.bool, device=L.dWd.device)
+    others[touched] = False
+    for n in ("dWd", "dWg", "dWu"):
+        assert getattr(L, n)[others].abs().max().item() == 0.0, n

@@ -94,7 +94,8 @@ def test_gather_segments_and_arbitrary_rows():
     torch.cuda.synchronize()
     assert m.moe_read_device_status(reset=True) == 0
     assert torch.equal(h, h_ref)
-    href = oracle.grouped_gemm_swiglu(oracle.widen_bf16(bits(xp.cpu())), bits(Wg.cpu()), bits(Wu.cpu()),
+    x_host = x.cpu()[tor.cpu().long()]  # the seeded rows, gathered on the host
+    href = oracle.grouped_gemm_swiglu(oracle.widen_bf16(bits(x_host)), bits(Wg.cpu()), bits(Wu.cpu()),
                                       so.cpu().numpy(), se.cpu().numpy())
     assert_close(h, href, "h")
 

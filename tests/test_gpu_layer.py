@@ -5,8 +5,12 @@ Shapes are chosen so that every kernel runs several tiles with ragged tails:
 gate/up tile widths (I % 128 == 0 -> 128-wide g and u halves, else 64), all
 three down-projection tile widths (H % 256, % 128, % 64), several ranking
 chunks, and both router variants (E % 8 == 0 vectorised, else scalar).
-Each stage is checked on its own by feeding the GPU's stored inputs (bf16)
-to the oracle, and the chain is checked against the oracle's fp32 chain.
+Every stored tensor of the layer (routing, permutation, h, g|u, y_perm, y,
+dy_perm, d_w, dgu, dx_perm, dx_acc, dX and the weight gradients) is compared
+with the same tensor of the oracle's own fp32 chain, run on the seeded
+inputs alone: no value the GPU computed is ever fed to the oracle.  The
+oracle keeps its intermediates in fp32 where the layer stores bf16; the
+acceptance bars cover that.
 """
 import numpy as np
 import pytest
@@ -14,7 +18,7 @@ import torch
 
 import moe_expert_layer_topk_gb300 as m
 import oracle
-from gpu_util import assert_close, bits, f32, inputs, oracle_backward, oracle_chain, to_dev
+from gpu_util import assert_close, bits, inputs, oracle_backward, oracle_chain, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -44,7 +48,8 @@ def run(request):
     torch.cuda.synchronize()
     status = m.moe_read_device_status(reset=True)
     f = oracle_chain(inp)
-    return dict(inp=inp, g=g, layer=layer, f=f, status=status, case=request.param)
+    b = oracle_backward(inp, f)
+    return dict(inp=inp, g=g, layer=layer, f=f, b=b, status=status, case=request.param)
 
 
 def test_no_device_status(run):
@@ -68,23 +73,13 @@ def test_dispatch_bit_exact(run):
 
 
 def test_gate_up_swiglu(run):
-    L, f, inp = run["layer"], run["f"], run["inp"]
-    h, gu = oracle.grouped_gemm_swiglu(f32(L.x_perm), bits(inp["Wg"]), bits(inp["Wu"]),
-                                       f["rt"]["offsets"], save_gu=True)
-    assert_close(L.h, h, "h")
-    assert_close(L.gu, gu, "gu")
+    L, f = run["layer"], run["f"]
+    assert_close(L.h, f["h"], "h")
+    assert_close(L.gu, f["gu"], "gu")
 
 
 def test_down(run):
-    L, f, inp = run["layer"], run["f"], run["inp"]
-    y_perm = oracle.grouped_gemm_down(f32(L.h), bits(inp["Wd"]), f["rt"]["offsets"])
-    assert_close(L.y_perm, y_perm, "y_perm")
-
-
-def test_combine(run):
-    L, f = run["layer"], run["f"]
-    y = oracle.combine(f32(L.y_perm), f32(L.topk_w), f["dp"]["row_of_slot"])
-    assert_close(L.y, y, "y (isolated)")
+    assert_close(run["layer"].y_perm, run["f"]["y_perm"], "y_perm")
 
 
 def test_forward_chain(run):
@@ -92,49 +87,32 @@ def test_forward_chain(run):
 
 
 def test_combine_bwd(run):
-    L, f, inp = run["layer"], run["f"], run["inp"]
-    dy = f32(inp["dy"])
-    dyp, dw = oracle.combine_bwd(dy, f32(L.y_perm), f32(L.topk_w), f["dp"]["row_of_slot"])
-    assert_close(L.dy_perm, dyp, "dy_perm")
-    assert_close(L.d_w, dw, "d_w")
+    L, b = run["layer"], run["b"]
+    assert_close(L.dy_perm, b["dy_perm"], "dy_perm")
+    assert_close(L.d_w, b["d_w"], "d_w")
 
 
 def test_down_bwd(run):
-    L, f, inp = run["layer"], run["f"], run["inp"]
-    dgu, dWd = oracle.grouped_gemm_down_bwd(f32(L.dy_perm), f32(L.h), f32(L.gu), bits(inp["Wd"]),
-                                            f["rt"]["offsets"])
-    assert_close(L.dgu, dgu, "dgu")
-    assert_close(L.dWd, dWd, "dWd")
+    L, b = run["layer"], run["b"]
+    assert_close(L.dgu, b["dgu"], "dgu")
+    assert_close(L.dWd, b["dWd"], "dWd")
 
 
 def test_gate_up_bwd(run):
-    L, f, inp = run["layer"], run["f"], run["inp"]
-    dxp, dWg, dWu = oracle.grouped_gemm_swiglu_bwd(f32(L.dgu), f32(L.x_perm), bits(inp["Wg"]),
-                                                   bits(inp["Wu"]), f["rt"]["offsets"])
-    assert_close(L.dx_perm, dxp, "dx_perm")
-    assert_close(L.dWg, dWg, "dWg")
-    assert_close(L.dWu, dWu, "dWu")
+    L, b = run["layer"], run["b"]
+    assert_close(L.dx_perm, b["dx_perm"], "dx_perm")
+    assert_close(L.dWg, b["dWg"], "dWg")
+    assert_close(L.dWu, b["dWu"], "dWu")
 
 
 def test_dispatch_bwd(run):
-    L, f = run["layer"], run["f"]
-    dxa = oracle.dispatch_bwd(f32(L.dx_perm), f["dp"]["row_of_slot"])
-    assert_close(L.dx_acc, dxa, "dx_acc", max_frac=1e-6, rel=1e-6)
+    assert_close(run["layer"].dx_acc, run["b"]["dx_acc"], "dx_acc")
 
 
 def test_router_bwd(run):
-    L, f = run["layer"], run["f"]
-    dWr, dx = oracle.route_topk_bwd(f32(L.d_w), f32(L.topk_w), f["rt"]["topk_idx"], f["x"], f["Wr"],
-                                    f32(L.dx_acc))
-    assert_close(L.dWr, dWr, "dWr", max_frac=1e-3, rel=1e-4)
-    assert_close(L.dx, dx, "dx (isolated)")
-
-
-def test_backward_chain(run):
-    L = run["layer"]
-    b = oracle_backward(run["inp"], run["f"])
-    for name in ("dx", "dWg", "dWu", "dWd", "dWr"):
-        assert_close(getattr(L, name), b[name], f"{name} (chain)")
+    L, b = run["layer"], run["b"]
+    assert_close(L.dWr, b["dWr"], "dWr")
+    assert_close(L.dx, b["dx"], "dx (chain)")
 
 
 def test_deterministic(run):
