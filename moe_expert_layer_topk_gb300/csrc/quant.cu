@@ -13,6 +13,8 @@
 // with shuffles, then writes the codes with 8-byte stores and the scale.
 #include <cuda_fp8.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace {
@@ -44,37 +46,55 @@ __device__ __forceinline__ uint2 codes8(uint4 v, float s) {
   return make_uint2(out[0], out[1]);
 }
 
-// NC: 16-byte vectors (8 bf16 each) a lane holds in registers.
+// Blocks per SM each quantiser instantiation is compiled for.
+__host__ __device__ constexpr int quant_blocks_per_sm(int nc) { return nc <= 1 ? 6 : (nc <= 3 ? 4 : (nc <= 4 ? 3 : 2)); }
+
+// NC: 16-byte vectors (8 bf16 each) a lane holds in registers per row.  The
+// grid holds what is resident at once; each warp walks rows
+// warp, warp + W, warp + 2W, ... (W warps in the grid) and loads its next
+// row while it reduces and converts the current one.
 template <int NC>
-__global__ void __launch_bounds__(32 * kQuantWarps, NC <= 1 ? 6 : (NC <= 4 ? 4 : 2))
+__global__ void __launch_bounds__(32 * kQuantWarps, quant_blocks_per_sm(NC))
     quantize_rows_e4m3_kernel(const __nv_bfloat16* __restrict__ a, int rows, int cols,
                               uint8_t* __restrict__ q, float* __restrict__ scale) {
   moe::pdl_wait();
   moe::pdl_trigger();
-  const int row = blockIdx.x * kQuantWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const uint4* src = reinterpret_cast<const uint4*>(a + (size_t)row * cols);
-  uint2* dst = reinterpret_cast<uint2*>(q + (size_t)row * cols);
+  const int lane = threadIdx.x & 31;
+  const int stride = gridDim.x * kQuantWarps;
   const int nv = cols / 8;
-  uint4 cache[NC];
-  float m = 0.0f;
+  auto load = [&](int row, uint4 (&c)[NC]) {
+    const uint4* src = reinterpret_cast<const uint4*>(a + (size_t)row * cols);
 #pragma unroll
-  for (int i = 0; i < NC; ++i) {
-    const int v = lane + 32 * i;
-    cache[i] = v < nv ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
-    m = amax8(cache[i], m);
+    for (int i = 0; i < NC; ++i) {
+      const int v = lane + 32 * i;
+      c[i] = v < nv ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  int row = blockIdx.x * kQuantWarps + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  uint4 cur[NC], nxt[NC];
+  load(row, cur);
+  for (; row < rows; row += stride) {
+    if (row + stride < rows) load(row + stride, nxt);
+    const uint4* src = reinterpret_cast<const uint4*>(a + (size_t)row * cols);
+    uint2* dst = reinterpret_cast<uint2*>(q + (size_t)row * cols);
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NC; ++i) m = amax8(cur[i], m);
+    for (int v = lane + 32 * NC; v < nv; v += 32) m = amax8(__ldg(src + v), m);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    const float s = m > 0.0f ? __fdiv_rn(m, 448.0f) : 1.0f;
+    if (lane == 0) scale[row] = s;
+#pragma unroll
+    for (int i = 0; i < NC; ++i) {
+      const int v = lane + 32 * i;
+      if (v < nv) dst[v] = codes8(cur[i], s);
+    }
+    for (int v = lane + 32 * NC; v < nv; v += 32) dst[v] = codes8(__ldg(src + v), s);
+#pragma unroll
+    for (int i = 0; i < NC; ++i) cur[i] = nxt[i];
   }
-  for (int v = lane + 32 * NC; v < nv; v += 32) m = amax8(__ldg(src + v), m);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-  const float s = m > 0.0f ? __fdiv_rn(m, 448.0f) : 1.0f;
-  if (lane == 0) scale[row] = s;
-#pragma unroll
-  for (int i = 0; i < NC; ++i) {
-    const int v = lane + 32 * i;
-    if (v < nv) dst[v] = codes8(cache[i], s);
-  }
-  for (int v = lane + 32 * NC; v < nv; v += 32) dst[v] = codes8(__ldg(src + v), s);
 }
 
 }  // namespace
@@ -90,13 +110,16 @@ extern "C" int moe_quantize_rows_e4m3(const void* a, int rows, int cols, void* q
   if (!a || !q || !scale) return moe::fail(MOE_ERR_INVALID_ARG, "%s: NULL pointer argument", fn);
   if (!moe::aligned16(a) || (reinterpret_cast<uintptr_t>(q) & 7u) || (reinterpret_cast<uintptr_t>(scale) & 3u))
     return moe::fail(MOE_ERR_ALIGNMENT, "%s: a must be 16-byte, q 8-byte, scale 4-byte aligned", fn);
-  const int blocks = (rows + kQuantWarps - 1) / kQuantWarps;
   const int per_lane = (cols / 8 + 31) / 32;  // 16-byte vectors per lane
-  auto kernel = per_lane <= 1   ? quantize_rows_e4m3_kernel<1>
-                : per_lane <= 2 ? quantize_rows_e4m3_kernel<2>
-                : per_lane <= 3 ? quantize_rows_e4m3_kernel<3>
-                : per_lane <= 4 ? quantize_rows_e4m3_kernel<4>
-                                : quantize_rows_e4m3_kernel<8>;
+  const int nc = per_lane <= 1 ? 1 : per_lane <= 2 ? 2 : per_lane <= 3 ? 3 : per_lane <= 4 ? 4 : 8;
+  auto kernel = nc == 1   ? quantize_rows_e4m3_kernel<1>
+                : nc == 2 ? quantize_rows_e4m3_kernel<2>
+                : nc == 3 ? quantize_rows_e4m3_kernel<3>
+                : nc == 4 ? quantize_rows_e4m3_kernel<4>
+                          : quantize_rows_e4m3_kernel<8>;
+  // one resident wave of blocks (each warp then walks several rows)
+  const int sms = moe::sm_count() > 0 ? moe::sm_count() : 148;
+  const int blocks = std::min((rows + kQuantWarps - 1) / kQuantWarps, sms * quant_blocks_per_sm(nc));
   cudaError_t e = moe::launch_pdl(kernel, dim3(blocks), dim3(32 * kQuantWarps), 0,
                                   static_cast<cudaStream_t>(stream),
                                   static_cast<const __nv_bfloat16*>(a), rows, cols,
