@@ -30,14 +30,15 @@
 //   warps 2..   epilogue: TMEM -> registers -> global (warp w reads TMEM
 //               lanes 32*(w%4)..+31, i.e. accumulator rows); four warps, or
 //               eight (two per lane quadrant, half the columns each) for the
-//               weight-gradient and SwiGLU-backward kinds
+//               weight-gradient, SwiGLU-backward and down-projection kinds
 //   last 4      row-gathering kinds only: they and warp 0 copy the A rows
 //               from x by token id with cp.async
 // Tile: 128 rows x BN columns (BN <= 256), k-block of one 128-byte swizzle
-// row (64 bf16 or 128 e4m3 elements), 4-stage shared-memory ring (3 for the router dX kind, whose
-// epilogue stages its addend), two 256-column accumulators in TMEM so the
-// epilogue of tile i overlaps the MMAs of tile i+1.  GATE_UP_BWD_DX runs as
-// cluster pairs (tcgen05 cta_group::2, 256-row tiles).
+// row (64 bf16 or 128 e4m3 elements), 4-stage shared-memory ring (3 for the
+// router dX kind, whose epilogue stages its addend), two 256-column
+// accumulators in TMEM so the epilogue of tile i overlaps the MMAs of tile
+// i+1.  GATE_UP_BWD_DX runs as cluster pairs (tcgen05 cta_group::2, 256-row
+// tiles).
 //
 // Every wait on an mbarrier is bounded (globaltimer): on timeout the CTA
 // records MOE_STATUS_TIMEOUT, all roles leave their loops, outstanding MMAs
