@@ -254,3 +254,45 @@ def test_fp8_layer_full_size_sampled_tokens():
     yp = oracle.grouped_gemm_down_fp8(hq, hs, W["Wd"][0], W["Wd"][1], off, remap)
     y_ref = oracle.combine(rne_bf16(yp), f["rt"]["topk_w"], f["dp"]["row_of_slot"])
     assert_close(y[toks], y_ref, "y (fp8, sampled tokens)")
+
+
+def test_fp8_ep_rank_local_segments_full_size():
+    """One EP rank's local expert compute in e4m3 at full size (32768 received
+    rows, 16 local experts, 128 source-rank x expert segments): the received
+    rows and the weights quantised on the GPU, both GEMMs over the segment
+    table, sampled rows against the oracle's fp8 chain on the same seeded
+    data (its own codes, its h rounded to bf16 and quantised)."""
+    from moe_expert_layer_topk_gb300.synth import CONFIGS, make_segment_inputs
+    shape = CONFIGS["ep_rank_local"]
+    s = make_segment_inputs(shape, 0)
+    R, H, I, E, nseg = s["R"], s["H"], s["I"], s["E"], s["num_seg"]
+    xp = s["x_perm"].cuda()
+    xq, xs = _quant_gpu(xp)
+    L = m.MoELayer(1, H, I, E, 1, 1, training=False, fp8=True)
+    w8 = L.quantize_weights(s["Wg"].cuda(), s["Wu"].cuda(), s["Wd"].cuda())
+    so, se = s["seg_offsets"].cuda(), s["seg_expert"].cuda()
+    h = torch.empty(R, I, dtype=torch.bfloat16, device="cuda")
+    m.moe_grouped_gemm_swiglu_fp8(xq, xs, None, 0, w8["Wg"], w8["Wg_scale"], w8["Wu"], w8["Wu_scale"], nseg,
+                                  so, se, R, H, I, E, h)
+    hq, hs = _quant_gpu(h)
+    y = torch.empty(R, H, dtype=torch.bfloat16, device="cuda")
+    m.moe_grouped_gemm_down_fp8(hq, hs, w8["Wd"], w8["Wd_scale"], nseg, so, se, R, H, I, E, y)
+    torch.cuda.synchronize()
+    assert m.moe_read_device_status(reset=True) == 0
+    son, sen = s["seg_offsets"].numpy(), s["seg_expert"].numpy()
+    rng = np.random.default_rng(9)
+    rows, experts = [], []
+    for q in rng.choice(nseg, 10, replace=False):
+        a, b = int(son[q]), int(son[q + 1])
+        for r in sorted({a, b - 1} if b > a else set()):
+            rows.append(r)
+            experts.append(int(sen[q]))
+    so2 = np.arange(len(rows) + 1, dtype=np.int32)
+    se2 = np.asarray(experts, np.int32)
+    aq, as_ = oracle.quantize_rows_e4m3(oracle.widen_bf16(bits(s["x_perm"][rows])))
+    W = {n: oracle.quantize_rows_e4m3(oracle.widen_bf16(bits(s[n]))) for n in ("Wg", "Wu", "Wd")}
+    href = oracle.grouped_gemm_swiglu_fp8(aq, as_, W["Wg"][0], W["Wg"][1], W["Wu"][0], W["Wu"][1], so2, se2)
+    assert_close(h[rows], href, "h (fp8, sampled rows)")
+    hq_o, hs_o = oracle.quantize_rows_e4m3(rne_bf16(href))
+    yref = oracle.grouped_gemm_down_fp8(hq_o, hs_o, W["Wd"][0], W["Wd"][1], so2, se2)
+    assert_close(y[rows], yref, "y_perm (fp8, sampled rows)")
