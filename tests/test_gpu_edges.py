@@ -1,5 +1,5 @@
 """Edge cases of the CUDA path against the CPU oracle: one token, one expert
-(a plain SwiGLU MLP), k = E, empty experts, every token on one expert,
+(a plain SwiGLU MLP), logit ties, k = E, empty experts, every token on one expert,
 segmented (source-rank x expert) row layouts, gradient accumulation, and the
 device status word for bad index data (kernels skip the bad entries)."""
 import numpy as np
@@ -52,6 +52,33 @@ def test_one_expert_is_a_dense_swiglu_mlp():
     x = g["x"].float()
     ref = (F.silu(x @ g["Wg"][0].float().T) * (x @ g["Wu"][0].float().T)) @ g["Wd"][0].float().T
     assert_close(L.y, ref.cpu().numpy(), "y vs torch fp32 MLP")
+
+
+def test_router_ties():
+    """Equal logits go to the lower expert id: duplicated router columns
+    (experts 5 = 2 and 6 = 1), zeroed columns (experts 0, 3, 7: logit 0 for
+    every token) and all-zero tokens (every logit 0, so experts 0..k-1 in
+    order, with equal weights)."""
+    inp = inputs(160, 256, 64, 8, 3, seed=21, ep=2, router_std=0.05)
+    Wr = inp["Wr"].clone()
+    Wr[:, 5] = Wr[:, 2]
+    Wr[:, 6] = Wr[:, 1]
+    Wr[:, [0, 3, 7]] = 0.0
+    inp["Wr"] = Wr
+    x = inp["x"].clone()
+    x[[4, 77, 159]] = 0.0
+    inp["x"] = x
+    L, _ = run_layer(inp)
+    f, _ = check_all(L, inp)
+    idx = L.topk_idx.cpu().numpy()
+    for t in (4, 77, 159):
+        assert idx[t].tolist() == [0, 1, 2]
+        assert torch.all(L.topk_w[t] == L.topk_w[t, 0])
+    # a tie inside the selection picks the lower id first
+    ties = (idx[:, :, None] == np.array([2, 5])).any(1).all(1)
+    for t in np.nonzero(ties)[0]:
+        row = idx[t].tolist()
+        assert row.index(2) < row.index(5)
 
 
 def test_k_equals_E():

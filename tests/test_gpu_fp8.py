@@ -212,6 +212,11 @@ def test_fp8_layer_forward(T, H, I, E, k, ep):
     assert_close(y, y8_ref, "y (fp8 layer vs fp8 oracle)")
     # format check: the e4m3 forward stays within e4m3's error of the bf16 layer
     assert_close(y, f["y"], "y (fp8 layer vs bf16 oracle)", max_frac=0.25, rel=0.1)
+    # deterministic: a second forward gives the same bits
+    y1 = y.clone()
+    y2 = L.forward(g["x"], g["Wr"], g["bias"], w8, None, None)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
 
 
 def test_fp8_layer_full_size_sampled_tokens():
