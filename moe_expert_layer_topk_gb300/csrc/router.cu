@@ -172,8 +172,15 @@ constexpr int kTopkTokPerBlock = kTopkWarps * kTopkTokPerWarp;
 template <int kNQ>
 __host__ __device__ constexpr int sum_batch() { return kNQ >= 32 ? 1 : (kNQ >= 16 ? 2 : (kNQ >= 8 ? 4 : 8)); }
 
-__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
+// Order-preserving map of a logit to an unsigned key (larger float, larger
+// key; the two zeros map to one key, as they compare equal); 0 is below
+// every key and marks "no candidate".
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t b = f == 0.f ? 0u : __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t u) {
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
 }
 
 template <int kNQ>
@@ -220,31 +227,28 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
 #pragma unroll
     for (int q = 0; q < kNQ; ++q)
       if (lane + 32 * q >= E) taken |= 1u << q;  // padding never wins
+    uint32_t key[kNQ];
+#pragma unroll
+    for (int q = 0; q < kNQ; ++q) key[q] = order_key(v[q]);
     float my_v = 0.f;
     int my_i = 0;
+    // round j: the largest logit left, equal logits to the lower expert id
+    // (a lane's own candidates in increasing id, then the warp's largest key
+    // and the lowest id holding it)
     for (int j = 0; j < k; ++j) {
-      float bv = 0.f;
-      int bi = INT_MAX;
+      uint32_t lk = 0;
+      int li = INT_MAX;
 #pragma unroll
-      for (int q = 0; q < kNQ; ++q) {
-        const int e = lane + 32 * q;
-        if (!((taken >> q) & 1u) && (bi == INT_MAX || better(v[q], e, bv, bi))) {
-          bv = v[q];
-          bi = e;
+      for (int q = 0; q < kNQ; ++q)
+        if (!((taken >> q) & 1u) && key[q] > lk) {
+          lk = key[q];
+          li = lane + 32 * q;
         }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (oi != INT_MAX && (bi == INT_MAX || better(ov, oi, bv, bi))) {
-          bv = ov;
-          bi = oi;
-        }
-      }
+      const uint32_t mk = __reduce_max_sync(0xffffffffu, lk);
+      const int bi = __reduce_min_sync(0xffffffffu, lk == mk ? li : INT_MAX);
       if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
       if (lane == j) {
-        my_v = bv;
+        my_v = key_value(mk);
         my_i = bi;
       }
     }
