@@ -113,7 +113,8 @@ int moe_read_device_status(int* status, int reset, void* stream);
  * Outputs: topk_idx int32 [T,k], topk_w fp32 [T,k], counts int32 [E],
  * offsets int32 [E+1], rank_offsets int32 [ep_size+1].
  * No capacity limit: every token keeps all k experts.  T == 0 is allowed.
- * The workspace holds the fp32 block sums of the logits, ceil(H/256) x T x E.
+ * The workspace holds the fp32 block sums of the logits, ceil(H/256) x T x E,
+ * and one 128-byte slot-counter line per expert.
  * ---------------------------------------------------------------------- */
 size_t moe_route_topk_workspace_size(int T, int H, int E);
 int moe_route_topk(const void* x, const float* Wr, const float* bias, int T, int H, int E, int k,

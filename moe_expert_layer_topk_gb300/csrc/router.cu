@@ -164,7 +164,10 @@ __global__ void __launch_bounds__(kLogitThreads) router_partials_kernel(
 // holds experts l, l+32, ...; kNQ registers per lane) from the h-block
 // partials, added left to right, bias last; k rounds of a warp-wide arg-max
 // over (logit descending, id ascending) pick the slots in order.  Slot
-// counts go to counts[] with integer atomics (order-independent).
+// counts go to a per-expert counter with integer atomics (order-independent);
+// each expert's counter sits on its own 128-byte line of the workspace, so
+// the T*k atomics do not queue on the few lines that counts[] spans.
+constexpr int kCountPad = 32;  // ints per expert counter line (128 bytes)
 constexpr int kTopkWarps = 8;
 constexpr int kTopkTokPerWarp = 2;
 constexpr int kTopkTokPerBlock = kTopkWarps * kTopkTokPerWarp;
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
     if (lane < k) {
       topk_idx[(size_t)t * k + lane] = my_i;
       topk_w[(size_t)t * k + lane] = __fdiv_rn(ex, s);
-      atomicAdd(counts + my_i, 1);
+      atomicAdd(counts + (size_t)my_i * kCountPad, 1);
     }
   }
 }
@@ -268,13 +271,15 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
 __global__ void zero_counts_kernel(int32_t* __restrict__ counts, int E) {
   pdl_wait();
   pdl_trigger();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = 0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) counts[(size_t)e * kCountPad] = 0;
 }
 
 // ------------------------------------------------------------ offsets kernel
-// One CTA: exclusive scan of counts -> offsets, EP-rank row ranges.
-__global__ void __launch_bounds__(1024) router_offsets_kernel(const int32_t* __restrict__ counts,
+// One CTA: the per-expert counters -> counts[], exclusive scan -> offsets,
+// EP-rank row ranges.
+__global__ void __launch_bounds__(1024) router_offsets_kernel(const int32_t* __restrict__ hist,
                                                               int E, int ep_size,
+                                                              int32_t* __restrict__ counts,
                                                               int32_t* __restrict__ offsets,
                                                               int32_t* __restrict__ rank_offsets) {
   pdl_wait();
@@ -282,7 +287,8 @@ __global__ void __launch_bounds__(1024) router_offsets_kernel(const int32_t* __r
   __shared__ int warp_sum[32];
   __shared__ int excl[kMaxExperts + 1];
   const int e = threadIdx.x;
-  const int c = e < E ? counts[e] : 0;
+  const int c = e < E ? hist[(size_t)e * kCountPad] : 0;
+  if (e < E) counts[e] = c;
   const int lane = e & 31, warp = e >> 5;
   int incl = c;
 #pragma unroll
@@ -418,10 +424,14 @@ __global__ void router_bwd_reduce_kernel(const float* __restrict__ P, int S, int
 
 size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
-// Route workspace: the h-block partials of the logits, fp32 [nblk_h][T][E].
-size_t route_ws_bytes(int T, int H, int E) {
+// Route workspace: the h-block partials of the logits, fp32 [nblk_h][T][E],
+// then one 128-byte counter line per expert.
+size_t route_part_bytes(int T, int H, int E) {
   const size_t nblk_h = (size_t)((H + kLogitBlockH - 1) / kLogitBlockH);
   return align256(sizeof(float) * nblk_h * (size_t)(T > 0 ? T : 1) * E);
+}
+size_t route_ws_bytes(int T, int H, int E) {
+  return route_part_bytes(T, H, E) + align256(sizeof(int32_t) * kCountPad * (size_t)E);
 }
 
 struct BwdLayout {
@@ -485,7 +495,8 @@ int moe_route_topk(const void* x, const float* Wr, const float* bias, int T, int
     return fail(MOE_ERR_WORKSPACE, "moe_route_topk: workspace %zu < %zu bytes", ws_bytes, need);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* part = static_cast<float*>(ws);
-  launch_pdl(zero_counts_kernel, 1, 256, 0, s, counts, E);
+  int32_t* hist = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + route_part_bytes(T, H, E));
+  launch_pdl(zero_counts_kernel, 1, 256, 0, s, hist, E);
   if (int rc = check_launch("moe_route_topk: zero counts")) return rc;
   if (T > 0) {
     static bool attr_set[64] = {};
@@ -512,20 +523,20 @@ int moe_route_topk(const void* x, const float* Wr, const float* bias, int T, int
     const int nblk = (T + kTopkTokPerBlock - 1) / kTopkTokPerBlock;
     const int nq = (E + 31) / 32;
     if (nq <= 1)
-      launch_pdl(router_topk_kernel<1>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
+      launch_pdl(router_topk_kernel<1>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, hist);
     else if (nq <= 2)
-      launch_pdl(router_topk_kernel<2>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
+      launch_pdl(router_topk_kernel<2>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, hist);
     else if (nq <= 4)
-      launch_pdl(router_topk_kernel<4>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
+      launch_pdl(router_topk_kernel<4>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, hist);
     else if (nq <= 8)
-      launch_pdl(router_topk_kernel<8>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
+      launch_pdl(router_topk_kernel<8>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, hist);
     else if (nq <= 16)
-      launch_pdl(router_topk_kernel<16>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
+      launch_pdl(router_topk_kernel<16>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, hist);
     else
-      launch_pdl(router_topk_kernel<32>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, counts);
+      launch_pdl(router_topk_kernel<32>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, hist);
     if (int rc = check_launch("moe_route_topk: top-k kernel")) return rc;
   }
-  launch_pdl(router_offsets_kernel, 1, 1024, 0, s, counts, E, ep_size, offsets, rank_offsets);
+  launch_pdl(router_offsets_kernel, 1, 1024, 0, s, hist, E, ep_size, counts, offsets, rank_offsets);
   return check_launch("moe_route_topk: offsets kernel");
 }
 
