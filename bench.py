@@ -314,10 +314,11 @@ def run_ours(args, shape, inp):
 
     # end to end through the public API with host buffers: every step copies
     # its x and dY from pinned host memory and reads its y and dX back.  The
-    # copies run on their own streams, pipelined over two input slots: the
+    # copies run on their own streams, pipelined over two slots: the
     # host-to-device copy of step i+1 and the device-to-host read of step i-1
-    # overlap step i's compute (its y and dX are first copied on the device
-    # into a per-slot staging buffer, inside the compute stream).
+    # overlap step i's compute, which writes its y and dX straight into the
+    # slot's output tensors (a slot is reused two steps later, after its
+    # read has finished).
     hx = inp["x"].pin_memory()
     hdy = inp["dy"].pin_memory()
     hy = torch.empty_like(inp["x"]).pin_memory()
@@ -341,10 +342,8 @@ def run_ours(args, shape, inp):
             dy_in[s].copy_(hdy, non_blocking=True)
             ev_in[s].record(h2d)
         stream.wait_event(ev_in[s])
-        layer.forward(x_in[s], g["Wr"], g["bias"], g["Wg"], g["Wu"], g["Wd"])
-        layer.backward(dy_in[s], x_in[s], g["Wr"], g["Wg"], g["Wu"], g["Wd"])
-        y_st[s].copy_(layer.y, non_blocking=True)
-        dx_st[s].copy_(layer.dx, non_blocking=True)
+        layer.forward(x_in[s], g["Wr"], g["bias"], g["Wg"], g["Wu"], g["Wd"], y=y_st[s])
+        layer.backward(dy_in[s], x_in[s], g["Wr"], g["Wg"], g["Wu"], g["Wd"], dx=dx_st[s])
         ev_done[s].record(stream)
         with torch.cuda.stream(d2h):
             d2h.wait_event(ev_done[s])

@@ -127,20 +127,23 @@ class MoELayer:
         moe_grouped_gemm_down(self.h, Wd, self.E, self.offsets, None, self.R, self.H, self.I,
                               self.E, self.y_perm, None, stream)
 
-    def combine(self, stream=None):
-        moe_combine(self.y_perm, self.topk_w, self.row_of_slot, self.T, self.H, self.k, self.y,
-                    stream)
+    def combine(self, stream=None, y=None):
+        moe_combine(self.y_perm, self.topk_w, self.row_of_slot, self.T, self.H, self.k,
+                    self.y if y is None else y, stream)
 
-    def forward(self, x, Wr, bias, Wg, Wu, Wd, stream=None):
+    def forward(self, x, Wr, bias, Wg, Wu, Wd, stream=None, y=None):
+        """y: optional bf16 [T,H] output tensor (default: the layer's own)."""
         self.route(x, Wr, bias, stream)
         self.dispatch(x, stream)
         self.experts(Wg, Wu, Wd, stream)
-        self.combine(stream)
-        return self.y
+        self.combine(stream, y)
+        return self.y if y is None else y
 
     # --------------------------------------------------------------- backward
-    def backward(self, dy, x, Wr, Wg, Wu, Wd, accumulate: bool = False, stream=None):
+    def backward(self, dy, x, Wr, Wg, Wu, Wd, accumulate: bool = False, stream=None, dx=None):
+        """dx: optional bf16 [T,H] output tensor (default: the layer's own)."""
         assert self.training, "layer was built without backward buffers"
+        dx = self.dx if dx is None else dx
         T, H, I, E, k, R = self.T, self.H, self.I, self.E, self.k, self.R
         moe_combine_bwd(dy, self.y_perm, self.topk_w, self.row_of_slot, T, H, k, self.dy_perm,
                         self.d_w, stream)
@@ -151,5 +154,5 @@ class MoELayer:
                                     stream)
         moe_dispatch_bwd(self.dx_perm, self.row_of_slot, T, H, k, self.dx_acc, stream)
         moe_route_topk_bwd(self.d_w, self.topk_w, self.topk_idx, x, Wr, self.dx_acc, T, H, E, k,
-                           self.dWr, self.dx, accumulate, self.ws_route_bwd, stream)
-        return self.dx
+                           self.dWr, dx, accumulate, self.ws_route_bwd, stream)
+        return dx
