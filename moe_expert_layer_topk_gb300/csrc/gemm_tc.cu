@@ -37,8 +37,8 @@
 // row (64 bf16 or 128 e4m3 elements), 4-stage shared-memory ring (3 for the
 // router dX kind, whose epilogue stages its addend), two 256-column
 // accumulators in TMEM so the epilogue of tile i overlaps the MMAs of tile
-// i+1.  GATE_UP_BWD_DX runs as cluster pairs (tcgen05 cta_group::2, 256-row
-// tiles).
+// i+1.  GATE_UP_FWD and GATE_UP_BWD_DX run as cluster pairs (tcgen05
+// cta_group::2, 256-row tiles).
 //
 // Every wait on an mbarrier is bounded (globaltimer): on timeout the CTA
 // records MOE_STATUS_TIMEOUT, all roles leave their loops, outstanding MMAs
@@ -182,7 +182,7 @@ struct Cfg {
   // without the segment tables
   static constexpr size_t SMEM_FIXED = 1024 + (size_t)STAGES * STAGE_BYTES + EP_TOTAL + sizeof(Ctl);
 };
-// the configurations launched (cluster pairs only for GATE_UP_BWD_DX)
+// the configurations launched (cluster pairs for GATE_UP_FWD and GATE_UP_BWD_DX)
 static_assert(Cfg<GATE_UP_FWD, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<GATE_UP_GATHER, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<GATE_UP_FP8, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
@@ -192,6 +192,7 @@ static_assert(Cfg<GATE_UP_FWD, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<DOWN_BWD_DX, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<GATE_UP_BWD_DX, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<GATE_UP_BWD_DX, 2>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
+                  Cfg<GATE_UP_FWD, 2>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<DENSE_ADD, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<DW, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax,
               "shared memory budget exceeded");
@@ -1019,11 +1020,13 @@ int launch(Params p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensor
   return check_launch(what);
 }
 
-// Cluster pairs are built only for the gate/up backward dX GEMM.
+// Cluster pairs are built for the gate/up GEMMs on permuted rows (forward
+// and backward dX), where they measured faster; the down-projection kinds
+// measured no faster (forward) or slower (backward dX) as pairs.
 template <int KIND>
 int run(bool pair, const Params& p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
         const CUtensorMap& o0, const CUtensorMap& o1, cudaStream_t s, const char* what) {
-  if constexpr (KIND == GATE_UP_BWD_DX) {
+  if constexpr (KIND == GATE_UP_BWD_DX || KIND == GATE_UP_FWD) {
     if (pair) return launch<KIND, 2>(p, a, b0, b1, o0, o1, s, what);
   }
   return launch<KIND, 1>(p, a, b0, b1, o0, o1, s, what);
@@ -1166,7 +1169,8 @@ int swiglu_impl(const void* a_src, const int32_t* gather_rows, int T, const void
   if (int rc = make_out_map(&th, h, I, R, false)) return rc;
   if (int rc = make_out_map(&tgu, gu_save ? gu_save : h, gu_save ? 2 * I : I, R, false)) return rc;
   if (gather_rows) return run<GATE_UP_GATHER>(false, p, ta, tg, tu, th, tgu, s, fn);
-  return run<GATE_UP_FWD>(false, p, ta, tg, tu, th, tgu, s, fn);
+  // cluster pairs: the leader loads the gate rows of B, the peer the up rows
+  return run<GATE_UP_FWD>(use_pair(p.BN), p, ta, tg, tu, th, tgu, s, fn);
 }
 
 // e4m3 operands: H and I must be multiples of 128 (one 128-byte k-block).
