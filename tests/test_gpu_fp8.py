@@ -219,14 +219,16 @@ def test_fp8_layer_forward(T, H, I, E, k, ep):
     assert torch.equal(y1, y2)
 
 
-def test_fp8_layer_full_size_sampled_tokens():
-    """The fp8 forward as bench.py times it (Qwen3-30B-A3B shapes, T=4096):
+@pytest.mark.parametrize("workload", ["qwen3_30b_fwd", "qwen3_30b_zipf_fwd"])
+def test_fp8_layer_full_size_sampled_tokens(workload):
+    """The fp8 forward at full size (Qwen3-30B-A3B shapes; T=4096 as bench.py
+    times it, and the Zipf-skewed T=16384 workload with empty experts):
     routing bit for bit over every token, the weight codes and scales of the
     experts the sampled tokens use bit for bit, and those tokens' outputs
     against the oracle's fp8 chain (x and h quantised per row, weights per
     output channel, h and y_perm rounded to bf16 where the layer stores them)."""
     from moe_expert_layer_topk_gb300.synth import CONFIGS, make_layer_inputs
-    shape = CONFIGS["qwen3_30b_fwd"]
+    shape = CONFIGS[workload]
     inp = make_layer_inputs(shape, 0, with_dy=False)
     g = to_dev(inp)
     L = m.MoELayer(shape.T, shape.H, shape.I, shape.E, shape.k, shape.ep_size, training=False, fp8=True)
@@ -234,9 +236,12 @@ def test_fp8_layer_full_size_sampled_tokens():
     y = L.forward(g["x"], g["Wr"], g["bias"], w8, None, None)
     torch.cuda.synchronize()
     assert m.moe_read_device_status(reset=True) == 0
-    rt = oracle.route_topk(bits(inp["x"]), inp["Wr"].numpy(), None, shape.k, shape.ep_size)
+    bias = None if inp.get("bias") is None else inp["bias"].numpy()
+    rt = oracle.route_topk(bits(inp["x"]), inp["Wr"].numpy(), bias, shape.k, shape.ep_size)
     assert np.array_equal(L.topk_idx.cpu().numpy(), rt["topk_idx"])
     assert np.array_equal(L.offsets.cpu().numpy(), rt["offsets"])
+    if workload == "qwen3_30b_zipf_fwd":
+        assert (rt["counts"] == 0).sum() >= 4  # empty experts in the gathering e4m3 GEMM
     rng = np.random.default_rng(8)
     toks = sorted(rng.choice(shape.T, 4, replace=False).tolist())
     sub = dict(inp)
