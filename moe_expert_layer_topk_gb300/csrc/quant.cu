@@ -6,11 +6,14 @@
 // nearest even and saturated at 448.  Rows are token rows of x, permuted
 // rows of h, or output channels of the expert weights ([E * out, in]).
 //
-// HBM-bound: one warp per row reads the row once into registers (NC
-// 16-byte vectors per lane, NC picked from the row length so that short
-// rows keep few registers and many warps per SM; rows longer than 2048
-// elements are read twice, the second time from L2), reduces |a| to amax
-// with shuffles, then writes the codes with 8-byte stores and the scale.
+// One warp per row reads the row once into registers (NC 16-byte vectors
+// per lane, NC picked from the row length so that short rows keep few
+// registers and many warps per SM; rows longer than 2048 elements are read
+// twice, the second time from L2), reduces |a| to amax with shuffles, then
+// writes the codes with 8-byte stores and the scale.  It moves 3 bytes per
+// element; the exact IEEE division per element (which makes the codes a
+// pure function of the input bits) costs about as much again: h at
+// 32768 x 768 takes 16 us with it and 8 us with a multiplication.
 #include <cuda_fp8.h>
 
 #include <algorithm>
