@@ -485,10 +485,10 @@ def run_fp8_forward(m, fg, fshape, dev, stream, args):
 
 
 # kernels launched per step by the calls in run_ours.step():
-# route 3, dispatch 3, gate/up 1, down 1, combine 1, combine_bwd 1,
-# down_bwd 3 and gate/up bwd 3 (dX GEMM, segment maps, dW GEMM),
-# dispatch_bwd 1, route_bwd 7
-KERNELS_PER_STEP = 3 + 3 + 1 + 1 + 1 + 1 + 3 + 3 + 1 + 7
+# route 4 (zero counters, partial logits, top-k, offsets), dispatch 3,
+# gate/up 1, down 1, combine 1, combine_bwd 1, down_bwd 3 and gate/up bwd 3
+# (dX GEMM, segment maps, dW GEMM), dispatch_bwd 1, route_bwd 7
+KERNELS_PER_STEP = 4 + 3 + 1 + 1 + 1 + 1 + 3 + 3 + 1 + 7
 
 
 def run_profile_router(args):
