@@ -1169,8 +1169,13 @@ int swiglu_impl(const void* a_src, const int32_t* gather_rows, int T, const void
   if (int rc = make_out_map(&th, h, I, R, false)) return rc;
   if (int rc = make_out_map(&tgu, gu_save ? gu_save : h, gu_save ? 2 * I : I, R, false)) return rc;
   if (gather_rows) return run<GATE_UP_GATHER>(false, p, ta, tg, tu, th, tgu, s, fn);
-  // cluster pairs: the leader loads the gate rows of B, the peer the up rows
-  return run<GATE_UP_FWD>(use_pair(p.BN), p, ta, tg, tu, th, tgu, s, fn);
+  // Cluster pairs (the leader loads the gate rows of B, the peer the up rows)
+  // for the dispatch layout, one segment per expert: measured faster at 256
+  // and 512 rows per expert.  With several segments per expert (the EP
+  // receive layout) each expert's weights stay in L2 across its segments and
+  // the 256-row tiles waste more rows: single CTAs measured faster there.
+  const bool pair = use_pair(p.BN) && num_seg <= E;
+  return run<GATE_UP_FWD>(pair, p, ta, tg, tu, th, tgu, s, fn);
 }
 
 // e4m3 operands: H and I must be multiples of 128 (one 128-byte k-block).
