@@ -224,6 +224,17 @@ int moe_grouped_gemm_down(const void* h, const void* Wd, int num_seg, const int3
  * H and I must be multiples of 128.  Forward only (no g,u save).
  * ---------------------------------------------------------------------- */
 
+/* A3 on e4m3 rows: moe_dispatch that writes the permuted rows as e4m3 codes.
+ * Row row(t,j) of xq_perm (uint8 [T*k, H]) holds the codes of x[t] scaled by
+ * token t's scale s_t = amax(|x[t]|) / 448, and xs_perm[row(t,j)] = s_t
+ * (fp32 [T*k]): exactly moe_quantize_rows_e4m3 of x followed by the
+ * permutation, in one pass over x.  row_of_slot and token_of_row as
+ * moe_dispatch; same workspace (moe_dispatch_workspace_size).  xq_perm feeds
+ * moe_grouped_gemm_swiglu_fp8 with token_of_row = NULL. */
+int moe_dispatch_e4m3(const void* x, const int32_t* topk_idx, const int32_t* offsets, int T, int H,
+                      int E, int k, void* xq_perm, float* xs_perm, int32_t* row_of_slot,
+                      int32_t* token_of_row, void* ws, size_t ws_bytes, void* stream);
+
 /* Per-row e4m3 quantisation of a bf16 matrix a [rows, cols] (cols % 8 == 0):
  * q uint8 [rows, cols] (8-byte aligned), scale fp32 [rows].  Bit-exact:
  * codes and scales are a pure function of the input bits. */

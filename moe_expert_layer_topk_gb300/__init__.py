@@ -20,7 +20,8 @@ from . import build as _build_mod
 __all__ = ["lib", "MoEError", "LIB_PATH", "ENTRY_POINTS",
            "moe_route_topk", "moe_dispatch", "moe_dispatch_no_alloc", "moe_grouped_gemm_swiglu",
            "moe_grouped_gemm_swiglu_gather", "moe_grouped_gemm_down",
-           "moe_quantize_rows_e4m3", "moe_grouped_gemm_swiglu_fp8", "moe_grouped_gemm_down_fp8",
+           "moe_quantize_rows_e4m3", "moe_dispatch_e4m3", "moe_grouped_gemm_swiglu_fp8",
+           "moe_grouped_gemm_down_fp8",
            "moe_combine", "moe_combine_bwd", "moe_grouped_gemm_down_bwd",
            "moe_grouped_gemm_swiglu_bwd", "moe_dispatch_bwd", "moe_route_topk_bwd",
            "moe_route_topk_workspace_size", "moe_dispatch_workspace_size",
@@ -46,6 +47,7 @@ ENTRY_POINTS = {
     "moe_grouped_gemm_swiglu_gather": ([_P, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_grouped_gemm_down": ([_P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _P], _I),
     "moe_quantize_rows_e4m3": ([_P, _I, _I, _P, _P, _P], _I),
+    "moe_dispatch_e4m3": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P], _I),
     "moe_grouped_gemm_swiglu_fp8": ([_P, _P, _P, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P], _I),
     "moe_grouped_gemm_down_fp8": ([_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P], _I),
     "moe_combine": ([_P, _P, _P, _I, _I, _I, _P, _P], _I),
@@ -182,6 +184,12 @@ def moe_grouped_gemm_down(h, Wd, num_seg, seg_offsets, seg_expert, R, H, I, E, y
 
 def moe_quantize_rows_e4m3(a, rows, cols, q, scale, stream=None):
     _call("moe_quantize_rows_e4m3", _ptr(a), rows, cols, _ptr(q), _ptr(scale), _stream(stream))
+
+
+def moe_dispatch_e4m3(x, topk_idx, offsets, T, H, E, k, xq_perm, xs_perm, row_of_slot, token_of_row, ws,
+                      stream=None):
+    _call("moe_dispatch_e4m3", _ptr(x), _ptr(topk_idx), _ptr(offsets), T, H, E, k, _ptr(xq_perm), _ptr(xs_perm),
+          _ptr(row_of_slot), _ptr(token_of_row), _ptr(ws), _nbytes(ws), _stream(stream))
 
 
 def moe_grouped_gemm_swiglu_fp8(a, a_scale, token_of_row, T, Wg, Wg_scale, Wu, Wu_scale, num_seg,

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -95,6 +96,31 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ void set_status(int* status, int bits) {
   if (status) atomicOr(status, bits);
+}
+
+// e4m3 row quantisation ("TorchTitan FSDP2 完全指南", performance table: FP8
+// matmuls; the recipe is the reading stated in moe_topk.h): the largest |a|
+// of eight bf16 values, the row scale from the row's largest |a|, and eight
+// codes e4m3(a / s) (IEEE division, round to nearest even, saturated).
+__device__ __forceinline__ float amax_bf16x8(uint4 v, float m) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(bf16lo(w[i])), fabsf(bf16hi(w[i]))));
+  return m;
+}
+__device__ __forceinline__ float e4m3_row_scale(float amax) { return amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f; }
+__device__ __forceinline__ uint2 e4m3_codes8(uint4 v, float s) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t out[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float2 a = make_float2(__fdiv_rn(bf16lo(w[2 * h]), s), __fdiv_rn(bf16hi(w[2 * h]), s));
+    const float2 b = make_float2(__fdiv_rn(bf16lo(w[2 * h + 1]), s), __fdiv_rn(bf16hi(w[2 * h + 1]), s));
+    const uint32_t ca = __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
+    const uint32_t cb = __nv_cvt_float2_to_fp8x2(b, __NV_SATFINITE, __NV_E4M3);
+    out[h] = (ca & 0xFFFFu) | (cb << 16);
+  }
+  return make_uint2(out[0], out[1]);
 }
 
 }  // namespace moe

@@ -84,10 +84,14 @@ __global__ void __launch_bounds__(256) chunk_scan_kernel(int32_t* __restrict__ c
 // picks an expert at most once).  Then all 8 warps copy the chunk's token
 // rows to their k destinations; the first row of every copying warp is
 // loaded while warp 0 is still ranking.
+// kE4M3: the destination rows receive the token's e4m3 codes instead (its
+// scale from the largest |x| of the whole row, one fp32 scale written per
+// destination row to xs_perm), the same codes as quantising x per token.
+template <bool kE4M3>
 __global__ void __launch_bounds__(256) dispatch_kernel(
     const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ topk_idx,
     const int32_t* __restrict__ chunk_base, int T, int H, int E, int k,
-    __nv_bfloat16* __restrict__ x_perm, int32_t* __restrict__ row_of_slot,
+    void* __restrict__ x_perm_out, float* __restrict__ xs_perm, int32_t* __restrict__ row_of_slot,
     int32_t* __restrict__ token_of_row, int* status) {
   pdl_wait();
   pdl_trigger();
@@ -105,7 +109,7 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
   const int nvec = H / 8;  // 16-byte vectors per row
   // the first 8 vectors per lane of this warp's first token, in flight during the ranking
   uint4 pre[8];
-  const bool prefetch = x_perm != nullptr && warp > 0 && warp < nt;
+  const bool prefetch = x_perm_out != nullptr && warp > 0 && warp < nt;
   if (prefetch) {
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(t0 + warp) * H);
 #pragma unroll
@@ -142,7 +146,50 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
     }
   }
   __syncthreads();
-  if (!x_perm) return;
+  if (!x_perm_out) return;
+  if constexpr (kE4M3) {
+    uint8_t* xq = static_cast<uint8_t*>(x_perm_out);
+    for (int i = warp; i < nt; i += 8) {
+      const int t = t0 + i;
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+      // the row's largest |x| (its first 256 vectors stay in registers)
+      uint4 buf[8];
+      float m = 0.f;
+      for (int v0 = 0; v0 < nvec; v0 += 32 * 8) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int v = v0 + u * 32 + lane;
+          if (v < nvec) {
+            const uint4 w = (prefetch && i == warp && v0 == 0) ? pre[u] : __ldg(src + v);
+            if (v0 == 0) buf[u] = w;
+            m = amax_bf16x8(w, m);
+          }
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      const float sc = e4m3_row_scale(m);
+      for (int v0 = 0; v0 < nvec; v0 += 32 * 8) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int v = v0 + u * 32 + lane;
+          if (v < nvec) {
+            const uint2 c = e4m3_codes8(v0 == 0 ? buf[u] : __ldg(src + v), sc);
+            for (int j = 0; j < k; ++j) {
+              const int row = rows[i * k + j];
+              if (row >= 0) reinterpret_cast<uint2*>(xq + (size_t)row * H)[v] = c;
+            }
+          }
+        }
+      }
+      if (lane < k) {
+        const int row = rows[i * k + lane];
+        if (row >= 0) xs_perm[row] = sc;
+      }
+    }
+    return;
+  }
+  __nv_bfloat16* x_perm = static_cast<__nv_bfloat16*>(x_perm_out);
   for (int i = warp; i < nt; i += 8) {
     const int t = t0 + i;
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
@@ -311,6 +358,27 @@ int grid_for(size_t work, int per_block) {
   return (int)(b < cap ? (b > 0 ? b : 1) : cap);
 }
 
+// Ranking (per-chunk histograms, their scan) and the row kernel of a dispatch
+// whose scratch (the chunk bases) is `ws`.
+template <bool kE4M3>
+int dispatch_launch(const void* x, const int32_t* topk_idx, const int32_t* offsets, int T, int H, int E,
+                    int k, void* x_perm, float* xs_perm, int32_t* row_of_slot, int32_t* token_of_row,
+                    void* ws, cudaStream_t s, const char* fn) {
+  int* status = status_word();
+  const int nchunk = (T + kChunkTok - 1) / kChunkTok;
+  int32_t* chunk_base = static_cast<int32_t*>(ws);
+  launch_pdl(chunk_hist_kernel, (nchunk + 7) / 8, 256, sizeof(int) * 8 * E, s, topk_idx, T, E, k, nchunk,
+                                                                       chunk_base, status);
+  if (int rc = check_launch("moe_dispatch: histogram kernel")) return rc;
+  launch_pdl(chunk_scan_kernel, (E + 7) / 8, 256, 0, s, chunk_base, offsets, nchunk, E, status);
+  if (int rc = check_launch("moe_dispatch: scan kernel")) return rc;
+  launch_pdl(dispatch_kernel<kE4M3>, nchunk, 256, sizeof(int) * (E + kChunkTok * k), s,
+             static_cast<const __nv_bfloat16*>(x), topk_idx, chunk_base, T, H, E, k, x_perm, xs_perm,
+             row_of_slot, token_of_row, status);
+  (void)fn;
+  return check_launch("moe_dispatch: row kernel");
+}
+
 int check_rows_args(const char* fn, int T, int H, int k) {
   if (T < 0 || H <= 0 || k <= 0) return fail(MOE_ERR_INVALID_ARG, "%s: need T>=0, H>0, k>0", fn);
   if (H % 64 != 0 || k > kMaxTopK || (long long)T * k >= (1ll << 31))
@@ -347,20 +415,29 @@ int moe_dispatch(const void* x, const int32_t* topk_idx, const int32_t* offsets,
   if (ws_bytes < need)
     return fail(MOE_ERR_WORKSPACE, "moe_dispatch: workspace %zu < %zu bytes", ws_bytes, need);
   if (T == 0) return MOE_OK;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int* status = status_word();
-  const int nchunk = (T + kChunkTok - 1) / kChunkTok;
-  int32_t* chunk_base = static_cast<int32_t*>(ws);
-  launch_pdl(chunk_hist_kernel, (nchunk + 7) / 8, 256, sizeof(int) * 8 * E, s, topk_idx, T, E, k, nchunk,
-                                                                       chunk_base, status);
-  if (int rc = check_launch("moe_dispatch: histogram kernel")) return rc;
-  launch_pdl(chunk_scan_kernel, (E + 7) / 8, 256, 0, s, chunk_base, offsets, nchunk, E, status);
-  if (int rc = check_launch("moe_dispatch: scan kernel")) return rc;
-  launch_pdl(dispatch_kernel, nchunk, 256, sizeof(int) * (E + kChunkTok * k), s, 
-      static_cast<const __nv_bfloat16*>(x), topk_idx, chunk_base, T, H, E, k,
-      static_cast<__nv_bfloat16*>(x_perm), row_of_slot, token_of_row, status);
-  return check_launch("moe_dispatch: row kernel");
+  return dispatch_launch<false>(x, topk_idx, offsets, T, H, E, k, x_perm, nullptr, row_of_slot,
+                                token_of_row, ws, static_cast<cudaStream_t>(stream), "moe_dispatch");
 }
+
+int moe_dispatch_e4m3(const void* x, const int32_t* topk_idx, const int32_t* offsets, int T, int H,
+                      int E, int k, void* xq_perm, float* xs_perm, int32_t* row_of_slot,
+                      int32_t* token_of_row, void* ws, size_t ws_bytes, void* stream) {
+  clear_error();
+  const char* fn = "moe_dispatch_e4m3";
+  if (int rc = check_rows_args(fn, T, H, k)) return rc;
+  if (E <= 0 || E > kMaxExperts || k > E) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "%s: need 1<=E<=1024, k<=E", fn);
+  if (!ws || (T > 0 && (!x || !topk_idx || !offsets || !xq_perm || !xs_perm || !row_of_slot || !token_of_row)))
+    return fail(MOE_ERR_INVALID_ARG, "%s: NULL pointer argument", fn);
+  if (!aligned16(x) || !aligned16(xq_perm) || !aligned16(ws) || (reinterpret_cast<uintptr_t>(xs_perm) & 3u))
+    return fail(MOE_ERR_ALIGNMENT, "%s: x, xq_perm and ws must be 16-byte, xs_perm 4-byte aligned", fn);
+  const size_t need = moe_dispatch_workspace_size(T, E, k);
+  if (ws_bytes < need) return fail(MOE_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, need);
+  if (T == 0) return MOE_OK;
+  return dispatch_launch<true>(x, topk_idx, offsets, T, H, E, k, xq_perm, xs_perm, row_of_slot, token_of_row,
+                               ws, static_cast<cudaStream_t>(stream), fn);
+}
+
+
 
 int moe_combine(const void* y_perm, const float* topk_w, const int32_t* row_of_slot, int T, int H,
                 int k, void* y, void* stream) {
@@ -487,9 +564,9 @@ int moe_dispatch_no_alloc(const void* x, const int32_t* topk_idx, const int32_t*
   if (int rc = check_launch("moe_dispatch_no_alloc: histogram kernel")) return rc;
   launch_pdl(chunk_scan_kernel, (E + 7) / 8, 256, 0, s, chunk_base, offsets, nc, E, status);
   if (int rc = check_launch("moe_dispatch_no_alloc: scan kernel")) return rc;
-  launch_pdl(dispatch_kernel, nc, 256, sizeof(int) * (E + kChunkTok * k), s, 
-      static_cast<const __nv_bfloat16*>(x), topk_idx, chunk_base, T, H, E, k,
-      static_cast<__nv_bfloat16*>(x_perm), row_of_slot, token_of_row, status);
+  launch_pdl(dispatch_kernel<false>, nc, 256, sizeof(int) * (E + kChunkTok * k), s,
+             static_cast<const __nv_bfloat16*>(x), topk_idx, chunk_base, T, H, E, k, x_perm,
+             static_cast<float*>(nullptr), row_of_slot, token_of_row, status);
   return check_launch("moe_dispatch_no_alloc: row kernel");
 }
 

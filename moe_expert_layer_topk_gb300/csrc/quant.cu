@@ -14,8 +14,6 @@
 // element; the exact IEEE division per element (which makes the codes a
 // pure function of the input bits) costs about as much again: h at
 // 32768 x 768 takes 16 us with it and 8 us with a multiplication.
-#include <cuda_fp8.h>
-
 #include <algorithm>
 
 #include "common.cuh"
@@ -23,31 +21,6 @@
 namespace {
 
 constexpr int kQuantWarps = 8;   // rows per 256-thread block
-
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-__device__ __forceinline__ float amax8(uint4 v, float m) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(bf_lo(w[i])), fabsf(bf_hi(w[i]))));
-  return m;
-}
-
-// Eight bf16 values divided by s (IEEE division) -> eight e4m3 codes.
-__device__ __forceinline__ uint2 codes8(uint4 v, float s) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t out[2];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const float2 a = make_float2(__fdiv_rn(bf_lo(w[2 * h]), s), __fdiv_rn(bf_hi(w[2 * h]), s));
-    const float2 b = make_float2(__fdiv_rn(bf_lo(w[2 * h + 1]), s), __fdiv_rn(bf_hi(w[2 * h + 1]), s));
-    const uint32_t ca = __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
-    const uint32_t cb = __nv_cvt_float2_to_fp8x2(b, __NV_SATFINITE, __NV_E4M3);
-    out[h] = (ca & 0xFFFFu) | (cb << 16);
-  }
-  return make_uint2(out[0], out[1]);
-}
 
 // Blocks per SM each quantiser instantiation is compiled for.
 __host__ __device__ constexpr int quant_blocks_per_sm(int nc) { return nc <= 1 ? 6 : (nc <= 3 ? 4 : (nc <= 4 ? 3 : 2)); }
@@ -83,18 +56,18 @@ __global__ void __launch_bounds__(32 * kQuantWarps, quant_blocks_per_sm(NC))
     uint2* dst = reinterpret_cast<uint2*>(q + (size_t)row * cols);
     float m = 0.0f;
 #pragma unroll
-    for (int i = 0; i < NC; ++i) m = amax8(cur[i], m);
-    for (int v = lane + 32 * NC; v < nv; v += 32) m = amax8(__ldg(src + v), m);
+    for (int i = 0; i < NC; ++i) m = moe::amax_bf16x8(cur[i], m);
+    for (int v = lane + 32 * NC; v < nv; v += 32) m = moe::amax_bf16x8(__ldg(src + v), m);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    const float s = m > 0.0f ? __fdiv_rn(m, 448.0f) : 1.0f;
+    const float s = moe::e4m3_row_scale(m);
     if (lane == 0) scale[row] = s;
 #pragma unroll
     for (int i = 0; i < NC; ++i) {
       const int v = lane + 32 * i;
-      if (v < nv) dst[v] = codes8(cur[i], s);
+      if (v < nv) dst[v] = moe::e4m3_codes8(cur[i], s);
     }
-    for (int v = lane + 32 * NC; v < nv; v += 32) dst[v] = codes8(__ldg(src + v), s);
+    for (int v = lane + 32 * NC; v < nv; v += 32) dst[v] = moe::e4m3_codes8(__ldg(src + v), s);
 #pragma unroll
     for (int i = 0; i < NC; ++i) cur[i] = nxt[i];
   }

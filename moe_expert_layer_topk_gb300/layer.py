@@ -9,7 +9,7 @@ from __future__ import annotations
 
 import torch
 
-from . import (moe_combine, moe_combine_bwd, moe_dispatch, moe_dispatch_bwd,
+from . import (moe_combine, moe_combine_bwd, moe_dispatch, moe_dispatch_bwd, moe_dispatch_e4m3,
                moe_dispatch_workspace_size, moe_grouped_gemm_bwd_workspace_size,
                moe_grouped_gemm_down, moe_grouped_gemm_down_bwd, moe_grouped_gemm_down_fp8,
                moe_grouped_gemm_swiglu, moe_grouped_gemm_swiglu_bwd, moe_grouped_gemm_swiglu_fp8,
@@ -29,15 +29,16 @@ class MoELayer:
     gate/up GEMM reads its rows straight from x by token id, so x_perm is
     never written (moe_grouped_gemm_swiglu_gather).
 
-    fp8 (forward only, implies fused_dispatch): x is quantised to e4m3 per
-    token, the gate/up GEMM gathers its rows from those codes, h is
-    quantised per row, and both GEMMs run on e4m3 weights prepared once by
-    `quantize_weights` (one scale per output channel)."""
+    fp8 (forward only): dispatch writes the permuted rows as e4m3 codes with
+    one scale per token (moe_dispatch_e4m3), h is quantised per row, and
+    both GEMMs run on e4m3 weights prepared once by `quantize_weights` (one
+    scale per output channel)."""
 
     def __init__(self, T: int, H: int, I: int, E: int, k: int, ep_size: int = 1, *,
                  training: bool = True, fused_dispatch: bool = False, fp8: bool = False,
                  device: str | torch.device = "cuda"):
-        fused_dispatch = fused_dispatch or fp8
+        if fp8 and training:
+            raise ValueError("the e4m3 path is forward only")
         if fused_dispatch and training:
             raise ValueError("fused_dispatch keeps no x_perm, which the backward pass needs")
         self.T, self.H, self.I, self.E, self.k, self.ep_size = T, H, I, E, k, ep_size
@@ -56,7 +57,7 @@ class MoELayer:
         self.rank_offsets = e(ep_size + 1, dt=i32)
         self.ws_route = _ws(moe_route_topk_workspace_size(T, H, E), dev)
         self.ws_dispatch = _ws(moe_dispatch_workspace_size(T, E, k), dev)
-        self.x_perm = None if fused_dispatch else e(R, H, dt=bf)
+        self.x_perm = None if (fused_dispatch or fp8) else e(R, H, dt=bf)
         self.row_of_slot = e(T, k, dt=i32)
         self.token_of_row = e(R, dt=i32)
         self.h = e(R, I, dt=bf)
@@ -65,7 +66,7 @@ class MoELayer:
         self.y = e(T, H, dt=bf)
         if fp8:
             u8 = torch.uint8
-            self.x_q, self.x_scale = e(T, H, dt=u8), e(T, dt=f32)
+            self.x_q, self.x_scale = e(R, H, dt=u8), e(R, dt=f32)  # permuted rows, their tokens' scales
             self.h_q, self.h_scale = e(R, I, dt=u8), e(R, dt=f32)
         if training:
             self.dy_perm = e(R, H, dt=bf)
@@ -100,6 +101,10 @@ class MoELayer:
 
     def dispatch(self, x, stream=None):
         self._x = x  # the fused gate/up GEMM reads the rows from here
+        if self.fp8:
+            moe_dispatch_e4m3(x, self.topk_idx, self.offsets, self.T, self.H, self.E, self.k, self.x_q,
+                              self.x_scale, self.row_of_slot, self.token_of_row, self.ws_dispatch, stream)
+            return
         moe_dispatch(x, self.topk_idx, self.offsets, self.T, self.H, self.E, self.k, self.x_perm,
                      self.row_of_slot, self.token_of_row, self.ws_dispatch, stream)
 
@@ -109,10 +114,8 @@ class MoELayer:
         if self.fp8:
             w = Wg
             T, H, I, E, R = self.T, self.H, self.I, self.E, self.R
-            moe_quantize_rows_e4m3(self._x, T, H, self.x_q, self.x_scale, stream)
-            moe_grouped_gemm_swiglu_fp8(self.x_q, self.x_scale, self.token_of_row, T, w["Wg"],
-                                        w["Wg_scale"], w["Wu"], w["Wu_scale"], E, self.offsets, None,
-                                        R, H, I, E, self.h, stream)
+            moe_grouped_gemm_swiglu_fp8(self.x_q, self.x_scale, None, 0, w["Wg"], w["Wg_scale"], w["Wu"],
+                                        w["Wu_scale"], E, self.offsets, None, R, H, I, E, self.h, stream)
             moe_quantize_rows_e4m3(self.h, R, I, self.h_q, self.h_scale, stream)
             moe_grouped_gemm_down_fp8(self.h_q, self.h_scale, w["Wd"], w["Wd_scale"], E, self.offsets,
                                       None, R, H, I, E, self.y_perm, stream)

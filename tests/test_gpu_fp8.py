@@ -306,3 +306,30 @@ def test_fp8_ep_rank_local_segments_full_size():
     hq_o, hs_o = oracle.quantize_rows_e4m3(rne_bf16(href))
     yref = oracle.grouped_gemm_down_fp8(hq_o, hs_o, W["Wd"][0], W["Wd"][1], so2, se2)
     assert_close(y[rows], yref, "y_perm (fp8, sampled rows)")
+
+
+@pytest.mark.parametrize("T,H,E,k,bias", [(300, 256, 8, 2, None), (517, 2560, 16, 4, "zipf"), (64, 128, 130, 8, None)])
+def test_dispatch_e4m3_bit_exact(T, H, E, k, bias):
+    """moe_dispatch_e4m3: each permuted row holds its token's e4m3 codes and
+    scale bit for bit as the oracle quantises x per token, with the rows,
+    row_of_slot and token_of_row of moe_dispatch (H = 2560 takes the second
+    pass over rows longer than the 256 vectors held in registers; the Zipf
+    bias leaves experts empty)."""
+    inp = inputs(T, H, 64, E, k, seed=T + H, bias=bias, router_std=0.02 if bias is None else 0.3)
+    g = to_dev(inp)
+    L = m.MoELayer(T, H, 64, E, k, 1, training=False)
+    L.route(g["x"], g["Wr"], g["bias"])
+    L.dispatch(g["x"])
+    R = T * k
+    xq = torch.full((R, H), 0x5A, dtype=torch.uint8, device="cuda")
+    xs = torch.full((R,), float("nan"), dtype=torch.float32, device="cuda")
+    ros = torch.empty_like(L.row_of_slot)
+    tor = torch.empty_like(L.token_of_row)
+    m.moe_dispatch_e4m3(g["x"], L.topk_idx, L.offsets, T, H, E, k, xq, xs, ros, tor, L.ws_dispatch)
+    torch.cuda.synchronize()
+    assert m.moe_read_device_status(reset=True) == 0
+    assert torch.equal(ros, L.row_of_slot) and torch.equal(tor, L.token_of_row)
+    q_ref, s_ref = oracle.quantize_rows_e4m3(oracle.widen_bf16(bits(inp["x"])))
+    t = tor.cpu().numpy()
+    assert np.array_equal(xq.cpu().numpy(), q_ref[t])
+    assert np.array_equal(xs.cpu().numpy().view(np.uint32), s_ref[t].view(np.uint32))
