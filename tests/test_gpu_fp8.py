@@ -64,6 +64,38 @@ def test_quantize_rows_bit_exact(rows, cols):
     assert np.array_equal(q.cpu().numpy(), q_ref)
 
 
+def _hard_quantize_rows(gen):
+    """Rows that stress the quotient a / s: (i) power-of-two scales with
+    entries on e4m3 midpoints (exact ties, rounded to even), (ii) rows of
+    bf16-subnormal and near-subnormal magnitudes, whose scale is so small
+    that 1 / s overflows fp32, (iii) many rows of widely spread magnitudes,
+    so that some quotients fall within a few fp32 ulps of a midpoint."""
+    codes = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8)).astype(np.float64)
+    vals = np.sort(codes)
+    mids = (vals[1:] + vals[:-1]) / 2                     # 125 midpoints, 448 is the largest code
+    ties = []
+    for k in (-20, -3, 0, 5):
+        row = np.concatenate([mids, -mids, vals, [448.0]]) * 2.0 ** k
+        row = np.resize(row, 384)
+        row[0] = 448.0 * 2.0 ** k                          # amax: s = 2^k exactly
+        ties.append(row)
+    ties = torch.tensor(np.array(ties), dtype=torch.float32)
+    tiny = torch.cat([torch.randn(6, 384, generator=gen) * 2.0 ** e for e in (-133, -130, -127, -125, -122, -118)])
+    wide = torch.randn(2048, 384, generator=gen) * torch.exp(torch.empty(2048, 1).uniform_(-30, 30, generator=gen))
+    return torch.cat([ties, tiny, wide]).to(torch.bfloat16)
+
+
+def test_quantize_rows_bit_exact_hard_cases():
+    gen = torch.Generator().manual_seed(4242)
+    a = _hard_quantize_rows(gen)
+    rows, cols = a.shape
+    q, s = _quant_gpu(a.cuda())
+    torch.cuda.synchronize()
+    q_ref, s_ref = oracle.quantize_rows_e4m3(oracle.widen_bf16(bits(a)))
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+
+
 def test_quantize_rejects_bad_args():
     a = torch.zeros(4, 12, dtype=torch.bfloat16, device="cuda")
     q = torch.empty(4, 12, dtype=torch.uint8, device="cuda")
