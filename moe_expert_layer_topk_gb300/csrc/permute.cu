@@ -27,6 +27,8 @@ constexpr int kChunkTok = 16;  // tokens per ranking chunk
 // 29 us against 40 us for one block per chunk, whose warps (124
 // registers, 1.7 blocks an SM) waited on their rows' loads.
 constexpr int kE4M3Split = 2;
+// Batches of 32 slot expert ids the ranking warp keeps loaded ahead.
+constexpr int kRankAhead = 4;
 
 // --------------------------------------------------------------- histogram
 // chunk_base[e][c] = number of slots of chunk c routed to expert e.
@@ -131,15 +133,24 @@ __global__ void __launch_bounds__(256, kE4M3 ? 4 : 1) dispatch_kernel(
       if (v < nvec) pre[u] = __ldg(src + v);
     }
   }
+  // the ranking warp's expert ids of the next kRankAhead batches of 32
+  // slots, in flight (the first ones already while the counts load)
+  const int32_t* ids = topk_idx + (size_t)t0 * k;
+  int ahead[kRankAhead];
+  if (warp == 0) {
+#pragma unroll
+    for (int u = 0; u < kRankAhead; ++u) ahead[u] = u * 32 + lane < nslot ? ids[u * 32 + lane] : -1;
+  }
   __syncthreads();
   if (warp == 0) {
     for (int b = 0; b < nslot; b += 32) {
       const int q = b + lane;
-      int e = -1;
-      if (q < nslot) {
-        e = topk_idx[(size_t)t0 * k + q];
-        if (e < 0 || e >= E) e = -1;
-      }
+      int e = ahead[0];
+#pragma unroll
+      for (int u = 0; u + 1 < kRankAhead; ++u) ahead[u] = ahead[u + 1];
+      const int qn = q + 32 * kRankAhead;
+      ahead[kRankAhead - 1] = qn < nslot ? ids[qn] : -1;
+      if (q >= nslot || e < 0 || e >= E) e = -1;
       const unsigned peers = __match_any_sync(0xffffffffu, e);
       const int rank = __popc(peers & ((1u << lane) - 1u));
       int row = -1;
