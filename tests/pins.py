@@ -469,6 +469,34 @@ def pin_quantize_rows():
     assert np.abs(dec[5]).max() == 448.0 and q[5, 17] == 0xFE
 
 
+def pin_quantize_rows_power_of_two_scale():
+    """A row whose largest magnitude is 448 * 2^j has the scale 2^j exactly,
+    so every quotient a / s is exact and the codes must be torch's
+    conversion of a * 2^-j: midpoints between codes (ties to even), one
+    ulp either side of them and every code value, at scales from the fp32
+    subnormal 2^-130 up to 2^7."""
+    c = _finite_codes()
+    pos = np.sort(oracle.e4m3_decode(c[c < 0x80]).astype(np.float32))
+    mids = (pos[1:] + pos[:-1]) / np.float32(2)           # 5 significant bits: exact
+    near = np.concatenate([np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(np.inf))])
+    rows, expect = [], []
+    for j in (-130, -20, 0, 7):
+        # fp32 ulp neighbours only where 2^j keeps them normal; at 2^-130 they
+        # would lose bits as subnormals, the midpoints and codes do not
+        base = np.concatenate([mids, pos] + ([near] if j > -100 else [])).astype(np.float64)
+        row = np.concatenate([[448.0], base, -base]) * 2.0 ** j
+        row32 = row.astype(np.float32)
+        assert np.array_equal(row32.astype(np.float64), row)
+        rows.append(row32)
+        expect.append(_torch_e4m3_codes((row / 2.0 ** j).astype(np.float32)))
+    width = max(len(r) for r in rows)                      # pad with zeros (code 0)
+    rows = [np.pad(r, (0, width - len(r))) for r in rows]
+    expect = [np.pad(e, (0, width - len(e))) for e in expect]
+    q, s = oracle.quantize_rows_e4m3(np.stack(rows))
+    assert np.array_equal(s.astype(np.float64), np.array([2.0 ** j for j in (-130, -20, 0, 7)]))
+    assert np.array_equal(q, np.stack(expect))
+
+
 def _int_codes(rng, shape, lo=-8, hi=8):
     """e4m3 codes of random small integers (exactly representable)."""
     v = rng.integers(lo, hi + 1, shape).astype(np.float32)
@@ -529,8 +557,8 @@ def pin_fp8_reduces_to_bf16_oracle():
     assert rel_l2(y8, y16) < 1e-6
 
 
-FP8_PINS = [pin_e4m3_decode, pin_e4m3_encode, pin_quantize_rows, pin_fp8_gemms_integer_case,
-            pin_fp8_reduces_to_bf16_oracle]
+FP8_PINS = [pin_e4m3_decode, pin_e4m3_encode, pin_quantize_rows, pin_quantize_rows_power_of_two_scale,
+            pin_fp8_gemms_integer_case, pin_fp8_reduces_to_bf16_oracle]
 
 ALL_PINS = [pin_logit_block_order, pin_logits_error_bound, pin_topk_bruteforce, pin_topk_ties,
             pin_weights_closed_form, pin_counts_offsets, pin_permutation, pin_forward_dense_fp64,
