@@ -40,6 +40,7 @@ MUTANTS = {
     "e4m3_bias_8": ("moe_oracle.c", "v = ldexp(1.0 + m / 8.0, field - 7);", "v = ldexp(1.0 + m / 8.0, field - 8);"),
     "e4m3_no_subnormals": ("moe_oracle.c", "q = (int)nearbyint(m / ldexp(1.0, -9));", "q = 0;"),
     "quant_scale_240": ("moe_oracle.c", "amax > 0.0f ? amax / 448.0f : 1.0f", "amax > 0.0f ? amax / 240.0f : 1.0f"),
+    "quant_multiplies": ("moe_oracle.c", "e4m3_code(row[j] / s)", "e4m3_code(row[j] * s)"),
     "fp8_up_uses_gate_scale": ("moe_oracle.c", "Wu_scale[(size_t)e * I + i] * su", "Wg_scale[(size_t)e * I + i] * su"),
     "fp8_down_row_scale_dropped": ("moe_oracle.c", "(double)h_scale[r] * Wd_scale", "(double)h_scale[0] * Wd_scale"),
     "fp8_down_wrong_weight_row": ("moe_oracle.c", "const uint8_t* w = Wdq + ((size_t)e * H + n) * I;",
