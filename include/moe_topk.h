@@ -230,14 +230,18 @@ int moe_grouped_gemm_down(const void* h, const void* Wd, int num_seg, const int3
  * (fp32 [T*k]): exactly moe_quantize_rows_e4m3 of x followed by the
  * permutation, in one pass over x.  row_of_slot and token_of_row as
  * moe_dispatch; same workspace (moe_dispatch_workspace_size).  xq_perm feeds
- * moe_grouped_gemm_swiglu_fp8 with token_of_row = NULL. */
+ * moe_grouped_gemm_swiglu_fp8 with token_of_row = NULL.  x, xq_perm and ws
+ * 16-byte aligned, xs_perm 4-byte aligned (else MOE_ERR_ALIGNMENT); shape
+ * and status errors as moe_dispatch. */
 int moe_dispatch_e4m3(const void* x, const int32_t* topk_idx, const int32_t* offsets, int T, int H,
                       int E, int k, void* xq_perm, float* xs_perm, int32_t* row_of_slot,
                       int32_t* token_of_row, void* ws, size_t ws_bytes, void* stream);
 
 /* Per-row e4m3 quantisation of a bf16 matrix a [rows, cols] (cols % 8 == 0):
- * q uint8 [rows, cols] (8-byte aligned), scale fp32 [rows].  Bit-exact:
- * codes and scales are a pure function of the input bits. */
+ * q uint8 [rows, cols], scale fp32 [rows].  Bit-exact: codes and scales are
+ * a pure function of the input bits.  a 16-byte, q 8-byte and scale 4-byte
+ * aligned (else MOE_ERR_ALIGNMENT); rows < 0, cols <= 0, cols % 8 != 0 or a
+ * NULL pointer give MOE_ERR_INVALID_ARG; rows == 0 does nothing. */
 int moe_quantize_rows_e4m3(const void* a, int rows, int cols, void* q, float* scale, void* stream);
 
 /* A4 on e4m3 operands: h[r] = silu(g) * u -> bf16 [R,I], with g and u the
