@@ -1,5 +1,6 @@
 """Edge cases of the CUDA path against the CPU oracle: one token, one expert
-(a plain SwiGLU MLP), logit ties, k = E, empty experts, every token on one expert,
+(a plain SwiGLU MLP), logit ties, k = E, the largest E and k (1024, 32), empty
+experts, every token on one expert,
 segmented (source-rank x expert) row layouts, gradient accumulation, and the
 device status word for bad index data (kernels skip the bad entries)."""
 import numpy as np
@@ -116,6 +117,19 @@ def test_every_token_on_one_expert():
     L, _ = run_layer(inp)
     assert L.counts.cpu().tolist() == [0, 0, 0, 1000, 0, 0, 0, 0]
     check_all(L, inp)
+
+
+def test_maximum_experts_and_topk():
+    """The ABI's largest expert count and top-k together: E = 1024, k = 32,
+    EP over 8 ranks.  3072 slots over 1024 experts leave most experts with
+    a few rows and many with none; forward and backward against the oracle."""
+    inp = inputs(96, 128, 64, 1024, 32, seed=21, ep=8, router_std=0.3)
+    L, _ = run_layer(inp)
+    f, _ = check_all(L, inp)
+    counts = L.counts.cpu().numpy()
+    assert counts.sum() == 96 * 32 and (counts == 0).any()
+    assert np.array_equal(L.rank_offsets.cpu().numpy(), f["rt"]["rank_offsets"])
+    assert np.array_equal(f["rt"]["rank_offsets"], f["rt"]["offsets"][::128])
 
 
 def test_zero_tokens():
