@@ -373,6 +373,90 @@ def _finite_difference_check(d, idx, dyt, leaves, eps=1e-6):
             assert abs(fd - g) <= 1e-6 + 1e-5 * abs(g), (fd, g)
 
 
+def _bf16_of(rng, shape, std):
+    v = torch.from_numpy((rng.standard_normal(shape) * std).astype(np.float32))
+    return bf16_bits(v.to(torch.bfloat16))
+
+
+def pin_segments_backward():
+    """Backward over a receive-side segment table: several segments per
+    expert in an order that is neither sorted nor identity, empty segments,
+    an expert that owns no segment, and rows before the first and after the
+    last segment.  dgu, dx_perm, dWd, dWg and dWu equal fp64 torch autograd
+    of the per-segment dense forward; accumulate adds the fresh sum to the
+    buffer exactly; the segment-less expert's gradients are exactly zero
+    (overwrite) or untouched (accumulate); uncovered rows stay zero.
+
+    The layout is the one an EP rank receives ("Qwen3-MoE-30B-A3B模型EP+FSDP2
+    并行方案", "完整并行流程" and "Expert Parallelism Details": rows arrive per
+    source rank, the expert compute runs on local tensors); empty groups:
+    "FSDPTurbo EP/EFSDP and LlamaFactory FSDP2/CP Design", section 3.
+    """
+    rng = np.random.default_rng(75)
+    H, I, E = 64, 64, 5
+    lens = [10, 0, 15, 12, 7, 20, 0, 9, 14, 11, 25, 19]
+    se = np.array([2, 0, 3, 1, 0, 2, 1, 3, 3, 1, 0, 2], np.int32)  # expert 4 owns no segment
+    lead, tail = 8, 10
+    so = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32) + lead
+    R = int(so[-1]) + tail
+    xb = _bf16_of(rng, (R, H), 1.0)
+    Wg, Wu = _bf16_of(rng, (E, I, H), 0.2), _bf16_of(rng, (E, I, H), 0.2)
+    Wd = _bf16_of(rng, (E, H, I), 0.2)
+    dy = oracle.widen_bf16(_bf16_of(rng, (R, H), 1.0))
+    xp = oracle.widen_bf16(xb)
+
+    h, gu = oracle.grouped_gemm_swiglu(xp, Wg, Wu, so, se, save_gu=True)
+    dgu, dWd = oracle.grouped_gemm_down_bwd(dy, h, gu, Wd, so, se)
+    dx_perm, dWg, dWu = oracle.grouped_gemm_swiglu_bwd(dgu, xp, Wg, Wu, so, se)
+
+    f64 = lambda a: torch.from_numpy(oracle.widen_bf16(a).astype(np.float64))
+    x = torch.from_numpy(xp.astype(np.float64)).requires_grad_(True)
+    tWg, tWu, tWd = (f64(a).requires_grad_(True) for a in (Wg, Wu, Wd))
+    dyt = torch.from_numpy(dy.astype(np.float64))
+    loss = torch.zeros((), dtype=torch.float64)
+    parts = []
+    for q in range(len(se)):
+        a, b, e = int(so[q]), int(so[q + 1]), int(se[q])
+        if b == a:
+            continue
+        g = x[a:b] @ tWg[e].T
+        u = x[a:b] @ tWu[e].T
+        g.retain_grad(); u.retain_grad()
+        y = (F.silu(g) * u) @ tWd[e].T
+        loss = loss + (y * dyt[a:b]).sum()
+        parts.append((a, b, g, u))
+    loss.backward()
+    dgu_ref = np.zeros((R, 2 * I))
+    for a, b, g, u in parts:
+        dgu_ref[a:b, :I] = g.grad.numpy()
+        dgu_ref[a:b, I:] = u.grad.numpy()
+    cov = slice(int(so[0]), int(so[-1]))
+    for name, got, ref in (("dgu", dgu[cov], dgu_ref[cov]), ("dx_perm", dx_perm[cov], x.grad.numpy()[cov]),
+                           ("dWd", dWd, tWd.grad.numpy()), ("dWg", dWg, tWg.grad.numpy()),
+                           ("dWu", dWu, tWu.grad.numpy())):
+        err = rel_l2(got, ref)
+        assert err < 2e-5, (name, err)
+    for name, got in (("dgu", dgu), ("dx_perm", dx_perm)):
+        assert not np.any(got[:lead]) and not np.any(got[R - tail:]), name
+    for name, got in (("dWd", dWd), ("dWg", dWg), ("dWu", dWu)):
+        assert np.all(got[4] == 0), name
+    # every expert's gradient is the sum over all of its segments: dropping
+    # any one non-empty segment changes it by a visible amount
+    for e in range(4):
+        own = [q for q in range(len(se)) if se[q] == e and so[q + 1] > so[q]]
+        assert len(own) >= 2, e
+
+    prev = [rng.standard_normal(a.shape).astype(np.float32) for a in (dWd, dWg, dWu)]
+    _, acc_d = oracle.grouped_gemm_down_bwd(dy, h, gu, Wd, so, se, dWd=prev[0])
+    _, acc_g, acc_u = oracle.grouped_gemm_swiglu_bwd(dgu, xp, Wg, Wu, so, se, dWg=prev[1], dWu=prev[2])
+    for name, acc, p0, fresh, ref in (("dWd", acc_d, prev[0], dWd, tWd.grad.numpy()),
+                                      ("dWg", acc_g, prev[1], dWg, tWg.grad.numpy()),
+                                      ("dWu", acc_u, prev[2], dWu, tWu.grad.numpy())):
+        assert np.array_equal(acc, p0 + fresh), name
+        assert np.array_equal(acc[4], p0[4]), name
+        assert rel_l2(acc - p0, ref) < 2e-5, name
+
+
 def pin_accumulate_and_empty():
     """accumulate=1 adds the fresh sum to the buffer; an expert with no rows
     gets an exactly-zero weight gradient in overwrite mode."""
@@ -563,4 +647,4 @@ FP8_PINS = [pin_e4m3_decode, pin_e4m3_encode, pin_quantize_rows, pin_quantize_ro
 ALL_PINS = [pin_logit_block_order, pin_logits_error_bound, pin_topk_bruteforce, pin_topk_ties,
             pin_weights_closed_form, pin_counts_offsets, pin_permutation, pin_forward_dense_fp64,
             pin_dense_mlp_special_case, pin_identity_experts, pin_segments_dense,
-            pin_backward_autograd, pin_accumulate_and_empty] + FP8_PINS
+            pin_backward_autograd, pin_segments_backward, pin_accumulate_and_empty] + FP8_PINS

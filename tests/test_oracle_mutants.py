@@ -12,6 +12,13 @@ import pytest
 import oracle
 import pins
 
+# the expert-selection line of each weight-gradient loop, with enough of the
+# loop body to make it unique
+_DWD_SEG = ("    for (int s = 0; s < num_seg; ++s) {\n      if (seg_expert_of(seg_expert, s) != e) continue;\n"
+            "      for (int r = seg_offsets[s]; r < seg_offsets[s + 1]; ++r) {\n        const float* d = dy_perm")
+_DWGU_SEG = ("    for (int s = 0; s < num_seg; ++s) {\n      if (seg_expert_of(seg_expert, s) != e) continue;\n"
+             "      for (int r = seg_offsets[s]; r < seg_offsets[s + 1]; ++r) {\n        const float* dg = dgu")
+
 MUTANTS = {
     "tie_to_higher_id": ("moe_oracle.c", "logit[e] > logit[best]", "logit[e] >= logit[best]"),
     "logit_block_128": ("moe_oracle.h", "#define ORACLE_LOGIT_BLOCK 256", "#define ORACLE_LOGIT_BLOCK 128"),
@@ -47,7 +54,18 @@ MUTANTS = {
                                   "const uint8_t* w = Wdq + ((size_t)e * H + (H - 1 - n)) * I;"),
     "dispatch_bwd_drops_slot": ("moe_oracle.c", "for (int j = 0; j < k; ++j)\n        acc = acc + dx_perm",
                                 "for (int j = 1; j < k; ++j)\n        acc = acc + dx_perm"),
+    # weight gradients over a segment table with several segments per expert
+    "dWd_by_segment_id": ("moe_oracle.c", _DWD_SEG, _DWD_SEG.replace("seg_expert_of(seg_expert, s) != e", "s != e")),
+    "dWd_first_segment_only": ("moe_oracle.c", _DWD_SEG,
+                               "int seen = 0;\n" + _DWD_SEG.replace("!= e) continue;", "!= e || seen++) continue;")),
+    "dWgu_by_segment_id": ("moe_oracle.c", _DWGU_SEG, _DWGU_SEG.replace("seg_expert_of(seg_expert, s) != e", "s != e")),
+    "dWgu_first_segment_only": ("moe_oracle.c", _DWGU_SEG,
+                                "int seen = 0;\n" + _DWGU_SEG.replace("!= e) continue;", "!= e || seen++) continue;")),
 }
+
+# mutants that a specific pin exists to catch: it must be among the failures
+MUST_FAIL = {name: "pin_segments_backward" for name in
+             ("dWd_by_segment_id", "dWd_first_segment_only", "dWgu_by_segment_id", "dWgu_first_segment_only")}
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
@@ -70,3 +88,5 @@ def test_mutant_is_caught(tmp_path, name):
     finally:
         oracle.use(prev)
     assert failed, f"mutant {name} passed every pin"
+    if name in MUST_FAIL:
+        assert MUST_FAIL[name] in failed, (name, failed)
