@@ -116,13 +116,19 @@ class ClockSampler:
 
 # ------------------------------------------------------------ ncu traffic
 
-def recorded_traffic():
-    """DRAM bytes per launch of the forward gate/up GEMM as recorded from ncu
-    in profiles/traffic_gate_up_fwd_T8192.md, or None once the kernel's
-    sources no longer hash to the values recorded there."""
+# DRAM traffic per launch recorded from one-pass ncu captures, per entry-point
+# call, each valid only while the GEMM sources hash as recorded.
+TRAFFIC_PROFILES = {"gate_up": "traffic_gate_up_fwd_T8192.md", "gate_up_bwd_dw": "traffic_dw_gate_up_T8192.md"}
+
+
+def recorded_traffic(call="gate_up"):
+    """DRAM bytes (read + write) per launch of `call`'s kernel as recorded
+    from ncu under profiles/, or None when there is no record or the
+    kernel's sources no longer hash to the values recorded there."""
     import hashlib
-    prof = ROOT / "profiles" / "traffic_gate_up_fwd_T8192.md"
-    if not prof.exists():
+    name = TRAFFIC_PROFILES.get(call)
+    prof = ROOT / "profiles" / name if name else None
+    if prof is None or not prof.exists():
         return None
     value, hashes = None, {}
     for line in prof.read_text().splitlines():
@@ -139,6 +145,90 @@ def recorded_traffic():
         if not f.exists() or hashlib.sha256(f.read_bytes()).hexdigest() != digest:
             return None
     return value
+
+
+# --------------------------------------------------------- algorithmic costs
+
+def call_costs(T, H, I, E, k):
+    """Algorithmic flops (2 per multiply-add) and DRAM bytes of each call of
+    the training step: every operand read once, every result written once.
+    Weight gradients are fp32, activations bf16, indices and weights 4 bytes."""
+    R = T * k
+    W = E * I * H  # elements of one expert weight tensor (Wg, Wu or Wd)
+    idx = T * k * 4
+    return {
+        "route": {"flops": 2.0 * T * H * E, "bytes": T * H * 2 + H * E * 4 + 2 * idx, "pipe": "fma"},
+        "dispatch": {"flops": 0.0, "bytes": T * H * 2 + R * H * 2 + 3 * idx},
+        "gate_up": {"flops": 2.0 * R * H * 2 * I, "bytes": R * H * 2 + 2 * W * 2 + R * I * 2 + R * 2 * I * 2},
+        "down": {"flops": 2.0 * R * I * H, "bytes": R * I * 2 + W * 2 + R * H * 2},
+        "combine": {"flops": 0.0, "bytes": R * H * 2 + T * H * 2 + 2 * idx},
+        "combine_bwd": {"flops": 0.0, "bytes": T * H * 2 + 2 * R * H * 2 + 3 * idx},
+        "down_bwd_dx": {"flops": 2.0 * R * H * I, "bytes": R * H * 2 + W * 2 + 2 * R * 2 * I * 2},
+        "down_bwd_dw": {"flops": 2.0 * R * H * I, "bytes": R * H * 2 + R * I * 2 + W * 4},
+        "gate_up_bwd_dx": {"flops": 2.0 * R * 2 * I * H, "bytes": R * 2 * I * 2 + 2 * W * 2 + R * H * 2},
+        "gate_up_bwd_dw": {"flops": 2.0 * R * 2 * I * H, "bytes": R * 2 * I * 2 + R * H * 2 + 2 * W * 4},
+        "dispatch_bwd": {"flops": 0.0, "bytes": R * H * 2 + T * H * 4 + idx},
+        "route_bwd": {"flops": 2.0 * 2 * T * H * E, "bytes": T * H * 2 + T * H * 4 + T * H * 2 + H * E * 8 + 3 * idx},
+    }
+
+
+# the calls that launch one kernel (the weight-gradient halves also launch the
+# segment-map kernel of a few microseconds before their GEMM)
+SINGLE_KERNEL = {"gate_up": "grouped_gemm gate/up + SwiGLU (forward)", "down": "grouped_gemm down (forward)",
+                 "combine": "combine (weighted unpermute)", "combine_bwd": "combine backward",
+                 "down_bwd_dx": "grouped_gemm down backward dX + SwiGLU backward",
+                 "down_bwd_dw": "grouped_gemm dW_down (fp32)",
+                 "gate_up_bwd_dx": "grouped_gemm gate/up backward dX",
+                 "gate_up_bwd_dw": "grouped_gemm dW_gate/up (fp32)", "dispatch_bwd": "dispatch backward"}
+
+
+def rooflines(per_call, costs, pk, fma_tfma):
+    """Roofline of every call: time at the bound (the larger of the tensor,
+    FMA and HBM times) over the measured time.  Tensor-bound calls use the
+    sustained bf16 peak (they run inside a step of a second or more)."""
+    out = {}
+    for n, ms in per_call.items():
+        c = costs.get(n)
+        if c is None or ms <= 0:
+            continue
+        t = ms * 1e-3
+        t_mem = c["bytes"] / (pk["hbm_gbs"] * 1e9)
+        if c.get("pipe") == "fma":
+            t_cmp = c["flops"] / 2 / (fma_tfma * 1e12) if fma_tfma else 0.0
+            cmp_peak, cmp_unit, cmp_bound = fma_tfma, "TFMA/s", "alu"
+            achieved_cmp = c["flops"] / 2 / t / 1e12
+        else:
+            t_cmp = c["flops"] / (pk["bf16_tflops_sustained"] * 1e12)
+            cmp_peak, cmp_unit, cmp_bound = pk["bf16_tflops_sustained"], "TFLOP/s", "tensor"
+            achieved_cmp = c["flops"] / t / 1e12
+        gbs = c["bytes"] / t / 1e9
+        if t_cmp >= t_mem and c["flops"] > 0:
+            r = {"bound": cmp_bound, "achieved": achieved_cmp, "peak": cmp_peak, "unit": cmp_unit}
+        else:
+            r = {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s"}
+        r["frac"] = max(t_cmp, t_mem) / t
+        r["us"] = ms * 1e3
+        r["gbs"] = gbs
+        if c["flops"] > 0 and c.get("pipe") != "fma":
+            r["tflops"] = c["flops"] / t / 1e12
+            r["tensor_frac_of_burst"] = c["flops"] / t / 1e12 / pk["bf16_tflops"]
+        out[n] = r
+    return out
+
+
+def host_cpu():
+    """Host CPU threads and model name (lscpu, else the platform module)."""
+    import platform
+    model = None
+    try:
+        txt = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in txt.splitlines():
+            if line.strip().startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    return {"nproc": os.cpu_count(), "model": model or platform.processor() or platform.machine()}
 
 
 # --------------------------------------------------------------- multi-rank
@@ -229,6 +319,9 @@ def run_reference(args, shape, inp):
 
 # ------------------------------------------------------------------ GPU arm
 
+MIN_TIMED_S = 1.0  # the timed region covers whole blocks of K steps, at least this long
+
+
 def run_ours(args, shape, inp):
     import torch
 
@@ -240,10 +333,12 @@ def run_ours(args, shape, inp):
     g = {n: (v.to(dev) if isinstance(v, torch.Tensor) else v) for n, v in inp.items()}
     layer = m.MoELayer(T, H, I, E, k, shape.ep_size, device=dev)
     stream = torch.cuda.current_stream(dev)
+    ws_dw2 = torch.empty_like(layer.ws_gemm_bwd)
 
-    # per-call events: (name, start, end) recorded on the launching stream
-    names = ["route", "dispatch", "gate_up", "down", "combine", "combine_bwd", "down_bwd",
-             "gate_up_bwd", "dispatch_bwd", "route_bwd"]
+    # per-call events: (name, start, end) recorded on the launching stream;
+    # the backward GEMM calls run as their dX and weight-gradient halves
+    names = ["route", "dispatch", "gate_up", "down", "combine", "combine_bwd", "down_bwd_dx", "down_bwd_dw",
+             "gate_up_bwd_dx", "gate_up_bwd_dw", "dispatch_bwd", "route_bwd"]
 
     def step(ev=None):
         def mark(i):
@@ -259,37 +354,57 @@ def run_ours(args, shape, inp):
         layer.combine(); mark(5)
         m.moe_combine_bwd(g["dy"], layer.y_perm, layer.topk_w, layer.row_of_slot, T, H, k, layer.dy_perm,
                           layer.d_w); mark(6)
-        m.moe_grouped_gemm_down_bwd(layer.dy_perm, layer.h, layer.gu, g["Wd"], E, layer.offsets, None, R, H,
-                                    I, E, layer.dgu, layer.dWd, 0, layer.ws_gemm_bwd); mark(7)
-        m.moe_grouped_gemm_swiglu_bwd(layer.dgu, layer.x_perm, g["Wg"], g["Wu"], E, layer.offsets, None, R,
-                                      H, I, E, layer.dx_perm, layer.dWg, layer.dWu, 0,
-                                      layer.ws_gemm_bwd); mark(8)
-        m.moe_dispatch_bwd(layer.dx_perm, layer.row_of_slot, T, H, k, layer.dx_acc); mark(9)
+        m.moe_grouped_gemm_down_bwd_dx(layer.dy_perm, layer.gu, g["Wd"], E, layer.offsets, None, R, H, I, E,
+                                       layer.dgu); mark(7)
+        m.moe_grouped_gemm_down_bwd_dw(layer.dy_perm, layer.h, E, layer.offsets, None, R, H, I, E, layer.dWd, 0,
+                                       layer.ws_gemm_bwd); mark(8)
+        m.moe_grouped_gemm_swiglu_bwd_dx(layer.dgu, g["Wg"], g["Wu"], E, layer.offsets, None, R, H, I, E,
+                                         layer.dx_perm); mark(9)
+        m.moe_grouped_gemm_swiglu_bwd_dw(layer.dgu, layer.x_perm, E, layer.offsets, None, R, H, I, E, layer.dWg,
+                                         layer.dWu, 0, ws_dw2); mark(10)
+        m.moe_dispatch_bwd(layer.dx_perm, layer.row_of_slot, T, H, k, layer.dx_acc); mark(11)
         m.moe_route_topk_bwd(layer.d_w, layer.topk_w, layer.topk_idx, g["x"], g["Wr"], layer.dx_acc, T, H,
-                             E, k, layer.dWr, layer.dx, 0, layer.ws_route_bwd); mark(10)
+                             E, k, layer.dWr, layer.dx, 0, layer.ws_route_bwd); mark(12)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     if m.moe_read_device_status(reset=True) != 0:
         raise RuntimeError("device status word set during warm-up")
+    # one untimed block of K steps sizes the timed region: whole blocks of K
+    # steps, at least MIN_TIMED_S long, so that the clock samples see the load
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    for _ in range(args.steps):
+        step()
+    p1.record(stream)
+    torch.cuda.synchronize(dev)
+    block_s = max(p0.elapsed_time(p1) * 1e-3, 1e-6)
+    reps = max(1, min(200, int(-(-MIN_TIMED_S // block_s))))
+    reps = int(max_over_ranks(float(reps), dist, dev))
+    n_timed = reps * args.steps
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(11)] for _ in range(args.steps)]
+    nev = len(names) + 1
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(n_timed)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist, dev)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
-        time.sleep(0.1)
         t_start.record(stream)
-        for i in range(args.steps):
+        for i in range(n_timed):
             step(evs[i])
         t_end.record(stream)
         torch.cuda.synchronize(dev)
     barrier(dist, dev)
     ms_local = t_start.elapsed_time(t_end)
     ms = max_over_ranks(ms_local, dist, dev)
-    per_call = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
+    per_call = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n_timed))
                 for j, n in enumerate(names)}
+    if m.moe_read_device_status(reset=True) != 0:
+        raise RuntimeError("device status word set during the timed region")
+    del evs
+
+    fma_tfma = measure_fma_rate(m, dev, stream)
 
     # forward-only throughput at T=4096 (the forward workload)
     from moe_expert_layer_topk_gb300.synth import CONFIGS, make_layer_inputs
@@ -311,6 +426,10 @@ def run_ours(args, shape, inp):
     del flayer
     fp8 = run_fp8_forward(m, fg, fshape, dev, stream, args)
     del fg
+    pk, pk_kind = peaks()
+    extra = {"zipf_fwd": run_fwd_workload(m, "qwen3_30b_zipf_fwd", dev, stream, args, pk),
+             "ep_rank_local": run_ep_rank_local(m, dev, stream, args, pk),
+             "tiny_fwd": run_fwd_workload(m, "tiny_fwd", dev, stream, args, pk)}
 
     # end to end through the public API with host buffers: every step copies
     # its x and dY from pinned host memory and reads its y and dX back.  The
@@ -365,25 +484,23 @@ def run_ours(args, shape, inp):
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(es.elapsed_time(ee), dist, dev) / args.steps
     if m.moe_read_device_status(reset=True) != 0:
-        raise RuntimeError("device status word set during the timed region")
+        raise RuntimeError("device status word set during the end-to-end steps")
 
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
         return
 
-    pk, pk_kind = peaks()
-    fwd_fl, bwd_fl = layer_flops(T, H, I, E, k)
-    gemm_fl = {"gate_up": fwd_fl["gate_up"], "down": fwd_fl["down"], "down_bwd": bwd_fl["down_bwd"],
-               "gate_up_bwd": bwd_fl["gate_up_bwd"]}
-    gemm_ms = sum(per_call[n] for n in gemm_fl)
-    gemm_tflops = sum(gemm_fl.values()) / (gemm_ms * 1e-3) / 1e12
-    # dominant single-kernel call: the forward gate/up GEMM is one launch
-    dom = "gate_up"
-    dom_tflops = gemm_fl[dom] / (per_call[dom] * 1e-3) / 1e12
-    step_ms = ms / args.steps
+    costs = call_costs(T, H, I, E, k)
+    roof = rooflines(per_call, costs, pk, fma_tfma)
+    gemm_calls = ["gate_up", "down", "down_bwd_dx", "down_bwd_dw", "gate_up_bwd_dx", "gate_up_bwd_dw"]
+    gemm_ms = sum(per_call[n] for n in gemm_calls)
+    gemm_tflops = sum(costs[n]["flops"] for n in gemm_calls) / (gemm_ms * 1e-3) / 1e12
+    # dominant kernel: the single-kernel call with the largest measured time
+    dom = max(SINGLE_KERNEL, key=lambda n: per_call[n])
+    dr = roof[dom]
+    step_ms = ms / n_timed
     value = world * T / (step_ms * 1e-3)
-    traffic = recorded_traffic()
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
@@ -391,23 +508,34 @@ def run_ours(args, shape, inp):
         "config": {"workload": WORKLOAD, "T": T, "H": H, "I": I, "E": E, "k": k,
                    "step": "forward+backward (router, dispatch, gate/up+SwiGLU, down, combine and their backward)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (1.2 GB of expert weights per step)"},
+                   "l2": "inputs larger than L2 (1.2 GB of expert weights per step)",
+                   "timed": f"{reps} back-to-back blocks of {args.steps} steps ({n_timed} steps, "
+                            f"{ms_local * 1e-3:.2f} s) between one pair of events"},
+        "timed_steps": n_timed,
         "fwd_tokens_per_s": fshape.T / (fwd_ms * 1e-3),
         "fwd_ms": fwd_ms, "fwd_config": {"workload": FWD_WORKLOAD, "T": fshape.T,
                        "path": "fused dispatch: rows gathered from x by the gate/up GEMM"},
         "fp8_fwd": fp8,
+        **extra,
         "grouped_gemm_tflops": gemm_tflops,
+        "grouped_gemm_frac_of_sustained": gemm_tflops / pk["bf16_tflops_sustained"],
         "per_call_ms": per_call,
-        "roofline": {"bound": "tensor", "kernel": "grouped_gemm gate/up + SwiGLU (forward)",
-                     "achieved": dom_tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": dom_tflops / pk["bf16_tflops"], "peak_source": f"{pk_kind} bf16 burst",
-                     "traffic": traffic},
+        "roofline": {"bound": dr["bound"], "kernel": SINGLE_KERNEL[dom], "call": dom,
+                     "achieved": dr["achieved"], "peak": dr["peak"], "unit": dr["unit"], "frac": dr["frac"],
+                     "peak_source": (f"{pk_kind} HBM copy" if dr["bound"] == "hbm" else
+                                     f"{pk_kind} bf16 sustained"),
+                     "algorithmic_bytes": costs[dom]["bytes"], "algorithmic_flops": costs[dom]["flops"],
+                     "traffic": recorded_traffic(dom),
+                     "traffic_source": "one-pass ncu capture recorded under profiles/ (valid while the GEMM "
+                                       "sources hash as recorded there; else null)"},
+        "rooflines": roof,
+        "fma_peak_tfma_s": fma_tfma,
         "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(hx.numel() * 2 + hdy.numel() * 2),
                 "d2h_bytes_per_step": int(hy.numel() * 2 + hdx.numel() * 2),
                 "copies": "pinned host x, dY in and y, dX out every step, on two copy streams; "
                           "step i+1's inputs and step i-1's outputs move during step i"},
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": KERNELS_PER_STEP * n_timed,
         "clocks": clk.summary(),
     }
     if args.cpu_baseline:
@@ -415,12 +543,112 @@ def run_ours(args, shape, inp):
         oracle_sample_step(inp, args.cpu_tokens)
         dt = time.perf_counter() - t0
         line["cpu_baseline"] = {"value": args.cpu_tokens / dt, "unit": "tokens/s", "cores": cpu_cores_used(),
-                                "kind": "oracle",
+                                "host": host_cpu(), "kind": "oracle",
                                 "sample": f"first {args.cpu_tokens} tokens of {WORKLOAD}, forward+backward, "
                                           f"single-threaded C oracle, {dt:.1f} s"}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def measure_fma_rate(m, dev, stream):
+    """fp32 FMA rate of this GPU (TFMA/s) from the library's FMA-chain probe:
+    the best of a few launches, scalar and packed two-lane FMAs, timed with
+    events."""
+    import torch
+    out = torch.zeros(1, dtype=torch.float32, device=dev)
+    best = 0.0
+    for packed in (0, 1, 0, 1, 0, 1):
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        n = m.moe_probe_fma(packed, 4, 256, out)
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        best = max(best, n / (s0.elapsed_time(s1) * 1e-3) / 1e12)
+    return best
+
+
+def _timed_calls(calls, steps, warmup, stream, dev):
+    """Mean per-call and per-step milliseconds of `calls` (name -> fn) run in
+    order, `steps` times after `warmup` untimed passes, events on `stream`."""
+    import torch
+    for _ in range(warmup):
+        for f in calls.values():
+            f()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        evs[i][0].record(stream)
+        for j, f in enumerate(calls.values()):
+            f()
+            evs[i][j + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    per = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps))
+           for j, n in enumerate(calls)}
+    step_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][-1]) for i in range(steps))
+    return per, step_ms
+
+
+def run_fwd_workload(m, name, dev, stream, args, pk):
+    """Forward of a routed workload (route, dispatch, gate/up, down, combine)
+    on the permuted-row path, each call bracketed by events."""
+    import torch
+    from moe_expert_layer_topk_gb300.synth import CONFIGS, make_layer_inputs
+    shape = CONFIGS[name]
+    fin = make_layer_inputs(shape, 0)
+    g = {n: (v.to(dev) if isinstance(v, torch.Tensor) else v) for n, v in fin.items()}
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    L = m.MoELayer(T, H, I, E, k, shape.ep_size, training=False, device=dev)
+    R = L.R
+    calls = {"route": lambda: L.route(g["x"], g["Wr"], g["bias"]),
+             "dispatch": lambda: L.dispatch(g["x"]),
+             "gate_up": lambda: m.moe_grouped_gemm_swiglu(L.x_perm, g["Wg"], g["Wu"], E, L.offsets, None, R, H, I,
+                                                          E, L.h, None),
+             "down": lambda: m.moe_grouped_gemm_down(L.h, g["Wd"], E, L.offsets, None, R, H, I, E, L.y_perm),
+             "combine": lambda: L.combine()}
+    per, step_ms = _timed_calls(calls, args.steps, args.warmup, stream, dev)
+    if m.moe_read_device_status(reset=True) != 0:
+        raise RuntimeError(f"device status word set during {name}")
+    counts = L.counts.cpu()
+    fl_gu, fl_dn = 2.0 * R * H * 2 * I, 2.0 * R * I * H
+    gemm_tf = (fl_gu + fl_dn) / ((per["gate_up"] + per["down"]) * 1e-3) / 1e12
+    out = {"workload": name, "T": T, "H": H, "I": I, "E": E, "k": k, "tokens_per_s": T / (step_ms * 1e-3),
+           "ms": step_ms, "per_call_ms": per, "path": "permuted rows (dispatch writes x_perm)",
+           "gate_up_tflops": fl_gu / (per["gate_up"] * 1e-3) / 1e12,
+           "down_tflops": fl_dn / (per["down"] * 1e-3) / 1e12, "grouped_gemm_tflops": gemm_tf,
+           "grouped_gemm_frac_of_burst": gemm_tf / pk["bf16_tflops"],
+           "empty_experts": int((counts == 0).sum()), "max_expert_rows": int(counts.max())}
+    if shape.bias == "zipf":
+        out["routing"] = "Zipf(1.2) expert popularity from a router bias, 4 experts forced empty"
+    return out
+
+
+def run_ep_rank_local(m, dev, stream, args, pk):
+    """One EP rank's local expert compute: 32768 received rows in 8 source-rank
+    blocks x 16 local experts (128 segments), gate/up + SwiGLU and down."""
+    import torch
+    from moe_expert_layer_topk_gb300.synth import CONFIGS, make_segment_inputs
+    shape = CONFIGS["ep_rank_local"]
+    s = make_segment_inputs(shape, 0)
+    g = {n: (v.to(dev) if isinstance(v, torch.Tensor) else v) for n, v in s.items()}
+    R, H, I, E, S = s["R"], s["H"], s["I"], s["E"], s["num_seg"]
+    h = torch.empty(R, I, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
+    so, se = g["seg_offsets"], g["seg_expert"]
+    calls = {"gate_up": lambda: m.moe_grouped_gemm_swiglu(g["x_perm"], g["Wg"], g["Wu"], S, so, se, R, H, I, E, h,
+                                                          None),
+             "down": lambda: m.moe_grouped_gemm_down(h, g["Wd"], S, so, se, R, H, I, E, y)}
+    per, step_ms = _timed_calls(calls, args.steps, args.warmup, stream, dev)
+    if m.moe_read_device_status(reset=True) != 0:
+        raise RuntimeError("device status word set during ep_rank_local")
+    fl_gu, fl_dn = 2.0 * R * H * 2 * I, 2.0 * R * I * H
+    gemm_tf = (fl_gu + fl_dn) / (step_ms * 1e-3) / 1e12
+    return {"workload": "ep_rank_local", "rows": R, "H": H, "I": I, "local_experts": E, "segments": S,
+            "rows_per_s": R / (step_ms * 1e-3), "ms": step_ms, "per_call_ms": per,
+            "gate_up_tflops": fl_gu / (per["gate_up"] * 1e-3) / 1e12,
+            "down_tflops": fl_dn / (per["down"] * 1e-3) / 1e12, "grouped_gemm_tflops": gemm_tf,
+            "grouped_gemm_frac_of_burst": gemm_tf / pk["bf16_tflops"],
+            "weights_bytes": 3 * E * I * H * 2}
 
 
 def run_fp8_forward(m, fg, fshape, dev, stream, args):
@@ -485,10 +713,12 @@ def run_fp8_forward(m, fg, fshape, dev, stream, args):
 
 
 # kernels launched per step by the calls in run_ours.step():
-# route 4 (zero counters, partial logits, top-k, offsets), dispatch 3,
-# gate/up 1, down 1, combine 1, combine_bwd 1, down_bwd 3 and gate/up bwd 3
-# (dX GEMM, segment maps, dW GEMM), dispatch_bwd 1, route_bwd 7
-KERNELS_PER_STEP = 4 + 3 + 1 + 1 + 1 + 1 + 3 + 3 + 1 + 7
+# route 4 (partial logits, top-k with per-chunk counts, chunk scan, offsets),
+# dispatch 1 (rows from the route's chunk prefixes),
+# gate/up 1, down 1, combine 1, combine_bwd 1, the dX halves 1 each and the
+# weight-gradient halves 2 each (segment maps, dW GEMM), dispatch_bwd 1,
+# route_bwd 7
+KERNELS_PER_STEP = 4 + 1 + 1 + 1 + 1 + 1 + 3 + 3 + 1 + 7
 
 
 def run_profile_router(args):

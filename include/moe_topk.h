@@ -114,13 +114,31 @@ int moe_read_device_status(int* status, int reset, void* stream);
  * offsets int32 [E+1], rank_offsets int32 [ep_size+1].
  * No capacity limit: every token keeps all k experts.  T == 0 is allowed.
  * The workspace holds the fp32 block sums of the logits, ceil(H/256) x T x E,
- * and one 128-byte slot-counter line per expert.
+ * the slot total of every expert and the per-chunk slot counts described at
+ * moe_route_topk_chunks.
  * ---------------------------------------------------------------------- */
 size_t moe_route_topk_workspace_size(int T, int H, int E);
 int moe_route_topk(const void* x, const float* Wr, const float* bias, int T, int H, int E, int k,
                    int ep_size, int32_t* topk_idx, float* topk_w, int32_t* counts,
                    int32_t* offsets, int32_t* rank_offsets, void* ws, size_t ws_bytes,
                    void* stream);
+
+/* A1 + A2 as above, also returning where dispatch starts each chunk of 16
+ * tokens in each expert's rows:
+ *   chunk_prefix[e][c] = number of slots routed to expert e by tokens
+ *                        0 .. 16c-1   (int32 [E][ceil(T/16)], c = chunk)
+ * so the first row of chunk c's slots in expert e is offsets[e] +
+ * chunk_prefix[e][c] (rows stable by token, "FSDPTurbo EP/EFSDP and
+ * LlamaFactory FSDP2/CP Design", section 3, the permute step).  With it,
+ * moe_dispatch_chunked permutes in one kernel instead of ranking the slots
+ * again.  chunk_prefix may be NULL only when T == 0.  The workspace
+ * (moe_route_topk_chunks_workspace_size) holds the logit block sums and the
+ * expert totals only. */
+size_t moe_route_topk_chunks_workspace_size(int T, int H, int E);
+int moe_route_topk_chunks(const void* x, const float* Wr, const float* bias, int T, int H, int E, int k,
+                          int ep_size, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                          int32_t* rank_offsets, int32_t* chunk_prefix, void* ws, size_t ws_bytes,
+                          void* stream);
 
 /* ------------------------------------------------------------------------
  * A3  dispatch (permute).
@@ -140,6 +158,17 @@ size_t moe_dispatch_workspace_size(int T, int E, int k);
 int moe_dispatch(const void* x, const int32_t* topk_idx, const int32_t* offsets, int T, int H,
                  int E, int k, void* x_perm, int32_t* row_of_slot, int32_t* token_of_row,
                  void* ws, size_t ws_bytes, void* stream);
+
+/* A3 with the chunk prefixes of moe_route_topk_chunks: the same rows,
+ * row_of_slot, token_of_row and x_perm as moe_dispatch (bit for bit), in
+ * one kernel and with no workspace; the route already counted the slots of
+ * every chunk of 16 tokens per expert.  chunk_prefix int32 [E][ceil(T/16)]
+ * and offsets from the same moe_route_topk_chunks call.  x_perm may be NULL
+ * (indices only).  A row outside [0, T*k) that inconsistent inputs would
+ * give is skipped and sets MOE_STATUS_BAD_INDEX. */
+int moe_dispatch_chunked(const void* x, const int32_t* topk_idx, const int32_t* offsets,
+                         const int32_t* chunk_prefix, int T, int H, int E, int k, void* x_perm,
+                         int32_t* row_of_slot, int32_t* token_of_row, void* stream);
 
 /* moe_dispatch without a workspace (the pages have no counterpart to this
  * entry point; it is a convenience of this library).
@@ -237,6 +266,12 @@ int moe_dispatch_e4m3(const void* x, const int32_t* topk_idx, const int32_t* off
                       int E, int k, void* xq_perm, float* xs_perm, int32_t* row_of_slot,
                       int32_t* token_of_row, void* ws, size_t ws_bytes, void* stream);
 
+/* moe_dispatch_e4m3 with the chunk prefixes of moe_route_topk_chunks (as
+ * moe_dispatch_chunked): the same codes, scales and indices, no workspace. */
+int moe_dispatch_e4m3_chunked(const void* x, const int32_t* topk_idx, const int32_t* offsets,
+                              const int32_t* chunk_prefix, int T, int H, int E, int k, void* xq_perm,
+                              float* xs_perm, int32_t* row_of_slot, int32_t* token_of_row, void* stream);
+
 /* Per-row e4m3 quantisation of a bf16 matrix a [rows, cols] (cols % 8 == 0):
  * q uint8 [rows, cols], scale fp32 [rows].  Bit-exact: codes and scales are
  * a pure function of the input bits.  a 16-byte, q 8-byte and scale 4-byte
@@ -312,6 +347,34 @@ int moe_grouped_gemm_swiglu_bwd(const void* dgu, const void* x_perm, const void*
                                 void* dx_perm, float* dWg, float* dWu, int accumulate, void* ws,
                                 size_t ws_bytes, void* stream);
 
+/* B2 and B3 in two halves each, launched by the calls above back to back.
+ * Issued separately, the dX half (which the all-to-all returns to the
+ * source ranks, "Qwen3-MoE-30B-A3B模型EP+FSDP2并行方案", section
+ * "为什么这么设计") can leave before the weight gradients are computed, and
+ * the weight-gradient GEMM can be timed on its own.  Results are
+ * bit-identical to the combined calls; arguments, layouts and error rules
+ * are theirs.
+ *   moe_grouped_gemm_down_bwd_dx:   dgu from dy_perm, gu_save, Wd (no workspace)
+ *   moe_grouped_gemm_down_bwd_dw:   dWd from dy_perm, h; ws as for moe_grouped_gemm_down_bwd
+ *   moe_grouped_gemm_swiglu_bwd_dx: dx_perm from dgu, Wg, Wu (no workspace)
+ *   moe_grouped_gemm_swiglu_bwd_dw: dWg, dWu from dgu, x_perm; ws as for moe_grouped_gemm_swiglu_bwd
+ * A dW half and a dX half may run concurrently on two streams; two dW calls
+ * that overlap need separate workspaces. */
+int moe_grouped_gemm_down_bwd_dx(const void* dy_perm, const void* gu_save, const void* Wd, int num_seg,
+                                 const int32_t* seg_offsets, const int32_t* seg_expert, int R, int H,
+                                 int I, int E, void* dgu, void* stream);
+int moe_grouped_gemm_down_bwd_dw(const void* dy_perm, const void* h, int num_seg,
+                                 const int32_t* seg_offsets, const int32_t* seg_expert, int R, int H,
+                                 int I, int E, float* dWd, int accumulate, void* ws, size_t ws_bytes,
+                                 void* stream);
+int moe_grouped_gemm_swiglu_bwd_dx(const void* dgu, const void* Wg, const void* Wu, int num_seg,
+                                   const int32_t* seg_offsets, const int32_t* seg_expert, int R, int H,
+                                   int I, int E, void* dx_perm, void* stream);
+int moe_grouped_gemm_swiglu_bwd_dw(const void* dgu, const void* x_perm, int num_seg,
+                                   const int32_t* seg_offsets, const int32_t* seg_expert, int R, int H,
+                                   int I, int E, float* dWg, float* dWu, int accumulate, void* ws,
+                                   size_t ws_bytes, void* stream);
+
 /* B4  dispatch backward: dx_acc[t] = sum_{j=0..k-1} dx_perm[row_of_slot[t,j]] in fp32,
  * increasing j.  dx_perm bf16 [R,H]; dx_acc fp32 [T,H]. */
 int moe_dispatch_bwd(const void* dx_perm, const int32_t* row_of_slot, int T, int H, int k,
@@ -331,6 +394,18 @@ int moe_route_topk_bwd(const float* d_w, const float* topk_w, const int32_t* top
                        const void* x, const float* Wr, const float* dx_acc, int T, int H, int E,
                        int k, float* dWr, void* dx, int accumulate, void* ws, size_t ws_bytes,
                        void* stream);
+
+/* Measurement aid (no counterpart on the pages): launches a kernel whose
+ * threads only run independent fp32 fused multiply-add chains, per_sm CTAs
+ * of 256 threads on every SM, `iters` x 128 FMAs per thread.  Timing it
+ * with events on `stream` gives the fp32 FMA rate this GPU sustains, the
+ * ceiling of the router's partial-logit kernel (whose summation order keeps
+ * it off the tensor cores).  *fmas (host) receives the number of FMAs the
+ * launch performs; out (device, >= 1 float) is written only in a case the
+ * probe's inputs never reach.  packed != 0: the chains advance in pairs by
+ * packed two-lane fp32 FMA instructions (fma.rn.f32x2).  1 <= per_sm <= 32,
+ * 1 <= iters <= 2^20. */
+int moe_probe_fma(int packed, int per_sm, int iters, float* out, long long* fmas, void* stream);
 
 #ifdef __cplusplus
 }

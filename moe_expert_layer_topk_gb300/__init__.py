@@ -18,15 +18,19 @@ import torch
 from . import build as _build_mod
 
 __all__ = ["lib", "MoEError", "LIB_PATH", "ENTRY_POINTS",
-           "moe_route_topk", "moe_dispatch", "moe_dispatch_no_alloc", "moe_grouped_gemm_swiglu",
+           "moe_route_topk", "moe_route_topk_chunks", "moe_route_topk_chunks_workspace_size",
+           "moe_dispatch", "moe_dispatch_chunked", "moe_dispatch_e4m3_chunked", "moe_dispatch_no_alloc",
+           "moe_grouped_gemm_swiglu",
            "moe_grouped_gemm_swiglu_gather", "moe_grouped_gemm_down",
            "moe_quantize_rows_e4m3", "moe_dispatch_e4m3", "moe_grouped_gemm_swiglu_fp8",
            "moe_grouped_gemm_down_fp8",
            "moe_combine", "moe_combine_bwd", "moe_grouped_gemm_down_bwd",
-           "moe_grouped_gemm_swiglu_bwd", "moe_dispatch_bwd", "moe_route_topk_bwd",
+           "moe_grouped_gemm_swiglu_bwd", "moe_grouped_gemm_down_bwd_dx", "moe_grouped_gemm_down_bwd_dw",
+           "moe_grouped_gemm_swiglu_bwd_dx", "moe_grouped_gemm_swiglu_bwd_dw",
+           "moe_dispatch_bwd", "moe_route_topk_bwd",
            "moe_route_topk_workspace_size", "moe_dispatch_workspace_size",
            "moe_route_topk_bwd_workspace_size", "moe_grouped_gemm_bwd_workspace_size",
-           "moe_read_device_status", "moe_abi_version"]
+           "moe_read_device_status", "moe_abi_version", "moe_probe_fma"]
 
 LIB_PATH: Path = _build_mod.LIB
 
@@ -39,7 +43,11 @@ ENTRY_POINTS = {
     "moe_read_device_status": ([_P, _I, _P], _I),
     "moe_route_topk_workspace_size": ([_I, _I, _I], _Z),
     "moe_route_topk": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _Z, _P], _I),
+    "moe_route_topk_chunks_workspace_size": ([_I, _I, _I], _Z),
+    "moe_route_topk_chunks": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P], _I),
     "moe_dispatch_workspace_size": ([_I, _I, _I], _Z),
+    "moe_dispatch_chunked": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
+    "moe_dispatch_e4m3_chunked": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
     "moe_dispatch": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P], _I),
     "moe_dispatch_no_alloc_max_scratch": ([], _Z),
     "moe_dispatch_no_alloc": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
@@ -56,9 +64,14 @@ ENTRY_POINTS = {
     "moe_grouped_gemm_down_bwd": ([_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _Z, _P], _I),
     "moe_grouped_gemm_swiglu_bwd": ([_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _Z, _P],
                                     _I),
+    "moe_grouped_gemm_down_bwd_dx": ([_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P], _I),
+    "moe_grouped_gemm_down_bwd_dw": ([_P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _I, _P, _Z, _P], _I),
+    "moe_grouped_gemm_swiglu_bwd_dx": ([_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P], _I),
+    "moe_grouped_gemm_swiglu_bwd_dw": ([_P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _Z, _P], _I),
     "moe_dispatch_bwd": ([_P, _P, _I, _I, _I, _P, _P], _I),
     "moe_route_topk_bwd_workspace_size": ([_I, _I, _I], _Z),
     "moe_route_topk_bwd": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _Z, _P], _I),
+    "moe_probe_fma": ([_I, _I, _I, _P, ctypes.POINTER(ctypes.c_longlong), _P], _I),
 }
 
 _lib = None
@@ -125,6 +138,10 @@ def moe_route_topk_workspace_size(T, H, E) -> int:
     return lib().moe_route_topk_workspace_size(T, H, E)
 
 
+def moe_route_topk_chunks_workspace_size(T, H, E) -> int:
+    return lib().moe_route_topk_chunks_workspace_size(T, H, E)
+
+
 def moe_dispatch_workspace_size(T, E, k) -> int:
     return lib().moe_dispatch_workspace_size(T, E, k)
 
@@ -148,6 +165,25 @@ def moe_route_topk(x, Wr, bias, T, H, E, k, ep_size, topk_idx, topk_w, counts, o
     _call("moe_route_topk", _ptr(x), _ptr(Wr), _ptr(bias), T, H, E, k, ep_size, _ptr(topk_idx),
           _ptr(topk_w), _ptr(counts), _ptr(offsets), _ptr(rank_offsets), _ptr(ws), _nbytes(ws),
           _stream(stream))
+
+
+def moe_route_topk_chunks(x, Wr, bias, T, H, E, k, ep_size, topk_idx, topk_w, counts, offsets,
+                          rank_offsets, chunk_prefix, ws, stream=None):
+    _call("moe_route_topk_chunks", _ptr(x), _ptr(Wr), _ptr(bias), T, H, E, k, ep_size, _ptr(topk_idx),
+          _ptr(topk_w), _ptr(counts), _ptr(offsets), _ptr(rank_offsets), _ptr(chunk_prefix), _ptr(ws),
+          _nbytes(ws), _stream(stream))
+
+
+def moe_dispatch_chunked(x, topk_idx, offsets, chunk_prefix, T, H, E, k, x_perm, row_of_slot, token_of_row,
+                         stream=None):
+    _call("moe_dispatch_chunked", _ptr(x), _ptr(topk_idx), _ptr(offsets), _ptr(chunk_prefix), T, H, E, k,
+          _ptr(x_perm), _ptr(row_of_slot), _ptr(token_of_row), _stream(stream))
+
+
+def moe_dispatch_e4m3_chunked(x, topk_idx, offsets, chunk_prefix, T, H, E, k, xq_perm, xs_perm, row_of_slot,
+                              token_of_row, stream=None):
+    _call("moe_dispatch_e4m3_chunked", _ptr(x), _ptr(topk_idx), _ptr(offsets), _ptr(chunk_prefix), T, H, E, k,
+          _ptr(xq_perm), _ptr(xs_perm), _ptr(row_of_slot), _ptr(token_of_row), _stream(stream))
 
 
 def moe_dispatch(x, topk_idx, offsets, T, H, E, k, x_perm, row_of_slot, token_of_row, ws,
@@ -229,6 +265,31 @@ def moe_grouped_gemm_swiglu_bwd(dgu, x_perm, Wg, Wu, num_seg, seg_offsets, seg_e
           int(accumulate), _ptr(ws), _nbytes(ws), _stream(stream))
 
 
+def moe_grouped_gemm_down_bwd_dx(dy_perm, gu_save, Wd, num_seg, seg_offsets, seg_expert, R, H, I, E, dgu,
+                                 stream=None):
+    _call("moe_grouped_gemm_down_bwd_dx", _ptr(dy_perm), _ptr(gu_save), _ptr(Wd), num_seg, _ptr(seg_offsets),
+          _ptr(seg_expert), R, H, I, E, _ptr(dgu), _stream(stream))
+
+
+def moe_grouped_gemm_down_bwd_dw(dy_perm, h, num_seg, seg_offsets, seg_expert, R, H, I, E, dWd, accumulate=0,
+                                 ws=None, stream=None):
+    _call("moe_grouped_gemm_down_bwd_dw", _ptr(dy_perm), _ptr(h), num_seg, _ptr(seg_offsets), _ptr(seg_expert),
+          R, H, I, E, _ptr(dWd), int(accumulate), _ptr(ws), _nbytes(ws), _stream(stream))
+
+
+def moe_grouped_gemm_swiglu_bwd_dx(dgu, Wg, Wu, num_seg, seg_offsets, seg_expert, R, H, I, E, dx_perm,
+                                   stream=None):
+    _call("moe_grouped_gemm_swiglu_bwd_dx", _ptr(dgu), _ptr(Wg), _ptr(Wu), num_seg, _ptr(seg_offsets),
+          _ptr(seg_expert), R, H, I, E, _ptr(dx_perm), _stream(stream))
+
+
+def moe_grouped_gemm_swiglu_bwd_dw(dgu, x_perm, num_seg, seg_offsets, seg_expert, R, H, I, E, dWg, dWu,
+                                   accumulate=0, ws=None, stream=None):
+    _call("moe_grouped_gemm_swiglu_bwd_dw", _ptr(dgu), _ptr(x_perm), num_seg, _ptr(seg_offsets),
+          _ptr(seg_expert), R, H, I, E, _ptr(dWg), _ptr(dWu), int(accumulate), _ptr(ws), _nbytes(ws),
+          _stream(stream))
+
+
 def moe_dispatch_bwd(dx_perm, row_of_slot, T, H, k, dx_acc, stream=None):
     _call("moe_dispatch_bwd", _ptr(dx_perm), _ptr(row_of_slot), T, H, k, _ptr(dx_acc),
           _stream(stream))
@@ -244,3 +305,10 @@ def moe_route_topk_bwd(d_w, topk_w, topk_idx, x, Wr, dx_acc, T, H, E, k, dWr, dx
 from .layer import MoELayer  # noqa: E402  (buffers + call sequence over the entry points)
 
 __all__.append("MoELayer")
+
+
+def moe_probe_fma(packed, per_sm, iters, out, stream=None) -> int:
+    """Launch the FMA-rate probe; returns the number of FMAs it performs."""
+    n = ctypes.c_longlong(0)
+    _call("moe_probe_fma", int(packed), int(per_sm), int(iters), _ptr(out), ctypes.byref(n), _stream(stream))
+    return int(n.value)

@@ -52,10 +52,19 @@ inline int check_launch(const char* what) {
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
   return MOE_OK;
 }
+// the same, naming the entry point and the kernel of a multi-kernel call
+inline int check_launch(const char* fn, const char* kernel) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s: %s", fn, kernel, cudaGetErrorString(e));
+  return MOE_OK;
+}
 
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxSegments = 1024;
+// tokens per ranking chunk: the router's top-k CTA and the dispatch row CTA
+// each cover one chunk, and the route's chunk prefixes are per chunk
+constexpr int kRouteChunk = 16;
 
 // Internal entry points shared between translation units (not exported).
 struct GroupedSegs {

@@ -68,9 +68,77 @@ int sm_count() {
   return g_sms[d];
 }
 
+// fp32 FMA rate probe: every thread runs kChains independent fused
+// multiply-add chains for `iters` x 16 steps (8 warps per CTA, `per_sm` CTAs
+// per SM), so the issue slots of all four schedulers of every SM fill with
+// FMAs.  kPacked: the chains advance in pairs, one packed two-lane fp32 FMA
+// instruction (fma.rn.f32x2) per pair.
+constexpr int kProbeThreads = 256;
+constexpr int kProbeChains = 8;
+
+template <bool kPacked>
+__global__ void __launch_bounds__(kProbeThreads) fma_probe_kernel(int iters, float m, float c, float* out) {
+  float a[kProbeChains];
+#pragma unroll
+  for (int i = 0; i < kProbeChains; ++i) a[i] = (float)(threadIdx.x + i);
+  if constexpr (kPacked) {
+    uint64_t v[kProbeChains / 2];
+    const float2 mm = make_float2(m, m), cc = make_float2(c, c);
+    const uint64_t mv = *reinterpret_cast<const uint64_t*>(&mm), cv = *reinterpret_cast<const uint64_t*>(&cc);
+#pragma unroll
+    for (int i = 0; i < kProbeChains / 2; ++i) {
+      const float2 p = make_float2(a[2 * i], a[2 * i + 1]);
+      v[i] = *reinterpret_cast<const uint64_t*>(&p);
+    }
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+#pragma unroll
+        for (int i = 0; i < kProbeChains / 2; ++i)
+          asm volatile("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(v[i]) : "l"(mv), "l"(cv));
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kProbeChains / 2; ++i) {
+      const float2 p = *reinterpret_cast<const float2*>(&v[i]);
+      a[2 * i] = p.x;
+      a[2 * i + 1] = p.y;
+    }
+  } else {
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+#pragma unroll
+        for (int i = 0; i < kProbeChains; ++i) a[i] = fmaf(a[i], m, c);
+      }
+    }
+  }
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kProbeChains; ++i) s += a[i];
+  if (s == 12345.678f) out[0] = s;  // keeps the chains alive; never true for the probe's inputs
+}
+
 }  // namespace moe
 
 extern "C" {
+
+int moe_probe_fma(int packed, int per_sm, int iters, float* out, long long* fmas, void* stream) {
+  moe::clear_error();
+  if (per_sm < 1 || per_sm > 32 || iters < 1 || iters > (1 << 20) || !out || !fmas)
+    return moe::fail(MOE_ERR_INVALID_ARG,
+                     "moe_probe_fma: need 1<=per_sm<=32, 1<=iters<=2^20, out and fmas");
+  const int sms = moe::sm_count();
+  if (sms <= 0) return moe::fail(MOE_ERR_CUDA, "moe_probe_fma: cannot query the SM count");
+  const int grid = sms * per_sm;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (packed)
+    moe::fma_probe_kernel<true><<<grid, moe::kProbeThreads, 0, s>>>(iters, 0.999f, 1e-3f, out);
+  else
+    moe::fma_probe_kernel<false><<<grid, moe::kProbeThreads, 0, s>>>(iters, 0.999f, 1e-3f, out);
+  *fmas = (long long)grid * moe::kProbeThreads * moe::kProbeChains * 16 * (long long)iters;
+  return moe::check_launch("moe_probe_fma");
+}
 
 int moe_abi_version(void) { return 102; }
 

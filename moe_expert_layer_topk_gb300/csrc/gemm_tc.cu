@@ -37,13 +37,15 @@
 // row (64 bf16 or 128 e4m3 elements), 4-stage shared-memory ring (3 for the
 // router dX kind, whose epilogue stages its addend), two 256-column
 // accumulators in TMEM so the epilogue of tile i overlaps the MMAs of tile
-// i+1.  GATE_UP_FWD and GATE_UP_BWD_DX run as cluster pairs (tcgen05
-// cta_group::2, 256-row tiles).
+// i+1.  GATE_UP_BWD_DX, and GATE_UP_FWD in the dispatch layout (one segment
+// per expert), run as cluster pairs (tcgen05 cta_group::2, 256-row tiles).
 //
 // Every wait on an mbarrier is bounded (globaltimer): on timeout the CTA
 // records MOE_STATUS_TIMEOUT, all roles leave their loops, outstanding MMAs
 // are drained with a bounded wait and TMEM is freed before returning.
 #include <cuda.h>
+
+#include <initializer_list>
 
 #include "tc_common.cuh"
 
@@ -956,12 +958,12 @@ __global__ void dw_segment_maps_kernel(const __grid_constant__ CUtensorMap tplA,
 
 int pick_bn(int n) { return n % 256 == 0 ? 256 : (n % 128 == 0 ? 128 : 64); }
 
-// Cluster pairs (256-row tiles) pay off where they were measured faster: the
-// gate/up backward dX GEMM (K = 2I, MN-major B).  Other kinds run one CTA
-// per 128-row tile.
+// Cluster pairs (256-row tiles) need at least 128 output columns per tile
+// (64 per CTA).  They are used where they measured faster: the gate/up
+// backward dX GEMM always, and the gate/up forward GEMM on permuted rows in
+// the dispatch layout (see swiglu_impl).  Every other kind runs one CTA per
+// 128-row tile.
 bool use_pair(int bn) { return bn >= 128; }
-template <int KIND>
-bool pair_for(int bn) { return KIND == GATE_UP_BWD_DX && use_pair(bn); }
 
 bool g_attr[kNumKinds][2][64] = {};
 
@@ -1112,6 +1114,7 @@ int launch_dense_add_bf16(const void* A, const void* B, const float* add, void* 
 }
 
 size_t dw_split_maps_bytes(int num_seg) { return (size_t)num_seg * tc::kSegMapBytes; }
+
 
 int launch_dw_split(const void* A, const void* B, int K_rows, int M, int N,
                     const int32_t* seg_offsets, int num_seg, float* out, void* maps,
@@ -1345,41 +1348,46 @@ int moe_grouped_gemm_down(const void* h, const void* Wd, int num_seg, const int3
   return run<DOWN_FWD>(pair, p, ta, tb, tb, to, to, static_cast<cudaStream_t>(stream), fn);
 }
 
-int moe_grouped_gemm_down_bwd(const void* dy_perm, const void* h, const void* gu_save,
-                              const void* Wd, int num_seg, const int32_t* seg_offsets,
-                              const int32_t* seg_expert, int R, int H, int I, int E, void* dgu,
-                              float* dWd, int accumulate, void* ws, size_t ws_bytes, void* stream) {
-  clear_error();
-  const char* fn = "moe_grouped_gemm_down_bwd";
-  if (int rc = check_grouped(fn, num_seg, seg_offsets, R, H, I, E)) return rc;
-  if (!dy_perm || !h || !gu_save || !Wd || !dgu || !dWd)
-    return fail(MOE_ERR_INVALID_ARG, "%s: NULL pointer argument", fn);
-  if (!aligned16(dy_perm) || !aligned16(h) || !aligned16(gu_save) || !aligned16(Wd) ||
-      !aligned16(dgu) || !aligned16(dWd))
-    return fail(MOE_ERR_ALIGNMENT, "%s: tensors must be 16-byte aligned", fn);
-  if (int rc = check_bwd_ws(fn, num_seg, ws, ws_bytes)) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (R > 0 && num_seg > 0) {
-    // dgu = SwiGLU'(dy_perm . Wd[e])
-    Params p = base_params(num_seg, seg_offsets, seg_expert, E);
-    p.M = R;
-    p.N = I;
-    p.K = H;
-    p.BN = pick_bn(I);
-    p.n_tiles = I / p.BN;
-    p.b_group_rows = H;
-    p.I = I;
-    p.out0 = dgu;
-    p.aux = gu_save;
-    CUtensorMap ta, tb;
-    if (int rc = make_tmap(&ta, dy_perm, H, R, 64, BM)) return rc;
-    if (int rc = make_tmap_mn(&tb, Wd, I, (uint64_t)E * H, p.BN / 64)) return rc;
-    CUtensorMap to;
-    if (int rc = make_out_map(&to, dgu, 2 * I, R, false)) return rc;
-    if (int rc = run<DOWN_BWD_DX>(false, p, ta, tb, tb, to, to, s, fn))
-      return rc;
-  }
-  // dWd[e] = dy_perm[rows of e]^T . h[rows of e]
+// B2 and B3 each run as two halves: the dX GEMM (rows x weights, with the
+// SwiGLU backward in the down half's epilogue) and the weight-gradient GEMM
+// (the per-segment operand maps, then the DW kind).  The combined entry
+// points launch both on the same stream.
+
+static int check_bwd_ptrs(const char* fn, std::initializer_list<const void*> ptrs) {
+  for (const void* q : ptrs)
+    if (!q) return fail(MOE_ERR_INVALID_ARG, "%s: NULL pointer argument", fn);
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return fail(MOE_ERR_ALIGNMENT, "%s: tensors must be 16-byte aligned", fn);
+  return MOE_OK;
+}
+
+// dgu = SwiGLU'(dy_perm . Wd[e])
+static int down_bwd_dx(const void* dy_perm, const void* gu_save, const void* Wd, int num_seg,
+                       const int32_t* seg_offsets, const int32_t* seg_expert, int R, int H, int I, int E,
+                       void* dgu, cudaStream_t s, const char* fn) {
+  if (R == 0 || num_seg == 0) return MOE_OK;
+  Params p = base_params(num_seg, seg_offsets, seg_expert, E);
+  p.M = R;
+  p.N = I;
+  p.K = H;
+  p.BN = pick_bn(I);
+  p.n_tiles = I / p.BN;
+  p.b_group_rows = H;
+  p.I = I;
+  p.out0 = dgu;
+  p.aux = gu_save;
+  CUtensorMap ta, tb;
+  if (int rc = make_tmap(&ta, dy_perm, H, R, 64, BM)) return rc;
+  if (int rc = make_tmap_mn(&tb, Wd, I, (uint64_t)E * H, p.BN / 64)) return rc;
+  CUtensorMap to;
+  if (int rc = make_out_map(&to, dgu, 2 * I, R, false)) return rc;
+  return run<DOWN_BWD_DX>(false, p, ta, tb, tb, to, to, s, fn);
+}
+
+// dWd[e] = dy_perm[rows of e]^T . h[rows of e]
+static int down_bwd_dw(const void* dy_perm, const void* h, int num_seg, const int32_t* seg_offsets,
+                       const int32_t* seg_expert, int R, int H, int I, int E, float* dWd, int accumulate,
+                       void* ws, cudaStream_t s, const char* fn) {
   if (num_seg == 0) {
     if (accumulate) return MOE_OK;
     cudaError_t e = cudaMemsetAsync(dWd, 0, sizeof(float) * (size_t)E * H * I, s);
@@ -1396,53 +1404,45 @@ int moe_grouped_gemm_down_bwd(const void* dy_perm, const void* h, const void* gu
   p.out0 = dWd;
   CUtensorMap to;
   if (int rc = make_out_map(&to, dWd, I, (uint64_t)E * H, true)) return rc;
-  return run_dw(pair_for<DW>(p.BN), p, dy_perm, h, to, to, ws, s, fn);
+  return run_dw(false, p, dy_perm, h, to, to, ws, s, fn);
 }
 
-int moe_grouped_gemm_swiglu_bwd(const void* dgu, const void* x_perm, const void* Wg,
-                                const void* Wu, int num_seg, const int32_t* seg_offsets,
-                                const int32_t* seg_expert, int R, int H, int I, int E,
-                                void* dx_perm, float* dWg, float* dWu, int accumulate, void* ws,
-                                size_t ws_bytes, void* stream) {
-  clear_error();
-  const char* fn = "moe_grouped_gemm_swiglu_bwd";
-  if (int rc = check_grouped(fn, num_seg, seg_offsets, R, H, I, E)) return rc;
-  if (!dgu || !x_perm || !Wg || !Wu || !dx_perm || !dWg || !dWu)
-    return fail(MOE_ERR_INVALID_ARG, "%s: NULL pointer argument", fn);
-  if (!aligned16(dgu) || !aligned16(x_perm) || !aligned16(Wg) || !aligned16(Wu) ||
-      !aligned16(dx_perm) || !aligned16(dWg) || !aligned16(dWu))
-    return fail(MOE_ERR_ALIGNMENT, "%s: tensors must be 16-byte aligned", fn);
-  if (int rc = check_bwd_ws(fn, num_seg, ws, ws_bytes)) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (R > 0 && num_seg > 0) {
-    // dx_perm = [dg du] . [Wg[e]; Wu[e]]
-    Params p = base_params(num_seg, seg_offsets, seg_expert, E);
-    p.M = R;
-    p.N = H;
-    p.K = 2 * I;
-    p.BN = pick_bn(H);
-    p.n_tiles = H / p.BN;
-    p.b_group_rows = I;
-    p.I = I;
-    p.ldo = H;
-    p.out0 = dx_perm;
-    CUtensorMap ta, tg, tu;
-    if (int rc = make_tmap(&ta, dgu, 2 * I, R, 64, BM)) return rc;
-    const uint32_t nck = p.BN / 64 / (pair_for<GATE_UP_BWD_DX>(p.BN) ? 2 : 1);
-    if (int rc = make_tmap_mn(&tg, Wg, H, (uint64_t)E * I, nck)) return rc;
-    if (int rc = make_tmap_mn(&tu, Wu, H, (uint64_t)E * I, nck)) return rc;
-    CUtensorMap to;
-    if (int rc = make_out_map(&to, dx_perm, H, R, false)) return rc;
-    if (int rc = run<GATE_UP_BWD_DX>(pair_for<GATE_UP_BWD_DX>(p.BN), p, ta, tg, tu, to, to, s, fn))
-      return rc;
-  }
+// dx_perm = [dg du] . [Wg[e]; Wu[e]]
+static int swiglu_bwd_dx(const void* dgu, const void* Wg, const void* Wu, int num_seg,
+                         const int32_t* seg_offsets, const int32_t* seg_expert, int R, int H, int I, int E,
+                         void* dx_perm, cudaStream_t s, const char* fn) {
+  if (R == 0 || num_seg == 0) return MOE_OK;
+  Params p = base_params(num_seg, seg_offsets, seg_expert, E);
+  p.M = R;
+  p.N = H;
+  p.K = 2 * I;
+  p.BN = pick_bn(H);
+  p.n_tiles = H / p.BN;
+  p.b_group_rows = I;
+  p.I = I;
+  p.ldo = H;
+  p.out0 = dx_perm;
+  const bool pair = use_pair(p.BN);
+  CUtensorMap ta, tg, tu;
+  if (int rc = make_tmap(&ta, dgu, 2 * I, R, 64, BM)) return rc;
+  const uint32_t nck = p.BN / 64 / (pair ? 2 : 1);
+  if (int rc = make_tmap_mn(&tg, Wg, H, (uint64_t)E * I, nck)) return rc;
+  if (int rc = make_tmap_mn(&tu, Wu, H, (uint64_t)E * I, nck)) return rc;
+  CUtensorMap to;
+  if (int rc = make_out_map(&to, dx_perm, H, R, false)) return rc;
+  return run<GATE_UP_BWD_DX>(pair, p, ta, tg, tu, to, to, s, fn);
+}
+
+// [dWg[e]; dWu[e]] = dgu[rows of e]^T . x_perm[rows of e]   (M = 2I split at I)
+static int swiglu_bwd_dw(const void* dgu, const void* x_perm, int num_seg, const int32_t* seg_offsets,
+                         const int32_t* seg_expert, int R, int H, int I, int E, float* dWg, float* dWu,
+                         int accumulate, void* ws, cudaStream_t s, const char* fn) {
   if (num_seg == 0) {
     if (accumulate) return MOE_OK;
     cudaError_t e = cudaMemsetAsync(dWg, 0, sizeof(float) * (size_t)E * I * H, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(dWu, 0, sizeof(float) * (size_t)E * I * H, s);
     return e == cudaSuccess ? MOE_OK : fail(MOE_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
   }
-  // [dWg[e]; dWu[e]] = dgu[rows of e]^T . x_perm[rows of e]   (M = 2I split at I)
   Params p = base_params(num_seg, seg_offsets, seg_expert, E);
   p.M = 2 * I;
   p.N = H;
@@ -1457,7 +1457,87 @@ int moe_grouped_gemm_swiglu_bwd(const void* dgu, const void* x_perm, const void*
   CUtensorMap tog, tou;
   if (int rc = make_out_map(&tog, dWg, H, (uint64_t)E * I, true)) return rc;
   if (int rc = make_out_map(&tou, dWu, H, (uint64_t)E * I, true)) return rc;
-  return run_dw(pair_for<DW>(p.BN), p, dgu, x_perm, tog, tou, ws, s, fn);
+  return run_dw(false, p, dgu, x_perm, tog, tou, ws, s, fn);
+}
+
+int moe_grouped_gemm_down_bwd(const void* dy_perm, const void* h, const void* gu_save,
+                              const void* Wd, int num_seg, const int32_t* seg_offsets,
+                              const int32_t* seg_expert, int R, int H, int I, int E, void* dgu,
+                              float* dWd, int accumulate, void* ws, size_t ws_bytes, void* stream) {
+  clear_error();
+  const char* fn = "moe_grouped_gemm_down_bwd";
+  if (int rc = check_grouped(fn, num_seg, seg_offsets, R, H, I, E)) return rc;
+  if (int rc = check_bwd_ptrs(fn, {dy_perm, h, gu_save, Wd, dgu, dWd})) return rc;
+  if (int rc = check_bwd_ws(fn, num_seg, ws, ws_bytes)) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (int rc = down_bwd_dx(dy_perm, gu_save, Wd, num_seg, seg_offsets, seg_expert, R, H, I, E, dgu, s, fn))
+    return rc;
+  return down_bwd_dw(dy_perm, h, num_seg, seg_offsets, seg_expert, R, H, I, E, dWd, accumulate, ws, s, fn);
+}
+
+int moe_grouped_gemm_down_bwd_dx(const void* dy_perm, const void* gu_save, const void* Wd, int num_seg,
+                                 const int32_t* seg_offsets, const int32_t* seg_expert, int R, int H,
+                                 int I, int E, void* dgu, void* stream) {
+  clear_error();
+  const char* fn = "moe_grouped_gemm_down_bwd_dx";
+  if (int rc = check_grouped(fn, num_seg, seg_offsets, R, H, I, E)) return rc;
+  if (int rc = check_bwd_ptrs(fn, {dy_perm, gu_save, Wd, dgu})) return rc;
+  return down_bwd_dx(dy_perm, gu_save, Wd, num_seg, seg_offsets, seg_expert, R, H, I, E, dgu,
+                     static_cast<cudaStream_t>(stream), fn);
+}
+
+int moe_grouped_gemm_down_bwd_dw(const void* dy_perm, const void* h, int num_seg,
+                                 const int32_t* seg_offsets, const int32_t* seg_expert, int R, int H,
+                                 int I, int E, float* dWd, int accumulate, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  clear_error();
+  const char* fn = "moe_grouped_gemm_down_bwd_dw";
+  if (int rc = check_grouped(fn, num_seg, seg_offsets, R, H, I, E)) return rc;
+  if (int rc = check_bwd_ptrs(fn, {dy_perm, h, dWd})) return rc;
+  if (int rc = check_bwd_ws(fn, num_seg, ws, ws_bytes)) return rc;
+  return down_bwd_dw(dy_perm, h, num_seg, seg_offsets, seg_expert, R, H, I, E, dWd, accumulate, ws,
+                     static_cast<cudaStream_t>(stream), fn);
+}
+
+int moe_grouped_gemm_swiglu_bwd(const void* dgu, const void* x_perm, const void* Wg,
+                                const void* Wu, int num_seg, const int32_t* seg_offsets,
+                                const int32_t* seg_expert, int R, int H, int I, int E,
+                                void* dx_perm, float* dWg, float* dWu, int accumulate, void* ws,
+                                size_t ws_bytes, void* stream) {
+  clear_error();
+  const char* fn = "moe_grouped_gemm_swiglu_bwd";
+  if (int rc = check_grouped(fn, num_seg, seg_offsets, R, H, I, E)) return rc;
+  if (int rc = check_bwd_ptrs(fn, {dgu, x_perm, Wg, Wu, dx_perm, dWg, dWu})) return rc;
+  if (int rc = check_bwd_ws(fn, num_seg, ws, ws_bytes)) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (int rc = swiglu_bwd_dx(dgu, Wg, Wu, num_seg, seg_offsets, seg_expert, R, H, I, E, dx_perm, s, fn))
+    return rc;
+  return swiglu_bwd_dw(dgu, x_perm, num_seg, seg_offsets, seg_expert, R, H, I, E, dWg, dWu, accumulate, ws,
+                       s, fn);
+}
+
+int moe_grouped_gemm_swiglu_bwd_dx(const void* dgu, const void* Wg, const void* Wu, int num_seg,
+                                   const int32_t* seg_offsets, const int32_t* seg_expert, int R, int H,
+                                   int I, int E, void* dx_perm, void* stream) {
+  clear_error();
+  const char* fn = "moe_grouped_gemm_swiglu_bwd_dx";
+  if (int rc = check_grouped(fn, num_seg, seg_offsets, R, H, I, E)) return rc;
+  if (int rc = check_bwd_ptrs(fn, {dgu, Wg, Wu, dx_perm})) return rc;
+  return swiglu_bwd_dx(dgu, Wg, Wu, num_seg, seg_offsets, seg_expert, R, H, I, E, dx_perm,
+                       static_cast<cudaStream_t>(stream), fn);
+}
+
+int moe_grouped_gemm_swiglu_bwd_dw(const void* dgu, const void* x_perm, int num_seg,
+                                   const int32_t* seg_offsets, const int32_t* seg_expert, int R, int H,
+                                   int I, int E, float* dWg, float* dWu, int accumulate, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  clear_error();
+  const char* fn = "moe_grouped_gemm_swiglu_bwd_dw";
+  if (int rc = check_grouped(fn, num_seg, seg_offsets, R, H, I, E)) return rc;
+  if (int rc = check_bwd_ptrs(fn, {dgu, x_perm, dWg, dWu})) return rc;
+  if (int rc = check_bwd_ws(fn, num_seg, ws, ws_bytes)) return rc;
+  return swiglu_bwd_dw(dgu, x_perm, num_seg, seg_offsets, seg_expert, R, H, I, E, dWg, dWu, accumulate, ws,
+                       static_cast<cudaStream_t>(stream), fn);
 }
 
 }  // extern "C"

@@ -18,7 +18,7 @@
 namespace moe {
 namespace {
 
-constexpr int kChunkTok = 16;  // tokens per ranking chunk
+constexpr int kChunkTok = kRouteChunk;  // tokens per ranking chunk
 // Blocks that share one chunk in the quantising dispatch: each ranks the
 // chunk again (cheap) and quantises its share of the chunk's tokens, so
 // that more warps hold a row in flight than one block per chunk gives.
@@ -88,7 +88,9 @@ __global__ void __launch_bounds__(256) chunk_scan_kernel(int32_t* __restrict__ c
 }
 
 // ------------------------------------------------------- rank and row copy
-// One CTA per chunk of 16 tokens.  Warp 0 hands out rows slot by slot in
+// One CTA per chunk of 16 tokens, whose first row per expert is
+// chunk_base[e][chunk] (+ base_add[e] when given: the route's chunk prefixes
+// count from 0 within each expert).  Warp 0 hands out rows slot by slot in
 // (token, slot) order: lanes that hold the same expert in one batch of 32
 // slots get consecutive rows in lane order (= token order, since a token
 // picks an expert at most once).  Then all 8 warps copy the chunk's token
@@ -103,7 +105,7 @@ __global__ void __launch_bounds__(256) chunk_scan_kernel(int32_t* __restrict__ c
 template <bool kE4M3>
 __global__ void __launch_bounds__(256, kE4M3 ? 4 : 1) dispatch_kernel(
     const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ topk_idx,
-    const int32_t* __restrict__ chunk_base, int T, int H, int E, int k,
+    const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ base_add, int T, int H, int E, int k,
     void* __restrict__ x_perm_out, float* __restrict__ xs_perm, int32_t* __restrict__ row_of_slot,
     int32_t* __restrict__ token_of_row, int* status) {
   pdl_wait();
@@ -119,7 +121,8 @@ __global__ void __launch_bounds__(256, kE4M3 ? 4 : 1) dispatch_kernel(
   const int nslot = nt * k;
   const int R = T * k;
   const int nchunk = gridDim.x / kSplit;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = chunk_base[(size_t)e * nchunk + c];
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    cnt[e] = chunk_base[(size_t)e * nchunk + c] + (base_add ? base_add[e] : 0);
   const int nvec = H / 8;  // 16-byte vectors per row
   const int first = sub * 8 + warp;  // this warp's first token of the chunk
   // the first 8 vectors per lane of this warp's first token, in flight during the ranking
@@ -387,6 +390,19 @@ int grid_for(size_t work, int per_block) {
   return (int)(b < cap ? (b > 0 ? b : 1) : cap);
 }
 
+// The row kernel of a dispatch whose chunk bases are ready (chunk_base, plus
+// base_add[e] when given).
+template <bool kE4M3>
+int dispatch_rows_launch(const void* x, const int32_t* topk_idx, const int32_t* chunk_base,
+                         const int32_t* base_add, int T, int H, int E, int k, void* x_perm, float* xs_perm,
+                         int32_t* row_of_slot, int32_t* token_of_row, cudaStream_t s, const char* fn) {
+  const int nchunk = (T + kChunkTok - 1) / kChunkTok;
+  launch_pdl(dispatch_kernel<kE4M3>, nchunk * (kE4M3 ? kE4M3Split : 1), 256, sizeof(int) * (E + kChunkTok * k), s,
+             static_cast<const __nv_bfloat16*>(x), topk_idx, chunk_base, base_add, T, H, E, k, x_perm, xs_perm,
+             row_of_slot, token_of_row, status_word());
+  return check_launch(fn, "row kernel");
+}
+
 // Ranking (per-chunk histograms, their scan) and the row kernel of a dispatch
 // whose scratch (the chunk bases) is `ws`.
 template <bool kE4M3>
@@ -397,15 +413,12 @@ int dispatch_launch(const void* x, const int32_t* topk_idx, const int32_t* offse
   const int nchunk = (T + kChunkTok - 1) / kChunkTok;
   int32_t* chunk_base = static_cast<int32_t*>(ws);
   launch_pdl(chunk_hist_kernel, (nchunk + 7) / 8, 256, sizeof(int) * 8 * E, s, topk_idx, T, E, k, nchunk,
-                                                                       chunk_base, status);
-  if (int rc = check_launch("moe_dispatch: histogram kernel")) return rc;
+             chunk_base, status);
+  if (int rc = check_launch(fn, "histogram kernel")) return rc;
   launch_pdl(chunk_scan_kernel, (E + 7) / 8, 256, 0, s, chunk_base, offsets, nchunk, E, status);
-  if (int rc = check_launch("moe_dispatch: scan kernel")) return rc;
-  launch_pdl(dispatch_kernel<kE4M3>, nchunk * (kE4M3 ? kE4M3Split : 1), 256, sizeof(int) * (E + kChunkTok * k), s,
-             static_cast<const __nv_bfloat16*>(x), topk_idx, chunk_base, T, H, E, k, x_perm, xs_perm,
-             row_of_slot, token_of_row, status);
-  (void)fn;
-  return check_launch("moe_dispatch: row kernel");
+  if (int rc = check_launch(fn, "scan kernel")) return rc;
+  return dispatch_rows_launch<kE4M3>(x, topk_idx, chunk_base, nullptr, T, H, E, k, x_perm, xs_perm, row_of_slot,
+                                     token_of_row, s, fn);
 }
 
 int check_rows_args(const char* fn, int T, int H, int k) {
@@ -464,6 +477,39 @@ int moe_dispatch_e4m3(const void* x, const int32_t* topk_idx, const int32_t* off
   if (T == 0) return MOE_OK;
   return dispatch_launch<true>(x, topk_idx, offsets, T, H, E, k, xq_perm, xs_perm, row_of_slot, token_of_row,
                                ws, static_cast<cudaStream_t>(stream), fn);
+}
+
+int moe_dispatch_chunked(const void* x, const int32_t* topk_idx, const int32_t* offsets,
+                         const int32_t* chunk_prefix, int T, int H, int E, int k, void* x_perm,
+                         int32_t* row_of_slot, int32_t* token_of_row, void* stream) {
+  clear_error();
+  const char* fn = "moe_dispatch_chunked";
+  if (int rc = check_rows_args(fn, T, H, k)) return rc;
+  if (E <= 0 || E > kMaxExperts || k > E) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "%s: need 1<=E<=1024, k<=E", fn);
+  if (T > 0 && (!topk_idx || !offsets || !chunk_prefix || !row_of_slot || !token_of_row || (x_perm && !x)))
+    return fail(MOE_ERR_INVALID_ARG, "%s: NULL pointer argument", fn);
+  if ((x && !aligned16(x)) || (x_perm && !aligned16(x_perm)))
+    return fail(MOE_ERR_ALIGNMENT, "%s: x and x_perm must be 16-byte aligned", fn);
+  if (T == 0) return MOE_OK;
+  return dispatch_rows_launch<false>(x, topk_idx, chunk_prefix, offsets, T, H, E, k, x_perm, nullptr, row_of_slot,
+                                     token_of_row, static_cast<cudaStream_t>(stream), fn);
+}
+
+int moe_dispatch_e4m3_chunked(const void* x, const int32_t* topk_idx, const int32_t* offsets,
+                              const int32_t* chunk_prefix, int T, int H, int E, int k, void* xq_perm,
+                              float* xs_perm, int32_t* row_of_slot, int32_t* token_of_row, void* stream) {
+  clear_error();
+  const char* fn = "moe_dispatch_e4m3_chunked";
+  if (int rc = check_rows_args(fn, T, H, k)) return rc;
+  if (E <= 0 || E > kMaxExperts || k > E) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "%s: need 1<=E<=1024, k<=E", fn);
+  if (T > 0 && (!x || !topk_idx || !offsets || !chunk_prefix || !xq_perm || !xs_perm || !row_of_slot ||
+                !token_of_row))
+    return fail(MOE_ERR_INVALID_ARG, "%s: NULL pointer argument", fn);
+  if (!aligned16(x) || !aligned16(xq_perm) || (reinterpret_cast<uintptr_t>(xs_perm) & 3u))
+    return fail(MOE_ERR_ALIGNMENT, "%s: x and xq_perm must be 16-byte, xs_perm 4-byte aligned", fn);
+  if (T == 0) return MOE_OK;
+  return dispatch_rows_launch<true>(x, topk_idx, chunk_prefix, offsets, T, H, E, k, xq_perm, xs_perm, row_of_slot,
+                                    token_of_row, static_cast<cudaStream_t>(stream), fn);
 }
 
 
@@ -585,18 +631,8 @@ int moe_dispatch_no_alloc(const void* x, const int32_t* topk_idx, const int32_t*
   int32_t* chunk_base = nullptr;
   if (int rc = dispatch_scratch(&chunk_base)) return rc;
   if (T == 0) return MOE_OK;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int* status = status_word();
-  const int nc = (int)nchunk;
-  launch_pdl(chunk_hist_kernel, (nc + 7) / 8, 256, sizeof(int) * 8 * E, s, topk_idx, T, E, k, nc,
-                                                                   chunk_base, status);
-  if (int rc = check_launch("moe_dispatch_no_alloc: histogram kernel")) return rc;
-  launch_pdl(chunk_scan_kernel, (E + 7) / 8, 256, 0, s, chunk_base, offsets, nc, E, status);
-  if (int rc = check_launch("moe_dispatch_no_alloc: scan kernel")) return rc;
-  launch_pdl(dispatch_kernel<false>, nc, 256, sizeof(int) * (E + kChunkTok * k), s,
-             static_cast<const __nv_bfloat16*>(x), topk_idx, chunk_base, T, H, E, k, x_perm,
-             static_cast<float*>(nullptr), row_of_slot, token_of_row, status);
-  return check_launch("moe_dispatch_no_alloc: row kernel");
+  return dispatch_launch<false>(x, topk_idx, offsets, T, H, E, k, x_perm, nullptr, row_of_slot, token_of_row,
+                                chunk_base, static_cast<cudaStream_t>(stream), "moe_dispatch_no_alloc");
 }
 
 }  // extern "C"

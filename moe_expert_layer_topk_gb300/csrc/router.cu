@@ -27,7 +27,11 @@ namespace {
 // CTA = 4 warps; thread = 8 tokens x 8 experts (tg = tid % 8, eg = tid / 8):
 // tokens 4tg..4tg+3 and 32+4tg..32+4tg+3 (so the eight tg of a warp read 128
 // contiguous bytes of xs per load, free of bank conflicts), experts
-// 8eg..8eg+7.
+// 8eg..8eg+7.  The 64 chains advance by packed two-lane FMA instructions
+// (fma.rn.f32x2) over pairs of experts with the token's x value in both
+// lanes: every lane is an IEEE fused multiply-add rounded to nearest, so the
+// chains are exactly those of one fmaf per (token, expert, h), with half the
+// instructions to issue (measured 3% faster than one fmaf per chain).
 // h advances in stages of 32: a double-buffered cp.async pipeline brings the Wr tile
 // [32 h][128 e] (fp32) into shared memory; the x tile [64 tokens][32 h]
 // (bf16) is read into registers one stage ahead, widened and stored
@@ -37,7 +41,7 @@ constexpr int kLogitExp = 128;
 constexpr int kLogitThreads = 128;
 constexpr int kLogitStage = 32;   // h per stage
 constexpr int kLogitBlockH = 256; // h per summation block
-constexpr int kLogitDepth = 2;    // W stages in flight (4 CTAs per SM)
+constexpr int kLogitDepth = 2;    // W stages in flight
 constexpr size_t kLogitSmem = sizeof(float) * (kLogitDepth * kLogitStage * kLogitExp + 2 * kLogitStage * kLogitTok);
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
@@ -55,8 +59,17 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+__device__ __forceinline__ uint64_t pair_of(float v) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ void fma2(uint64_t& acc, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
 template <bool kVec>
-__global__ void __launch_bounds__(kLogitThreads) router_partials_kernel(
+__global__ void __launch_bounds__(kLogitThreads, 4) router_partials_kernel(
     const __nv_bfloat16* __restrict__ x, const float* __restrict__ Wr, int T, int H, int E,
     float* __restrict__ part) {
   pdl_wait();
@@ -101,11 +114,12 @@ __global__ void __launch_bounds__(kLogitThreads) router_partials_kernel(
     r[1] = xok ? __ldg(xrow + hv + 1) : make_uint4(0, 0, 0, 0);
   };
 
-  float p[8][8];
+  // chains: pp[i][q] = token i, experts (8eg + 2q, 8eg + 2q + 1)
+  uint64_t pp[8][4];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) p[i][j] = 0.f;
+    for (int q = 0; q < 4; ++q) pp[i][q] = 0ull;
 
   uint4 xr[2];
   load_x(0, xr);
@@ -132,19 +146,30 @@ __global__ void __launch_bounds__(kLogitThreads) router_partials_kernel(
     const int buf = st % kLogitDepth;
 #pragma unroll 4
     for (int hh = 0; hh < kLogitStage; ++hh) {
+      const ulonglong2 wa = *reinterpret_cast<const ulonglong2*>(&ws[buf][hh][8 * eg]);
+      const ulonglong2 wb = *reinterpret_cast<const ulonglong2*>(&ws[buf][hh][8 * eg + 4]);
+      const uint64_t wv[4] = {wa.x, wa.y, wb.x, wb.y};
       const float4 xa = *reinterpret_cast<const float4*>(&xs[xb][hh][4 * tg]);
       const float4 xb4 = *reinterpret_cast<const float4*>(&xs[xb][hh][32 + 4 * tg]);
-      const float4 wa = *reinterpret_cast<const float4*>(&ws[buf][hh][8 * eg]);
-      const float4 wb = *reinterpret_cast<const float4*>(&ws[buf][hh][8 * eg + 4]);
-      const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb4.x, xb4.y, xb4.z, xb4.w};
-      const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+      const float xf[8] = {xa.x, xa.y, xa.z, xa.w, xb4.x, xb4.y, xb4.z, xb4.w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < 8; ++i) {
+        const uint64_t xx = pair_of(xf[i]);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) p[i][j] = __fmaf_rn(xv[i], wv[j], p[i][j]);
+        for (int q = 0; q < 4; ++q) fma2(pp[i][q], xx, wv[q]);
+      }
     }
   }
   cp_async_wait<0>();
+  float p[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 v = *reinterpret_cast<const float2*>(&pp[i][q]);
+      p[i][2 * q] = v.x;
+      p[i][2 * q + 1] = v.y;
+    }
   float* out = part + (size_t)blk * T * E;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -163,14 +188,14 @@ __global__ void __launch_bounds__(kLogitThreads) router_partials_kernel(
 // One warp per token: the token's logits are assembled in registers (lane l
 // holds experts l, l+32, ...; kNQ registers per lane) from the h-block
 // partials, added left to right, bias last; k rounds of a warp-wide arg-max
-// over (logit descending, id ascending) pick the slots in order.  Slot
-// counts go to a per-expert counter with integer atomics (order-independent);
-// each expert's counter sits on its own 128-byte line of the workspace, so
-// the T*k atomics do not queue on the few lines that counts[] spans.
-constexpr int kCountPad = 32;  // ints per expert counter line (128 bytes)
+// over (logit descending, id ascending) pick the slots in order.  A CTA
+// covers one ranking chunk of kRouteChunk tokens and counts its slots per
+// expert in shared memory; the counts go to chunk_cnt[e][chunk], every
+// entry written (no atomics on global memory, nothing to clear first).
 constexpr int kTopkWarps = 8;
 constexpr int kTopkTokPerWarp = 2;
 constexpr int kTopkTokPerBlock = kTopkWarps * kTopkTokPerWarp;
+static_assert(kTopkTokPerBlock == kRouteChunk, "a top-k CTA covers one ranking chunk");
 // h-block partials loaded per batch (kNQ * batch <= 32 values per lane)
 template <int kNQ>
 __host__ __device__ constexpr int sum_batch() { return kNQ >= 32 ? 1 : (kNQ >= 16 ? 2 : (kNQ >= 8 ? 4 : 8)); }
@@ -191,10 +216,13 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
                                                           const float* __restrict__ bias, int T,
                                                           int E, int k, int32_t* __restrict__ topk_idx,
                                                           float* __restrict__ topk_w,
-                                                          int32_t* __restrict__ counts) {
+                                                          int32_t* __restrict__ chunk_cnt, int nchunk) {
   pdl_wait();
   pdl_trigger();
+  extern __shared__ int chist[];  // [E] slots of this chunk per expert
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) chist[e] = 0;
+  __syncthreads();
   for (int it = 0; it < kTopkTokPerWarp; ++it) {
     const int t = blockIdx.x * kTopkTokPerBlock + warp * kTopkTokPerWarp + it;
     if (t >= T) break;
@@ -263,19 +291,41 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
     if (lane < k) {
       topk_idx[(size_t)t * k + lane] = my_i;
       topk_w[(size_t)t * k + lane] = __fdiv_rn(ex, s);
-      atomicAdd(counts + (size_t)my_i * kCountPad, 1);
+      atomicAdd(&chist[my_i], 1);
     }
   }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_cnt[(size_t)e * nchunk + blockIdx.x] = chist[e];
 }
 
-__global__ void zero_counts_kernel(int32_t* __restrict__ counts, int E) {
+// chunk_cnt[e][c] <- sum_{c' < c} chunk_cnt[e][c'] (in place, exclusive) and
+// totals[e] = all of e's slots.  One warp per expert walks its row of chunks
+// 32 at a time (coalesced): a warp scan of each batch plus the running carry.
+__global__ void __launch_bounds__(256) route_chunk_scan_kernel(int32_t* __restrict__ chunk_cnt, int nchunk,
+                                                               int E, int32_t* __restrict__ totals) {
   pdl_wait();
   pdl_trigger();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) counts[(size_t)e * kCountPad] = 0;
+  const int e = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (e >= E) return;
+  int32_t* row = chunk_cnt + (size_t)e * nchunk;
+  int carry = 0;
+  for (int c0 = 0; c0 < nchunk; c0 += 32) {
+    const int c = c0 + lane;
+    const int v = c < nchunk ? row[c] : 0;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    if (c < nchunk) row[c] = carry + incl - v;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) totals[e] = carry;
 }
 
 // ------------------------------------------------------------ offsets kernel
-// One CTA: the per-expert counters -> counts[], exclusive scan -> offsets,
+// One CTA: the per-expert totals -> counts[], exclusive scan -> offsets,
 // EP-rank row ranges.
 __global__ void __launch_bounds__(1024) router_offsets_kernel(const int32_t* __restrict__ hist,
                                                               int E, int ep_size,
@@ -287,7 +337,7 @@ __global__ void __launch_bounds__(1024) router_offsets_kernel(const int32_t* __r
   __shared__ int warp_sum[32];
   __shared__ int excl[kMaxExperts + 1];
   const int e = threadIdx.x;
-  const int c = e < E ? hist[(size_t)e * kCountPad] : 0;
+  const int c = e < E ? hist[e] : 0;
   if (e < E) counts[e] = c;
   const int lane = e & 31, warp = e >> 5;
   int incl = c;
@@ -424,14 +474,19 @@ __global__ void router_bwd_reduce_kernel(const float* __restrict__ P, int S, int
 
 size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
+
 // Route workspace: the h-block partials of the logits, fp32 [nblk_h][T][E],
-// then one 128-byte counter line per expert.
+// then the per-expert slot totals, then (moe_route_topk only) the per-chunk
+// slot counts [E][ceil(T/16)] that moe_route_topk_chunks returns instead.
+int route_nchunk(int T) { return (T + kRouteChunk - 1) / kRouteChunk; }
 size_t route_part_bytes(int T, int H, int E) {
   const size_t nblk_h = (size_t)((H + kLogitBlockH - 1) / kLogitBlockH);
   return align256(sizeof(float) * nblk_h * (size_t)(T > 0 ? T : 1) * E);
 }
-size_t route_ws_bytes(int T, int H, int E) {
-  return route_part_bytes(T, H, E) + align256(sizeof(int32_t) * kCountPad * (size_t)E);
+size_t route_chunk_bytes(int T, int E) { return align256(sizeof(int32_t) * (size_t)route_nchunk(T) * E); }
+size_t route_ws_bytes(int T, int H, int E, bool with_chunks) {
+  return route_part_bytes(T, H, E) + align256(sizeof(int32_t) * (size_t)E) +
+         (with_chunks ? route_chunk_bytes(T, E) : 0);
 }
 
 struct BwdLayout {
@@ -469,75 +524,122 @@ extern "C" {
 
 size_t moe_route_topk_workspace_size(int T, int H, int E) {
   if (T < 0 || H <= 0 || E <= 0) return 0;
-  return route_ws_bytes(T, H, E);
+  return route_ws_bytes(T, H, E, true);
 }
+
+size_t moe_route_topk_chunks_workspace_size(int T, int H, int E) {
+  if (T < 0 || H <= 0 || E <= 0) return 0;
+  return route_ws_bytes(T, H, E, false);
+}
+
+}  // extern "C"
+
+namespace moe {
+namespace {
+
+// Both route entry points: partial logits, top-k + per-chunk slot counts into
+// `chunk` ([E][ceil(T/16)]), their per-expert scan (chunk prefixes in place,
+// totals), counts / offsets / EP-rank ranges.
+int route_impl(const char* fn, const void* x, const float* Wr, const float* bias, int T, int H, int E, int k,
+               int ep_size, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+               int32_t* rank_offsets, int32_t* chunk, void* ws, cudaStream_t s) {
+  float* part = static_cast<float*>(ws);
+  int32_t* totals = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + route_part_bytes(T, H, E));
+  const int nchunk = route_nchunk(T);
+  if (T > 0) {
+    static bool attr_set[64] = {};
+    const int dev = current_device();
+    if (dev < 0 || dev >= 64) return fail(MOE_ERR_CUDA, "%s: no usable current device", fn);
+    constexpr size_t smem = kLogitSmem;
+    if (!attr_set[dev]) {
+      cudaError_t e1 = cudaFuncSetAttribute(router_partials_kernel<true>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      cudaError_t e2 = cudaFuncSetAttribute(router_partials_kernel<false>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e1 != cudaSuccess || e2 != cudaSuccess)
+        return fail(MOE_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e1 != cudaSuccess ? e1 : e2));
+      attr_set[dev] = true;
+    }
+    const int nblk_h = (H + kLogitBlockH - 1) / kLogitBlockH;
+    dim3 grid((T + kLogitTok - 1) / kLogitTok, nblk_h, (E + kLogitExp - 1) / kLogitExp);
+    if (E % 4 == 0)
+      launch_pdl(router_partials_kernel<true>, grid, kLogitThreads, smem, s,
+                 static_cast<const __nv_bfloat16*>(x), Wr, T, H, E, part);
+    else
+      launch_pdl(router_partials_kernel<false>, grid, kLogitThreads, smem, s,
+                 static_cast<const __nv_bfloat16*>(x), Wr, T, H, E, part);
+    if (int rc = check_launch("route: logits kernel")) return rc;
+    const int nq = (E + 31) / 32;
+    const size_t hs = sizeof(int) * (size_t)E;
+    if (nq <= 1)
+      launch_pdl(router_topk_kernel<1>, nchunk, 256, hs, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, chunk, nchunk);
+    else if (nq <= 2)
+      launch_pdl(router_topk_kernel<2>, nchunk, 256, hs, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, chunk, nchunk);
+    else if (nq <= 4)
+      launch_pdl(router_topk_kernel<4>, nchunk, 256, hs, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, chunk, nchunk);
+    else if (nq <= 8)
+      launch_pdl(router_topk_kernel<8>, nchunk, 256, hs, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, chunk, nchunk);
+    else if (nq <= 16)
+      launch_pdl(router_topk_kernel<16>, nchunk, 256, hs, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, chunk, nchunk);
+    else
+      launch_pdl(router_topk_kernel<32>, nchunk, 256, hs, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, chunk, nchunk);
+    if (int rc = check_launch("route: top-k kernel")) return rc;
+  }
+  // with no token every total is 0 (the scan runs over no chunk)
+  launch_pdl(route_chunk_scan_kernel, (E + 7) / 8, 256, 0, s, chunk, nchunk, E, totals);
+  if (int rc = check_launch("route: chunk scan kernel")) return rc;
+  launch_pdl(router_offsets_kernel, 1, 1024, 0, s, totals, E, ep_size, counts, offsets, rank_offsets);
+  return check_launch("route: offsets kernel");
+}
+
+int route_check(const char* fn, const void* x, const float* Wr, const float* bias, int T, int H, int E, int k,
+                int ep_size, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                int32_t* rank_offsets, void* ws, size_t ws_bytes, size_t need) {
+  if (T < 0 || H <= 0 || E <= 0 || k <= 0) return fail(MOE_ERR_INVALID_ARG, "%s: need T>=0, H>0, E>0, k>0", fn);
+  if (E > kMaxExperts || k > kMaxTopK || k > E || H % 64 != 0 || (long long)T * k >= (1ll << 31))
+    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "%s: need E<=1024, k<=min(E,32), H%%64==0, T*k<2^31 (E=%d k=%d H=%d)",
+                fn, E, k, H);
+  if (ep_size < 1 || E % ep_size != 0)
+    return fail(MOE_ERR_INVALID_ARG, "%s: ep_size=%d must divide E=%d", fn, ep_size, E);
+  if (!counts || !offsets || !rank_offsets || !ws || (T > 0 && (!x || !Wr || !topk_idx || !topk_w)))
+    return fail(MOE_ERR_INVALID_ARG, "%s: NULL pointer argument", fn);
+  if (!aligned16(x) || !aligned16(Wr) || !aligned16(ws) || (bias && !aligned16(bias)))
+    return fail(MOE_ERR_ALIGNMENT, "%s: x, Wr, bias and ws must be 16-byte aligned", fn);
+  if (ws_bytes < need) return fail(MOE_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, need);
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" {
 
 int moe_route_topk(const void* x, const float* Wr, const float* bias, int T, int H, int E, int k,
                    int ep_size, int32_t* topk_idx, float* topk_w, int32_t* counts,
                    int32_t* offsets, int32_t* rank_offsets, void* ws, size_t ws_bytes,
                    void* stream) {
   clear_error();
-  if (T < 0 || H <= 0 || E <= 0 || k <= 0)
-    return fail(MOE_ERR_INVALID_ARG, "moe_route_topk: need T>=0, H>0, E>0, k>0");
-  if (E > kMaxExperts || k > kMaxTopK || k > E || H % 64 != 0 || (long long)T * k >= (1ll << 31))
-    return fail(MOE_ERR_UNSUPPORTED_SHAPE,
-                "moe_route_topk: need E<=1024, k<=min(E,32), H%%64==0, T*k<2^31 (E=%d k=%d H=%d)", E,
-                k, H);
-  if (ep_size < 1 || E % ep_size != 0)
-    return fail(MOE_ERR_INVALID_ARG, "moe_route_topk: ep_size=%d must divide E=%d", ep_size, E);
-  if (!counts || !offsets || !rank_offsets || !ws ||
-      (T > 0 && (!x || !Wr || !topk_idx || !topk_w)))
-    return fail(MOE_ERR_INVALID_ARG, "moe_route_topk: NULL pointer argument");
-  if (!aligned16(x) || !aligned16(Wr) || !aligned16(ws) || (bias && !aligned16(bias)))
-    return fail(MOE_ERR_ALIGNMENT, "moe_route_topk: x, Wr, bias and ws must be 16-byte aligned");
-  const size_t need = route_ws_bytes(T, H, E);
-  if (ws_bytes < need)
-    return fail(MOE_ERR_WORKSPACE, "moe_route_topk: workspace %zu < %zu bytes", ws_bytes, need);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  float* part = static_cast<float*>(ws);
-  int32_t* hist = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + route_part_bytes(T, H, E));
-  launch_pdl(zero_counts_kernel, 1, 256, 0, s, hist, E);
-  if (int rc = check_launch("moe_route_topk: zero counts")) return rc;
-  if (T > 0) {
-    static bool attr_set[64] = {};
-    const int dev = current_device();
-    if (dev < 0 || dev >= 64) return fail(MOE_ERR_CUDA, "moe_route_topk: no usable current device");
-    if (!attr_set[dev]) {
-      cudaError_t e1 = cudaFuncSetAttribute(router_partials_kernel<true>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLogitSmem);
-      cudaError_t e2 = cudaFuncSetAttribute(router_partials_kernel<false>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLogitSmem);
-      if (e1 != cudaSuccess || e2 != cudaSuccess)
-        return fail(MOE_ERR_CUDA, "moe_route_topk: %s", cudaGetErrorString(e1 != cudaSuccess ? e1 : e2));
-      attr_set[dev] = true;
-    }
-    const int nblk_h = (H + kLogitBlockH - 1) / kLogitBlockH;
-    dim3 grid((T + kLogitTok - 1) / kLogitTok, nblk_h, (E + kLogitExp - 1) / kLogitExp);
-    if (E % 4 == 0)
-      launch_pdl(router_partials_kernel<true>, grid, kLogitThreads, kLogitSmem, s, 
-          static_cast<const __nv_bfloat16*>(x), Wr, T, H, E, part);
-    else
-      launch_pdl(router_partials_kernel<false>, grid, kLogitThreads, kLogitSmem, s, 
-          static_cast<const __nv_bfloat16*>(x), Wr, T, H, E, part);
-    if (int rc = check_launch("moe_route_topk: logits kernel")) return rc;
-    const int nblk = (T + kTopkTokPerBlock - 1) / kTopkTokPerBlock;
-    const int nq = (E + 31) / 32;
-    if (nq <= 1)
-      launch_pdl(router_topk_kernel<1>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, hist);
-    else if (nq <= 2)
-      launch_pdl(router_topk_kernel<2>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, hist);
-    else if (nq <= 4)
-      launch_pdl(router_topk_kernel<4>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, hist);
-    else if (nq <= 8)
-      launch_pdl(router_topk_kernel<8>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, hist);
-    else if (nq <= 16)
-      launch_pdl(router_topk_kernel<16>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, hist);
-    else
-      launch_pdl(router_topk_kernel<32>, nblk, 256, 0, s, part, nblk_h, bias, T, E, k, topk_idx, topk_w, hist);
-    if (int rc = check_launch("moe_route_topk: top-k kernel")) return rc;
-  }
-  launch_pdl(router_offsets_kernel, 1, 1024, 0, s, hist, E, ep_size, counts, offsets, rank_offsets);
-  return check_launch("moe_route_topk: offsets kernel");
+  const char* fn = "moe_route_topk";
+  if (int rc = route_check(fn, x, Wr, bias, T, H, E, k, ep_size, topk_idx, topk_w, counts, offsets, rank_offsets,
+                           ws, ws_bytes, T >= 0 && H > 0 && E > 0 ? route_ws_bytes(T, H, E, true) : 0))
+    return rc;
+  int32_t* chunk = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + route_ws_bytes(T, H, E, false));
+  return route_impl(fn, x, Wr, bias, T, H, E, k, ep_size, topk_idx, topk_w, counts, offsets, rank_offsets,
+                    chunk, ws, static_cast<cudaStream_t>(stream));
+}
+
+int moe_route_topk_chunks(const void* x, const float* Wr, const float* bias, int T, int H, int E, int k,
+                          int ep_size, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                          int32_t* rank_offsets, int32_t* chunk_prefix, void* ws, size_t ws_bytes,
+                          void* stream) {
+  clear_error();
+  const char* fn = "moe_route_topk_chunks";
+  if (int rc = route_check(fn, x, Wr, bias, T, H, E, k, ep_size, topk_idx, topk_w, counts, offsets, rank_offsets,
+                           ws, ws_bytes, T >= 0 && H > 0 && E > 0 ? route_ws_bytes(T, H, E, false) : 0))
+    return rc;
+  if (T > 0 && !chunk_prefix) return fail(MOE_ERR_INVALID_ARG, "%s: NULL pointer argument", fn);
+  return route_impl(fn, x, Wr, bias, T, H, E, k, ep_size, topk_idx, topk_w, counts, offsets, rank_offsets,
+                    chunk_prefix, ws, static_cast<cudaStream_t>(stream));
 }
 
 size_t moe_route_topk_bwd_workspace_size(int T, int H, int E) {

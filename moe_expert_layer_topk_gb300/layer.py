@@ -9,13 +9,13 @@ from __future__ import annotations
 
 import torch
 
-from . import (moe_combine, moe_combine_bwd, moe_dispatch, moe_dispatch_bwd, moe_dispatch_e4m3,
-               moe_dispatch_workspace_size, moe_grouped_gemm_bwd_workspace_size,
+from . import (moe_combine, moe_combine_bwd, moe_dispatch_bwd, moe_dispatch_chunked,
+               moe_dispatch_e4m3_chunked, moe_grouped_gemm_bwd_workspace_size,
                moe_grouped_gemm_down, moe_grouped_gemm_down_bwd, moe_grouped_gemm_down_fp8,
                moe_grouped_gemm_swiglu, moe_grouped_gemm_swiglu_bwd, moe_grouped_gemm_swiglu_fp8,
-               moe_grouped_gemm_swiglu_gather, moe_quantize_rows_e4m3, moe_route_topk,
-               moe_route_topk_bwd, moe_route_topk_bwd_workspace_size,
-               moe_route_topk_workspace_size)
+               moe_grouped_gemm_swiglu_gather, moe_quantize_rows_e4m3, moe_route_topk_bwd,
+               moe_route_topk_bwd_workspace_size, moe_route_topk_chunks,
+               moe_route_topk_chunks_workspace_size)
 
 
 def _ws(nbytes: int, device) -> torch.Tensor:
@@ -55,8 +55,9 @@ class MoELayer:
         self.counts = e(E, dt=i32)
         self.offsets = e(E + 1, dt=i32)
         self.rank_offsets = e(ep_size + 1, dt=i32)
-        self.ws_route = _ws(moe_route_topk_workspace_size(T, H, E), dev)
-        self.ws_dispatch = _ws(moe_dispatch_workspace_size(T, E, k), dev)
+        self.ws_route = _ws(moe_route_topk_chunks_workspace_size(T, H, E), dev)
+        # where each 16-token chunk starts in each expert's rows (from the route, for the dispatch)
+        self.chunk_prefix = e(E, (T + 15) // 16, dt=i32)
         self.x_perm = None if (fused_dispatch or fp8) else e(R, H, dt=bf)
         self.row_of_slot = e(T, k, dt=i32)
         self.token_of_row = e(R, dt=i32)
@@ -95,18 +96,18 @@ class MoELayer:
         return out
 
     def route(self, x, Wr, bias=None, stream=None):
-        moe_route_topk(x, Wr, bias, self.T, self.H, self.E, self.k, self.ep_size, self.topk_idx,
-                       self.topk_w, self.counts, self.offsets, self.rank_offsets, self.ws_route,
-                       stream)
+        moe_route_topk_chunks(x, Wr, bias, self.T, self.H, self.E, self.k, self.ep_size, self.topk_idx,
+                              self.topk_w, self.counts, self.offsets, self.rank_offsets, self.chunk_prefix,
+                              self.ws_route, stream)
 
     def dispatch(self, x, stream=None):
         self._x = x  # the fused gate/up GEMM reads the rows from here
         if self.fp8:
-            moe_dispatch_e4m3(x, self.topk_idx, self.offsets, self.T, self.H, self.E, self.k, self.x_q,
-                              self.x_scale, self.row_of_slot, self.token_of_row, self.ws_dispatch, stream)
+            moe_dispatch_e4m3_chunked(x, self.topk_idx, self.offsets, self.chunk_prefix, self.T, self.H, self.E,
+                                      self.k, self.x_q, self.x_scale, self.row_of_slot, self.token_of_row, stream)
             return
-        moe_dispatch(x, self.topk_idx, self.offsets, self.T, self.H, self.E, self.k, self.x_perm,
-                     self.row_of_slot, self.token_of_row, self.ws_dispatch, stream)
+        moe_dispatch_chunked(x, self.topk_idx, self.offsets, self.chunk_prefix, self.T, self.H, self.E, self.k,
+                             self.x_perm, self.row_of_slot, self.token_of_row, stream)
 
     def experts(self, Wg, Wu, Wd, stream=None):
         """Wg, Wu, Wd: bf16 expert weights, or (fp8 layers) the dict that

@@ -78,3 +78,10 @@ def oracle_backward(inp, f):
     dWr, dx = oracle.route_topk_bwd(dw, f["rt"]["topk_w"], f["rt"]["topk_idx"], f["x"], f["Wr"], dxa)
     return dict(dy_perm=dyp, d_w=dw, dgu=dgu, dWd=dWd, dx_perm=dxp, dWg=dWg, dWu=dWu, dx_acc=dxa,
                 dWr=dWr, dx=dx)
+
+
+def dispatch_ws(T, E, k):
+    """A workspace for moe_dispatch / moe_dispatch_e4m3 (the layer itself
+    dispatches from the route's chunk prefixes and keeps none)."""
+    import moe_expert_layer_topk_gb300 as m
+    return torch.empty(max(256, m.moe_dispatch_workspace_size(T, E, k)), dtype=torch.uint8, device="cuda")

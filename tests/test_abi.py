@@ -82,6 +82,12 @@ def test_grouped_gemm_rejects_bad_shapes(L):
     assert L.moe_grouped_gemm_swiglu_gather(P, P, 16, P, P, 8, P, None, 64, 100, 64, 8, P, None, None) == SHAPE
     assert L.moe_grouped_gemm_swiglu_gather(P + 8, P, 16, P, P, 8, P, None, 64, 128, 64, 8, P, None,
                                             None) == ALIGN
+    # the backward GEMMs' dX and weight-gradient halves check like the combined calls
+    assert L.moe_grouped_gemm_down_bwd_dx(P, None, P, 8, P, None, 64, 128, 64, 8, P, None) == INVALID
+    assert L.moe_grouped_gemm_down_bwd_dw(P, P, 8, P, None, 64, 128, 64, 8, P, 0, None, 0, None) == WS
+    assert L.moe_grouped_gemm_swiglu_bwd_dx(P, P, P, 8, P, None, 64, 100, 64, 8, P, None) == SHAPE
+    assert L.moe_grouped_gemm_swiglu_bwd_dw(P, P + 8, 8, P, None, 64, 128, 64, 8, P, P, 0, P, 1 << 20,
+                                            None) == ALIGN
     # the backward GEMMs need 256 bytes of 128-byte aligned workspace per segment
     assert L.moe_grouped_gemm_bwd_workspace_size(8) == 8 * 256
     assert L.moe_grouped_gemm_bwd_workspace_size(0) == 0

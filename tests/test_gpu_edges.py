@@ -10,7 +10,7 @@ import torch.nn.functional as F
 
 import moe_expert_layer_topk_gb300 as m
 import oracle
-from gpu_util import assert_close, inputs, oracle_backward, oracle_chain, to_dev
+from gpu_util import assert_close, inputs, oracle_backward, oracle_chain, to_dev, dispatch_ws
 from moe_expert_layer_topk_gb300.synth import LayerShape, bf16_bits, make_segment_inputs
 
 pytestmark = pytest.mark.gpu
@@ -208,7 +208,7 @@ def test_bad_index_data_sets_status_without_fault():
     bad[5, 1] = 8          # expert id == E
     bad[9, 0] = -3
     m.moe_dispatch(g["x"], bad, L.offsets, 64, 128, 8, 2, L.x_perm, L.row_of_slot, L.token_of_row,
-                   L.ws_dispatch)
+                   dispatch_ws(64, 8, 2))
     torch.cuda.synchronize()
     st = m.moe_read_device_status(reset=True)
     assert st & 1, st  # MOE_STATUS_BAD_INDEX

@@ -22,7 +22,7 @@ import torch
 
 import moe_expert_layer_topk_gb300 as m
 import oracle
-from gpu_util import assert_close, bits, inputs, oracle_chain, to_dev
+from gpu_util import assert_close, bits, inputs, oracle_chain, to_dev, dispatch_ws
 
 pytestmark = pytest.mark.gpu
 
@@ -357,7 +357,7 @@ def test_dispatch_e4m3_bit_exact(T, H, E, k, bias):
     xs = torch.full((R,), float("nan"), dtype=torch.float32, device="cuda")
     ros = torch.empty_like(L.row_of_slot)
     tor = torch.empty_like(L.token_of_row)
-    m.moe_dispatch_e4m3(g["x"], L.topk_idx, L.offsets, T, H, E, k, xq, xs, ros, tor, L.ws_dispatch)
+    m.moe_dispatch_e4m3(g["x"], L.topk_idx, L.offsets, T, H, E, k, xq, xs, ros, tor, dispatch_ws(T, E, k))
     torch.cuda.synchronize()
     assert m.moe_read_device_status(reset=True) == 0
     assert torch.equal(ros, L.row_of_slot) and torch.equal(tor, L.token_of_row)

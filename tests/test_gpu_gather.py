@@ -8,7 +8,7 @@ import torch
 
 import moe_expert_layer_topk_gb300 as m
 import oracle
-from gpu_util import assert_close, bits, inputs, oracle_chain, to_dev
+from gpu_util import assert_close, bits, inputs, oracle_chain, to_dev, dispatch_ws
 from moe_expert_layer_topk_gb300.synth import CONFIGS, make_layer_inputs
 
 pytestmark = pytest.mark.gpu
@@ -42,7 +42,7 @@ def test_gather_matches_permuted_path_and_oracle(case):
     rows = L.row_of_slot.clone()
     tok = L.token_of_row.clone()
     m.moe_dispatch(g["x"], L.topk_idx, L.offsets, T, H, E, k, None, L.row_of_slot, L.token_of_row,
-                   L.ws_dispatch)
+                   dispatch_ws(T, E, k))
     h = torch.empty_like(h_ref)
     gu = torch.empty_like(gu_ref)
     m.moe_grouped_gemm_swiglu_gather(g["x"], L.token_of_row, T, g["Wg"], g["Wu"], E, L.offsets, None, R, H,
