@@ -366,7 +366,14 @@ def run_ours(args, shape, inp):
         m.moe_route_topk_bwd(layer.d_w, layer.topk_w, layer.topk_idx, g["x"], g["Wr"], layer.dx_acc, T, H,
                              E, k, layer.dWr, layer.dx, 0, layer.ws_route_bwd); mark(12)
 
+    def layer_step():
+        # the step as the layer runs it: the dispatch and router backward on a
+        # side stream beside the gate/up weight gradient
+        layer.forward(g["x"], g["Wr"], g["bias"], g["Wg"], g["Wu"], g["Wd"])
+        layer.backward(g["dy"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"])
+
     for _ in range(args.warmup):
+        layer_step()
         step()
     torch.cuda.synchronize(dev)
     if m.moe_read_device_status(reset=True) != 0:
@@ -376,7 +383,7 @@ def run_ours(args, shape, inp):
     p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     p0.record(stream)
     for _ in range(args.steps):
-        step()
+        layer_step()
     p1.record(stream)
     torch.cuda.synchronize(dev)
     block_s = max(p0.elapsed_time(p1) * 1e-3, 1e-6)
@@ -387,17 +394,26 @@ def run_ours(args, shape, inp):
     nev = len(names) + 1
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(n_timed)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c_start, c_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist, dev)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
         t_start.record(stream)
         for i in range(n_timed):
-            step(evs[i])
+            layer_step()
         t_end.record(stream)
+        torch.cuda.synchronize(dev)
+        # the same steps with every call on one stream, bracketed by events of
+        # its own: the per-call times and rooflines
+        c_start.record(stream)
+        for i in range(n_timed):
+            step(evs[i])
+        c_end.record(stream)
         torch.cuda.synchronize(dev)
     barrier(dist, dev)
     ms_local = t_start.elapsed_time(t_end)
     ms = max_over_ranks(ms_local, dist, dev)
+    seq_ms = c_start.elapsed_time(c_end) / n_timed
     per_call = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n_timed))
                 for j, n in enumerate(names)}
     if m.moe_read_device_status(reset=True) != 0:
@@ -510,8 +526,14 @@ def run_ours(args, shape, inp):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (1.2 GB of expert weights per step)",
                    "timed": f"{reps} back-to-back blocks of {args.steps} steps ({n_timed} steps, "
-                            f"{ms_local * 1e-3:.2f} s) between one pair of events"},
+                            f"{ms_local * 1e-3:.2f} s) between one pair of events",
+                   "schedule": f"MoELayer.forward + backward; the dispatch and router backward on a side "
+                               f"stream beside the gate/up weight gradient, which leaves "
+                               f"{layer.TAIL_SMS} SMs to them"},
         "timed_steps": n_timed,
+        "per_call_pass": {"ms_per_step": seq_ms,
+                          "how": "the same steps again, every call on one stream with CUDA events of its "
+                                 "own around it (per_call_ms and the rooflines come from this pass)"},
         "fwd_tokens_per_s": fshape.T / (fwd_ms * 1e-3),
         "fwd_ms": fwd_ms, "fwd_config": {"workload": FWD_WORKLOAD, "T": fshape.T,
                        "path": "fused dispatch: rows gathered from x by the gate/up GEMM"},
@@ -712,7 +734,8 @@ def run_fp8_forward(m, fg, fshape, dev, stream, args):
             "hbm_peak_gbs": pk["hbm_gbs"]}
 
 
-# kernels launched per step by the calls in run_ours.step():
+# kernels launched per step by the calls in run_ours.step() (and by
+# MoELayer.forward + backward, the same calls):
 # route 4 (partial logits, top-k with per-chunk counts, chunk scan, offsets),
 # dispatch 1 (rows from the route's chunk prefixes),
 # gate/up 1, down 1, combine 1, combine_bwd 1, the dX halves 1 each and the
@@ -740,7 +763,8 @@ def run_profile_router(args):
 
 
 def run_profile_case(args):
-    """Untimed forward+backward passes of one layer shape (for ncu captures)."""
+    """Untimed forward+backward passes of one layer shape (for ncu captures),
+    the backward on one stream."""
     import torch
 
     import moe_expert_layer_topk_gb300 as m
@@ -752,7 +776,8 @@ def run_profile_case(args):
     layer = m.MoELayer(T, H, I, E, k, 1)
     for _ in range(args.steps):
         layer.forward(g["x"], g["Wr"], None, g["Wg"], g["Wu"], g["Wd"])
-        layer.backward(g["dy"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"])
+        # one stream, every GEMM on all SMs: the kernels as the per-call pass times them
+        layer.backward(g["dy"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"], overlap=False)
     torch.cuda.synchronize()
     print(json.dumps({"profile_case": [T, H, I, E, k], "passes": args.steps,
                       "device_status": m.moe_read_device_status(reset=True)}))

@@ -395,6 +395,17 @@ int moe_route_topk_bwd(const float* d_w, const float* topk_w, const int32_t* top
                        int k, float* dWr, void* dx, int accumulate, void* ws, size_t ws_bytes,
                        void* stream);
 
+/* Persistent-grid limit of the grouped GEMMs (no counterpart on the pages).
+ * Every grouped GEMM kernel (the forward, backward and router-backward
+ * GEMMs of the calls above) runs one CTA per SM over its tiles.  After
+ * this call, those launched from the calling thread use at most max_sms
+ * SMs (0 = all, the default), leaving the rest to work issued on another
+ * stream: the layer runs the dispatch and router backward beside the
+ * gate/up weight gradient this way.  Results do not depend on the limit.
+ * *previous (host, may be NULL) receives the limit in force before.
+ * MOE_ERR_INVALID_ARG if max_sms < 0. */
+int moe_set_gemm_sm_limit(int max_sms, int* previous);
+
 /* Measurement aid (no counterpart on the pages): launches a kernel whose
  * threads only run independent fp32 fused multiply-add chains, per_sm CTAs
  * of 256 threads on every SM, `iters` x 128 FMAs per thread.  Timing it

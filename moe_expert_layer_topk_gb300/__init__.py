@@ -30,7 +30,7 @@ __all__ = ["lib", "MoEError", "LIB_PATH", "ENTRY_POINTS",
            "moe_dispatch_bwd", "moe_route_topk_bwd",
            "moe_route_topk_workspace_size", "moe_dispatch_workspace_size",
            "moe_route_topk_bwd_workspace_size", "moe_grouped_gemm_bwd_workspace_size",
-           "moe_read_device_status", "moe_abi_version", "moe_probe_fma"]
+           "moe_read_device_status", "moe_abi_version", "moe_probe_fma", "moe_set_gemm_sm_limit", "sm_count"]
 
 LIB_PATH: Path = _build_mod.LIB
 
@@ -72,6 +72,7 @@ ENTRY_POINTS = {
     "moe_route_topk_bwd_workspace_size": ([_I, _I, _I], _Z),
     "moe_route_topk_bwd": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _Z, _P], _I),
     "moe_probe_fma": ([_I, _I, _I, _P, ctypes.POINTER(ctypes.c_longlong), _P], _I),
+    "moe_set_gemm_sm_limit": ([_I, ctypes.POINTER(ctypes.c_int)], _I),
 }
 
 _lib = None
@@ -302,6 +303,19 @@ def moe_route_topk_bwd(d_w, topk_w, topk_idx, x, Wr, dx_acc, T, H, E, k, dWr, dx
           _stream(stream))
 
 
+def moe_set_gemm_sm_limit(max_sms: int) -> int:
+    """Limit the grouped GEMMs issued from this thread to max_sms SMs (0 = all);
+    returns the previous limit."""
+    prev = ctypes.c_int(0)
+    _call("moe_set_gemm_sm_limit", int(max_sms), ctypes.byref(prev))
+    return prev.value
+
+
+def sm_count(device=None) -> int:
+    return torch.cuda.get_device_properties(device if device is not None else torch.cuda.current_device()) \
+        .multi_processor_count
+
+
 from .layer import MoELayer  # noqa: E402  (buffers + call sequence over the entry points)
 
 __all__.append("MoELayer")
@@ -312,3 +326,4 @@ def moe_probe_fma(packed, per_sm, iters, out, stream=None) -> int:
     n = ctypes.c_longlong(0)
     _call("moe_probe_fma", int(packed), int(per_sm), int(iters), _ptr(out), ctypes.byref(n), _stream(stream))
     return int(n.value)
+

@@ -966,6 +966,8 @@ int pick_bn(int n) { return n % 256 == 0 ? 256 : (n % 128 == 0 ? 128 : 64); }
 bool use_pair(int bn) { return bn >= 128; }
 
 bool g_attr[kNumKinds][2][64] = {};
+// SMs the persistent GEMM grids may use, for launches from this thread (0: all)
+thread_local int g_gemm_sm_limit = 0;
 
 // Launches grouped_gemm_kernel<KIND, CTAS>: completes the CTAS-dependent
 // parameters, sizes the shared memory to the segment tables and the
@@ -995,8 +997,9 @@ int launch(Params p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensor
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
     g_attr[KIND][CTAS - 1][dev] = true;
   }
-  const int sms = sm_count();
+  int sms = sm_count();
   if (sms <= 0) return fail(MOE_ERR_CUDA, "%s: cannot query the SM count", what);
+  if (g_gemm_sm_limit > 0 && g_gemm_sm_limit < sms) sms = g_gemm_sm_limit;
   const long long units_max = sms / CTAS;
   long long units = upper < units_max ? upper : units_max;
   if (units < 1) units = 1;
@@ -1228,6 +1231,14 @@ int swiglu_fp8_impl(const void* a, const float* a_scale, const int32_t* gather_r
 }  // namespace moe
 
 extern "C" {
+
+int moe_set_gemm_sm_limit(int max_sms, int* previous) {
+  clear_error();
+  if (max_sms < 0) return fail(MOE_ERR_INVALID_ARG, "moe_set_gemm_sm_limit: max_sms must be >= 0");
+  if (previous) *previous = g_gemm_sm_limit;
+  g_gemm_sm_limit = max_sms;
+  return MOE_OK;
+}
 
 size_t moe_grouped_gemm_bwd_workspace_size(int num_seg) {
   return num_seg > 0 ? (size_t)num_seg * kSegMapBytes : 0;

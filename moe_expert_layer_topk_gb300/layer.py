@@ -12,7 +12,8 @@ import torch
 from . import (moe_combine, moe_combine_bwd, moe_dispatch_bwd, moe_dispatch_chunked,
                moe_dispatch_e4m3_chunked, moe_grouped_gemm_bwd_workspace_size,
                moe_grouped_gemm_down, moe_grouped_gemm_down_bwd, moe_grouped_gemm_down_fp8,
-               moe_grouped_gemm_swiglu, moe_grouped_gemm_swiglu_bwd, moe_grouped_gemm_swiglu_fp8,
+               moe_grouped_gemm_swiglu, moe_grouped_gemm_swiglu_bwd_dw, moe_grouped_gemm_swiglu_bwd_dx,
+               moe_grouped_gemm_swiglu_fp8, moe_set_gemm_sm_limit, sm_count,
                moe_grouped_gemm_swiglu_gather, moe_quantize_rows_e4m3, moe_route_topk_bwd,
                moe_route_topk_bwd_workspace_size, moe_route_topk_chunks,
                moe_route_topk_chunks_workspace_size)
@@ -47,6 +48,7 @@ class MoELayer:
         self.fused_dispatch = fused_dispatch
         self.fp8 = fp8
         self._x = None
+        self._side = None  # side stream of the backward's tail (created on first use)
         dev = torch.device(device)
         i32, f32, bf = torch.int32, torch.float32, torch.bfloat16
         e = lambda *s, dt: torch.empty(*s, dtype=dt, device=dev)  # noqa: E731
@@ -144,8 +146,20 @@ class MoELayer:
         return self.y if y is None else y
 
     # --------------------------------------------------------------- backward
-    def backward(self, dy, x, Wr, Wg, Wu, Wd, accumulate: bool = False, stream=None, dx=None):
-        """dx: optional bf16 [T,H] output tensor (default: the layer's own)."""
+    # SMs left free for the backward's tail (dispatch and router backward, on
+    # a side stream) while the gate/up weight-gradient GEMM runs: measured at
+    # T=8192 on GB300, the two together took 514 us this way against 558 us
+    # one after the other (525 us on two streams with no limit).
+    TAIL_SMS = 16
+
+    def backward(self, dy, x, Wr, Wg, Wu, Wd, accumulate: bool = False, stream=None, dx=None,
+                 overlap: bool = True):
+        """dx: optional bf16 [T,H] output tensor (default: the layer's own).
+
+        overlap: run the dispatch and router backward on a side stream beside
+        the gate/up weight gradient (which then leaves TAIL_SMS SMs free);
+        the results are the same either way, and the call returns with the
+        work of both streams ordered before anything later on `stream`."""
         assert self.training, "layer was built without backward buffers"
         dx = self.dx if dx is None else dx
         T, H, I, E, k, R = self.T, self.H, self.I, self.E, self.k, self.R
@@ -153,10 +167,30 @@ class MoELayer:
                         self.d_w, stream)
         moe_grouped_gemm_down_bwd(self.dy_perm, self.h, self.gu, Wd, E, self.offsets, None, R, H, I,
                                   E, self.dgu, self.dWd, accumulate, self.ws_gemm_bwd, stream)
-        moe_grouped_gemm_swiglu_bwd(self.dgu, self.x_perm, Wg, Wu, E, self.offsets, None, R, H, I, E,
-                                    self.dx_perm, self.dWg, self.dWu, accumulate, self.ws_gemm_bwd,
-                                    stream)
-        moe_dispatch_bwd(self.dx_perm, self.row_of_slot, T, H, k, self.dx_acc, stream)
+        moe_grouped_gemm_swiglu_bwd_dx(self.dgu, Wg, Wu, E, self.offsets, None, R, H, I, E, self.dx_perm,
+                                       stream)
+        tail = stream
+        if overlap:
+            main = stream if stream is not None else torch.cuda.current_stream(self.dx_perm.device)
+            if self._side is None:
+                self._side = torch.cuda.Stream(self.dx_perm.device)
+                self._ev_fork, self._ev_join = torch.cuda.Event(), torch.cuda.Event()
+            self._ev_fork.record(main)
+            self._side.wait_event(self._ev_fork)
+            tail = self._side
+            prev = moe_set_gemm_sm_limit(max(1, sm_count(self.dx_perm.device) - self.TAIL_SMS))
+            try:
+                moe_grouped_gemm_swiglu_bwd_dw(self.dgu, self.x_perm, E, self.offsets, None, R, H, I, E, self.dWg,
+                                               self.dWu, accumulate, self.ws_gemm_bwd, main)
+            finally:
+                moe_set_gemm_sm_limit(prev)
+        else:
+            moe_grouped_gemm_swiglu_bwd_dw(self.dgu, self.x_perm, E, self.offsets, None, R, H, I, E, self.dWg,
+                                           self.dWu, accumulate, self.ws_gemm_bwd, stream)
+        moe_dispatch_bwd(self.dx_perm, self.row_of_slot, T, H, k, self.dx_acc, tail)
         moe_route_topk_bwd(self.d_w, self.topk_w, self.topk_idx, x, Wr, self.dx_acc, T, H, E, k,
-                           self.dWr, dx, accumulate, self.ws_route_bwd, stream)
+                           self.dWr, dx, accumulate, self.ws_route_bwd, tail)
+        if overlap:
+            self._ev_join.record(self._side)
+            main.wait_event(self._ev_join)
         return dx

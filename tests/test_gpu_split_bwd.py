@@ -89,3 +89,56 @@ def test_split_halves_segments_accumulate_two_streams():
         assert torch.equal(got, ref), name
     assert not torch.equal(dWd, prev[0])
 
+
+
+def test_sm_limit_changes_no_result():
+    """A limit on the GEMMs' persistent grid (here 20 SMs, and 1) changes
+    nothing in the results; the previous limit comes back."""
+    inp = inputs(700, 256, 128, 10, 3, seed=83)
+    g = to_dev(inp)
+    T, H, I, E, k = 700, 256, 128, 10, 3
+    L = m.MoELayer(T, H, I, E, k, 1)
+    L.forward(g["x"], g["Wr"], None, g["Wg"], g["Wu"], g["Wd"])
+    L.backward(g["dy"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"], overlap=False)
+    torch.cuda.synchronize()
+    ref = {n: getattr(L, n).clone() for n in ("y", "dgu", "dx_perm", "dWg", "dWu", "dWd", "dWr", "dx")}
+    for limit in (20, 1):
+        assert m.moe_set_gemm_sm_limit(limit) == 0
+        try:
+            L.forward(g["x"], g["Wr"], None, g["Wg"], g["Wu"], g["Wd"])
+            L.backward(g["dy"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"], overlap=False)
+        finally:
+            assert m.moe_set_gemm_sm_limit(0) == limit
+        torch.cuda.synchronize()
+        assert m.moe_read_device_status(reset=True) == 0
+        for n, v in ref.items():
+            assert torch.equal(getattr(L, n), v), (limit, n)
+
+
+def test_layer_backward_overlap_matches_one_stream():
+    """The backward with its dispatch and router tail on a side stream gives
+    the one-stream results bit for bit, also on a caller's own stream and
+    with accumulation into the weight gradients."""
+    inp = inputs(900, 256, 128, 16, 4, seed=84, ep=2)
+    g = to_dev(inp)
+    T, H, I, E, k = 900, 256, 128, 16, 4
+    L = m.MoELayer(T, H, I, E, k, 2)
+    L.forward(g["x"], g["Wr"], None, g["Wg"], g["Wu"], g["Wd"])
+    L.backward(g["dy"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"], overlap=False)
+    torch.cuda.synchronize()
+    names = ("dgu", "dx_perm", "dx_acc", "dWg", "dWu", "dWd", "dWr", "dx")
+    ref = {n: getattr(L, n).clone() for n in names}
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for n in names:
+            getattr(L, n).fill_(7.0)
+        L.backward(g["dy"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"], stream=s)
+    s.synchronize()
+    assert m.moe_read_device_status(reset=True) == 0
+    for n in names:
+        assert torch.equal(getattr(L, n), ref[n]), n
+    # accumulate: a second overlapped pass adds the same gradients again
+    L.backward(g["dy"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"], accumulate=True)
+    torch.cuda.synchronize()
+    for n in ("dWg", "dWu", "dWd", "dWr"):
+        assert torch.equal(getattr(L, n), ref[n] + ref[n]), n
