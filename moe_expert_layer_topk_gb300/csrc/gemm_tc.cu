@@ -585,11 +585,11 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
     // Each warp owns 32 accumulator rows of the tile (TMEM lanes
     // 32*(warp%4)..+31).  Results leave in boxes of 32 rows x 64 bytes:
     // every lane writes its own row of the box into shared memory (64-byte
-    // swizzle, conflict-free), then the warp reads the box back row-segment
-    // by row-segment and writes it with coalesced 16-byte stores (8 full
-    // 64-byte row segments per instruction), skipping rows past the end of
-    // the expert's rows.  These stores do not queue behind the operand
-    // loads on the TMA unit.
+    // swizzle, conflict-free); then either a TMA bulk store writes the box
+    // (the kinds named at kTmaOut, when all 32 rows are valid), or the warp
+    // reads the box back row-segment by row-segment and writes it with
+    // coalesced 16-byte stores (8 full 64-byte row segments per
+    // instruction), skipping rows past the end of the expert's rows.
     const int q = warp & 3;
     uint8_t* ep_base = smem + (size_t)STG * C::STAGE_BYTES + (size_t)(warp - 2) * C::EP_WARP;
     const int sw = (lane >> 1) & 3;  // 64-byte swizzle phase of this lane's row
@@ -620,8 +620,10 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
       }
       __syncwarp();
     };
-    // Full boxes of the fp32 weight gradients and of the down projection go
-    // out through TMA bulk stores instead (measured faster for those two).
+    // Full boxes of the fp32 weight gradients, of the down projection and of
+    // the SwiGLU backward's dg, du go out through TMA bulk stores instead
+    // (measured faster for those three; for h, g, u of the gate/up forward
+    // they measured no different).
     constexpr bool kTmaOut = KIND == DW || is_down_fwd(KIND);
     EpRing<C::RING> ring{ep_base, 0, lane};
     int gu_ctr = 0;  // DENSE_ADD: running count of this warp's 32-column chunks
@@ -820,7 +822,9 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
       } else if constexpr (KIND == DOWN_BWD_DX) {
         // The saved g, u of this lane's row and chunk come from global memory
         // straight into registers, one chunk ahead; dg and du leave through
-        // the warp's box as coalesced row stores.
+        // the warp's box by TMA stores (measured 15 us faster at T=8192 than
+        // coalesced row stores from the box, which only the last rows of a
+        // segment still use).
         const size_t pitch = (size_t)p.I * 4;
         for (int c = cbeg; any && c < cbeg + cspan; c += 32) {
           uint4 gn[4], un[4];
@@ -852,12 +856,24 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
             og4[i] = make_uint4(og[0], og[1], og[2], og[3]);
             ou4[i] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
           }
+          if (nvalid == 32) {
+            uint8_t* bx = ring.acquire();
 #pragma unroll
-          for (int i = 0; i < 4; ++i) put(ep_base, i, og4[i]);
-          flush(ep_base, p.out0, pitch, (size_t)(t.n0 + c) * 2, rb, nvalid, false);
+            for (int i = 0; i < 4; ++i) ring.put(bx, i, og4[i]);
+            ring.issue(bx, &tmO0, t.n0 + c, rb);
+            bx = ring.acquire();
 #pragma unroll
-          for (int i = 0; i < 4; ++i) put(ep_base, i, ou4[i]);
-          flush(ep_base, p.out0, pitch, (size_t)(p.I + t.n0 + c) * 2, rb, nvalid, false);
+            for (int i = 0; i < 4; ++i) ring.put(bx, i, ou4[i]);
+            ring.issue(bx, &tmO0, p.I + t.n0 + c, rb);
+          } else {  // the last rows of a segment: masked row stores
+            uint8_t* bx = ring.acquire();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) put(bx, i, og4[i]);
+            flush(bx, p.out0, pitch, (size_t)(t.n0 + c) * 2, rb, nvalid, false);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) put(bx, i, ou4[i]);
+            flush(bx, p.out0, pitch, (size_t)(p.I + t.n0 + c) * 2, rb, nvalid, false);
+          }
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             gq[i] = gn[i];
