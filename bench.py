@@ -642,6 +642,23 @@ def run_fwd_workload(m, name, dev, stream, args, pk):
            "empty_experts": int((counts == 0).sum()), "max_expert_rows": int(counts.max())}
     if shape.bias == "zipf":
         out["routing"] = "Zipf(1.2) expert popularity from a router bias, 4 experts forced empty"
+    if name == "tiny_fwd":
+        # the same forward replayed as one CUDA graph (launch-bound batch)
+        graph = L.capture_forward(g["x"], g["Wr"], g["bias"], g["Wg"], g["Wu"], g["Wd"])
+        for _ in range(args.warmup):
+            graph.replay()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        g0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        g1.record(stream)
+        torch.cuda.synchronize(dev)
+        if m.moe_read_device_status(reset=True) != 0:
+            raise RuntimeError("device status word set during the graphed tiny forward")
+        gms = g0.elapsed_time(g1) / args.steps
+        out["graph"] = {"tokens_per_s": T / (gms * 1e-3), "ms": gms,
+                        "path": "MoELayer.forward captured once as a CUDA graph, replayed"}
     return out
 
 

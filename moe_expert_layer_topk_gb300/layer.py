@@ -145,6 +145,22 @@ class MoELayer:
         self.combine(stream, y)
         return self.y if y is None else y
 
+    def capture_forward(self, x, Wr, bias, Wg, Wu, Wd) -> "torch.cuda.CUDAGraph":
+        """Record forward() on these tensors as a CUDA graph and return it.
+
+        `graph.replay()` then re-runs the whole forward (all its kernels,
+        one launch from the host) on whatever the same tensors hold, into
+        the layer's own y: for small batches, whose forward is bound by the
+        host issuing one call per kernel.  One forward runs first, outside
+        the capture, so that each call's first-use set-up (kernel
+        attributes, the device status word) is done before it."""
+        self.forward(x, Wr, bias, Wg, Wu, Wd)
+        torch.cuda.synchronize(self.y.device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self.forward(x, Wr, bias, Wg, Wu, Wd)
+        return graph
+
     # --------------------------------------------------------------- backward
     # SMs left free for the backward's tail (dispatch and router backward, on
     # a side stream) while the gate/up weight-gradient GEMM runs: measured at

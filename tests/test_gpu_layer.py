@@ -124,3 +124,28 @@ def test_deterministic(run):
     torch.cuda.synchronize()
     for n, v in keep.items():
         assert torch.equal(getattr(L, n), v), n
+
+
+def test_forward_replayed_as_cuda_graph():
+    """MoELayer.capture_forward: replaying the captured forward gives the
+    eager forward's y, also after new values are written into x."""
+    T, H, I, E, k = 256, 128, 64, 8, 2
+    inp = inputs(T, H, I, E, k, seed=95, with_dy=False)
+    g = to_dev(inp)
+    L = m.MoELayer(T, H, I, E, k, 1, training=False)
+    graph = L.capture_forward(g["x"], g["Wr"], None, g["Wg"], g["Wu"], g["Wd"])
+    graph.replay()
+    torch.cuda.synchronize()
+    y_graph = L.y.clone()
+    L.forward(g["x"], g["Wr"], None, g["Wg"], g["Wu"], g["Wd"])
+    torch.cuda.synchronize()
+    assert torch.equal(y_graph, L.y)
+    x2 = inputs(T, H, I, E, k, seed=96, with_dy=False)["x"].cuda()
+    g["x"].copy_(x2)
+    graph.replay()
+    torch.cuda.synchronize()
+    y2 = L.y.clone()
+    L.forward(g["x"], g["Wr"], None, g["Wg"], g["Wu"], g["Wd"])
+    torch.cuda.synchronize()
+    assert torch.equal(y2, L.y) and not torch.equal(y2, y_graph)
+    assert m.moe_read_device_status(reset=True) == 0
