@@ -139,3 +139,20 @@ def test_fp8_entry_points_reject_bad_args(L):
     # no rows: nothing to do
     assert L.moe_grouped_gemm_swiglu_fp8(P, P, None, 0, P, P, P, P, 8, P, None, 0, 128, 128, 8, P, None) == OK
     assert L.moe_grouped_gemm_down_fp8(P, P, P, P, 8, P, None, 0, 128, 128, 8, P, None) == OK
+
+
+def test_gemm_sm_limit_is_host_state(L):
+    """The GEMM grid limit is a per-thread host setting: set, read back as
+    the previous value, and rejected when negative (no device needed)."""
+    prev = ctypes.c_int(-1)
+    assert L.moe_set_gemm_sm_limit(5, ctypes.byref(prev)) == OK and prev.value == 0
+    assert L.moe_set_gemm_sm_limit(0, ctypes.byref(prev)) == OK and prev.value == 5
+    assert L.moe_set_gemm_sm_limit(-1, None) == INVALID
+    assert m.moe_set_gemm_sm_limit(0) == 0
+
+
+def test_fma_probe_rejects_bad_arguments(L):
+    n = ctypes.c_longlong(0)
+    assert L.moe_probe_fma(0, 0, 16, FAKE, ctypes.byref(n), None) == INVALID     # per_sm < 1
+    assert L.moe_probe_fma(1, 4, 0, FAKE, ctypes.byref(n), None) == INVALID     # iters < 1
+    assert L.moe_probe_fma(0, 4, 16, None, ctypes.byref(n), None) == INVALID    # no out

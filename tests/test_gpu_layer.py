@@ -149,3 +149,15 @@ def test_forward_replayed_as_cuda_graph():
     torch.cuda.synchronize()
     assert torch.equal(y2, L.y) and not torch.equal(y2, y_graph)
     assert m.moe_read_device_status(reset=True) == 0
+
+
+def test_fma_probe_counts_its_work():
+    """The FMA probe performs SMs x per_sm CTAs x 256 threads x 8 chains x
+    16 x iters fused multiply-adds, and never writes its guard output."""
+    out = torch.full((1,), -3.0, device="cuda")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for packed in (0, 1):
+        n = m.moe_probe_fma(packed, 2, 3, out)
+        torch.cuda.synchronize()
+        assert n == sms * 2 * 256 * 8 * 16 * 3
+    assert out.item() == -3.0
