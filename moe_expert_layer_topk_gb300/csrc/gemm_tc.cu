@@ -184,7 +184,7 @@ struct Cfg {
   // without the segment tables
   static constexpr size_t SMEM_FIXED = 1024 + (size_t)STAGES * STAGE_BYTES + EP_TOTAL + sizeof(Ctl);
 };
-// the configurations launched (cluster pairs for GATE_UP_FWD and GATE_UP_BWD_DX)
+// the configurations launched (cluster pairs for GATE_UP_FWD, GATE_UP_BWD_DX and DOWN_FWD)
 static_assert(Cfg<GATE_UP_FWD, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<GATE_UP_GATHER, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<GATE_UP_FP8, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
@@ -195,6 +195,7 @@ static_assert(Cfg<GATE_UP_FWD, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<GATE_UP_BWD_DX, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<GATE_UP_BWD_DX, 2>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<GATE_UP_FWD, 2>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
+                  Cfg<DOWN_FWD, 2>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<DENSE_ADD, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<DW, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax,
               "shared memory budget exceeded");
@@ -246,11 +247,12 @@ __device__ __forceinline__ void for_each_kblock(const Tile& t, const Params& p, 
     for (int kb = 0; kb < nkb; ++kb)
       if (!f(kb * KB, KB, t.seg)) return;
   } else if (p.seg_expert == nullptr) {
-    // identity table: group g owns exactly segment g
-    const int len = ctl->seg_off[t.group + 1] - ctl->seg_off[t.group];
-    if (ctl->seg_exp[t.group] >= 0)
+    // identity table: group g owns exactly segment g (none for g >= num_seg)
+    if (t.group < p.num_seg && ctl->seg_exp[t.group] >= 0) {
+      const int len = ctl->seg_off[t.group + 1] - ctl->seg_off[t.group];
       for (int r = 0; r < len; r += BK)
         if (!f(r, min(BK, len - r), t.group)) return;
+    }
   } else {
     for (int s = 0; s < p.num_seg; ++s) {
       if (ctl->seg_exp[s] != t.group) continue;
@@ -456,9 +458,28 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      int map_seg = -1;  // DW: segment whose maps this thread last acquired
+      // DW: segments whose maps this thread has acquired: the one in use,
+      // this tile's (acquired a tile ahead) and the next tile's
+      int map_seg = -1, this_seg = -1, next_seg = -1;
       for (int tile = unit; ok && tile < total; tile += nunits) {
         const Tile t = decode_tile<KIND, CTAS>(tile, p, ctl, rank);
+        if constexpr (KIND == DW) {
+          // with one segment per group, the next tile's maps are acquired
+          // and prefetched now, so their fetch overlaps this tile's loads
+          this_seg = next_seg;
+          next_seg = -1;
+          if (p.seg_expert == nullptr && tile + nunits < total) {
+            const int g = decode_tile<KIND, CTAS>(tile + nunits, p, ctl, rank).group;
+            if (g < p.num_seg && ctl->seg_exp[g] >= 0 && g != this_seg && g != map_seg) {
+              const CUtensorMap* mn = p.seg_maps + 2 * g;
+              tmap_acquire(mn);
+              tmap_acquire(mn + 1);
+              prefetch_tmap(mn);
+              prefetch_tmap(mn + 1);
+              next_seg = g;
+            }
+          }
+        }
         for_each_kblock<KIND>(t, p, ctl, [&](int row0, int, int seg) -> bool {
           if (!wait_bar(smem_u32(&ctl->empty[stage]), phase ^ 1u, &ctl->abort_flag, p.status)) {
             ok = false;
@@ -474,11 +495,11 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
             // the segment's own maps end at its last row: TMA fills the
             // rows of a tail k-block past it with zeros
             const CUtensorMap* ma = p.seg_maps + 2 * seg;
-            if (seg != map_seg) {
+            if (seg != map_seg && seg != this_seg && seg != next_seg) {
               tmap_acquire(ma);
               tmap_acquire(ma + 1);
-              map_seg = seg;
             }
+            map_seg = seg;
             tma_load_mn<CTAS>(sA, ma, fb, row0, t.m0 / 64);
             tma_load_mn<CTAS>(sB, ma + 1, fb, row0, t.n0 / 64 + ck0);
           } else {
@@ -976,9 +997,9 @@ int pick_bn(int n) { return n % 256 == 0 ? 256 : (n % 128 == 0 ? 128 : 64); }
 
 // Cluster pairs (256-row tiles) need at least 128 output columns per tile
 // (64 per CTA).  They are used where they measured faster: the gate/up
-// backward dX GEMM always, and the gate/up forward GEMM on permuted rows in
-// the dispatch layout (see swiglu_impl).  Every other kind runs one CTA per
-// 128-row tile.
+// backward dX GEMM, the bf16 down projection, and the gate/up forward GEMM
+// on permuted rows in the dispatch layout (see swiglu_impl).  Every other
+// kind runs one CTA per 128-row tile.
 bool use_pair(int bn) { return bn >= 128; }
 
 bool g_attr[kNumKinds][2][64] = {};
@@ -1042,12 +1063,12 @@ int launch(Params p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensor
 }
 
 // Cluster pairs are built for the gate/up GEMMs on permuted rows (forward
-// and backward dX), where they measured faster; the down-projection kinds
-// measured no faster (forward) or slower (backward dX) as pairs.
+// and backward dX) and the bf16 down projection, where they measured
+// faster; the down backward dX kind measured slower as pairs.
 template <int KIND>
 int run(bool pair, const Params& p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
         const CUtensorMap& o0, const CUtensorMap& o1, cudaStream_t s, const char* what) {
-  if constexpr (KIND == GATE_UP_BWD_DX || KIND == GATE_UP_FWD) {
+  if constexpr (KIND == GATE_UP_BWD_DX || KIND == GATE_UP_FWD || KIND == DOWN_FWD) {
     if (pair) return launch<KIND, 2>(p, a, b0, b1, o0, o1, s, what);
   }
   return launch<KIND, 1>(p, a, b0, b1, o0, o1, s, what);
@@ -1368,8 +1389,9 @@ int moe_grouped_gemm_down(const void* h, const void* Wd, int num_seg, const int3
   p.out0 = y_perm;
   CUtensorMap ta, tb;
   if (int rc = make_tmap(&ta, h, I, R, 64, BM)) return rc;
-  const bool pair = false;
-  if (int rc = make_tmap(&tb, Wd, I, (uint64_t)E * H, 64, p.BN)) return rc;
+  // pairs with one segment per expert, as for the gate/up forward
+  const bool pair = use_pair(p.BN) && num_seg <= E;
+  if (int rc = make_tmap(&tb, Wd, I, (uint64_t)E * H, 64, p.BN / (pair ? 2 : 1))) return rc;
   CUtensorMap to;
   if (int rc = make_out_map(&to, y_perm, H, R, false)) return rc;
   return run<DOWN_FWD>(pair, p, ta, tb, tb, to, to, static_cast<cudaStream_t>(stream), fn);

@@ -195,6 +195,58 @@ def test_segmented_rows(R, H, I, E, S):
     assert_close(dWu, dWu_ref, "dWu")
 
 
+def test_identity_table_with_fewer_segments_than_experts():
+    """A null seg_expert with num_seg < E: segment s holds expert s's rows and
+    the experts past the last segment have none, so their weight gradients
+    are zeros, or stay as they were when accumulating."""
+    R, H, I, E = 400, 128, 128, 6
+    shape = LayerShape(T=R, H=H, I=I, E=E, k=1, ep_size=1, segments=True, src_ranks=1)
+    s = make_segment_inputs(shape, seed=23)
+    so = torch.tensor([0, 100, 100, 250, 400], dtype=torch.int32)  # segment 1 empty
+    dev = "cuda"
+    xp, Wg, Wu, Wd = (s[n].to(dev) for n in ("x_perm", "Wg", "Wu", "Wd"))
+    so_d = so.to(dev)
+    nseg = len(so) - 1
+    h = torch.zeros(R, I, dtype=torch.bfloat16, device=dev)
+    gu = torch.zeros(R, 2 * I, dtype=torch.bfloat16, device=dev)
+    m.moe_grouped_gemm_swiglu(xp, Wg, Wu, nseg, so_d, None, R, H, I, E, h, gu)
+    dy_host = torch.randn(R, H, generator=torch.Generator().manual_seed(31)).to(torch.bfloat16)
+    dy = dy_host.to(dev)
+    dgu = torch.zeros(R, 2 * I, dtype=torch.bfloat16, device=dev)
+    dx = torch.zeros(R, H, dtype=torch.bfloat16, device=dev)
+    dWd = torch.full((E, H, I), float("nan"), device=dev)
+    dWg = torch.full((E, I, H), float("nan"), device=dev)
+    dWu = torch.full((E, I, H), float("nan"), device=dev)
+    ws = torch.empty(m.moe_grouped_gemm_bwd_workspace_size(nseg), dtype=torch.uint8, device=dev)
+    m.moe_grouped_gemm_down_bwd(dy, h, gu, Wd, nseg, so_d, None, R, H, I, E, dgu, dWd, 0, ws)
+    m.moe_grouped_gemm_swiglu_bwd(dgu, xp, Wg, Wu, nseg, so_d, None, R, H, I, E, dx, dWg, dWu, 0, ws)
+    torch.cuda.synchronize()
+    assert m.moe_read_device_status(reset=True) == 0
+    son = so.numpy()
+    xo = oracle.widen_bf16(bf16_bits(s["x_perm"]))
+    h_ref, gu_ref = oracle.grouped_gemm_swiglu(xo, bf16_bits(s["Wg"]), bf16_bits(s["Wu"]), son,
+                                               save_gu=True)
+    dy_ref = oracle.widen_bf16(bf16_bits(dy_host))
+    dgu_ref, dWd_ref = oracle.grouped_gemm_down_bwd(dy_ref, h_ref, gu_ref, bf16_bits(s["Wd"]), son)
+    dx_ref, dWg_ref, dWu_ref = oracle.grouped_gemm_swiglu_bwd(dgu_ref, xo, bf16_bits(s["Wg"]),
+                                                              bf16_bits(s["Wu"]), son)
+    for ref in (dWd_ref, dWg_ref, dWu_ref):
+        assert np.all(ref[nseg:] == 0) and np.all(ref[1] == 0)
+    assert_close(dgu, dgu_ref, "dgu")
+    assert_close(dWd, dWd_ref, "dWd")
+    assert_close(dx, dx_ref, "dx_perm")
+    assert_close(dWg, dWg_ref, "dWg")
+    assert_close(dWu, dWu_ref, "dWu")
+    # accumulating: experts without rows keep their values bit for bit
+    before = [t.clone() for t in (dWd, dWg, dWu)]
+    m.moe_grouped_gemm_down_bwd(dy, h, gu, Wd, nseg, so_d, None, R, H, I, E, dgu, dWd, 1, ws)
+    m.moe_grouped_gemm_swiglu_bwd(dgu, xp, Wg, Wu, nseg, so_d, None, R, H, I, E, dx, dWg, dWu, 1, ws)
+    torch.cuda.synchronize()
+    assert m.moe_read_device_status(reset=True) == 0
+    for t, b in zip((dWd, dWg, dWu), before):
+        assert torch.equal(t[nseg:], b[nseg:]) and torch.equal(t[1], b[1])
+        assert torch.equal(t[[0, 2, 3]], 2 * b[[0, 2, 3]])
+
 def test_bad_index_data_sets_status_without_fault():
     """Out-of-range expert ids and offsets that disagree with them are skipped
     by the kernels and reported through the device status word."""
