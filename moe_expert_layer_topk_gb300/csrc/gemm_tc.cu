@@ -682,10 +682,17 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
 #pragma unroll
         for (int a = 0; a < GU_AHEAD; ++a) gu_load(32 * a, gu_ctr + a);
       }
-      // with eight epilogue warps, warps 2..5 take the first half of the
-      // tile's columns and warps 6..9 the second
-      const int cspan = p.BN / (C::EPW / 4);
-      const int cbeg = ((warp - 2) >> 2) * cspan;
+      // With eight epilogue warps the two warps of a TMEM lane quadrant
+      // share the tile's 32-column chunks.  The SwiGLU-backward kind
+      // alternates them (warps 2..5 the even chunks, 6..9 the odd ones), so
+      // that both halves of each 128-byte row segment of g, u (read) and of
+      // dg, du (written) are touched at about the same time; the other kinds
+      // split the columns in halves (warps 2..5 the first, 6..9 the second).
+      constexpr bool kAlt = KIND == DOWN_BWD_DX;
+      const int sub = (warp - 2) >> 2, nsub = C::EPW / 4;
+      const int cbeg = kAlt ? 32 * sub : sub * (p.BN / nsub);
+      const int cstep = kAlt ? 32 * nsub : 32;
+      const int cend = kAlt ? p.BN : cbeg + p.BN / nsub;
       // SwiGLU backward: this lane's row of the saved g, u for a 32-column chunk
       uint4 gq[4], uq[4];
       auto ld_gu = [&](int c, uint4 (&g4)[4], uint4 (&u4)[4]) {
@@ -774,10 +781,10 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
         }
       } else if constexpr (is_down_fwd(KIND) || KIND == GATE_UP_BWD_DX) {
         const size_t pitch = (size_t)p.ldo * 2;
-        for (int c = cbeg; any && c < cbeg + cspan; c += 32) {
+        for (int c = cbeg; any && c < cend; c += cstep) {
           float nx0 = 0.0f;  // FP8: the next chunk's column scales
           if constexpr (is_fp8(KIND)) {
-            if (c + 32 < cbeg + cspan) nx0 = __ldg(p.b_scale0 + cs_base + c + 32 + lane);
+            if (c + cstep < cend) nx0 = __ldg(p.b_scale0 + cs_base + c + cstep + lane);
           }
           uint32_t a[32];
           tmem_ld32(taddr + c, a);
@@ -847,9 +854,9 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
         // coalesced row stores from the box, which only the last rows of a
         // segment still use).
         const size_t pitch = (size_t)p.I * 4;
-        for (int c = cbeg; any && c < cbeg + cspan; c += 32) {
+        for (int c = cbeg; any && c < cend; c += cstep) {
           uint4 gn[4], un[4];
-          if (c + 32 < cbeg + cspan) ld_gu(c + 32, gn, un);
+          if (c + cstep < cend) ld_gu(c + cstep, gn, un);
           uint32_t a[32];
           tmem_ld32(taddr + c, a);
           tmem_wait_ld();
@@ -907,7 +914,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
           const bool second = p.split_m > 0 && rb >= p.split_m;
           const int y = p.split_m > 0 ? t.group * p.split_m + (second ? rb - p.split_m : rb)
                                       : t.group * p.M + rb;
-          for (int c = cbeg; c < cbeg + cspan; c += 32) {
+          for (int c = cbeg; c < cend; c += cstep) {
             uint32_t a[32];
             if (nonempty) {
               tmem_ld32(taddr + c, a);
