@@ -914,6 +914,10 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
           const bool second = p.split_m > 0 && rb >= p.split_m;
           const int y = p.split_m > 0 ? t.group * p.split_m + (second ? rb - p.split_m : rb)
                                       : t.group * p.M + rb;
+          // the written fp32 lines under an evict-last L2 policy (measured
+          // 414 -> 392 us for dW_gate/up at T=8192 against the default
+          // policy, 422 with evict-first)
+          const uint64_t pol = l2_policy_evict_last();
           for (int c = cbeg; c < cend; c += cstep) {
             uint32_t a[32];
             if (nonempty) {
@@ -930,7 +934,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
               for (int i = 0; i < 4; ++i)
                 ring.put(bx, i, make_uint4(a[16 * half + 4 * i], a[16 * half + 4 * i + 1],
                                            a[16 * half + 4 * i + 2], a[16 * half + 4 * i + 3]));
-              ring.issue(bx, second ? &tmO1 : &tmO0, t.n0 + c + 16 * half, y, p.accumulate != 0);
+              ring.issue_hint(bx, second ? &tmO1 : &tmO0, t.n0 + c + 16 * half, y, p.accumulate != 0, pol);
             }
           }
         }

@@ -112,6 +112,32 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32
       : "memory");
 }
 
+// An L2 cache policy under which the lines an access touches are evicted
+// after evict-normal ones.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                                  uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "l"(pol)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_reduce_add_2d_hint(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                                       uint64_t pol) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], "
+      "%4;" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "l"(pol)
+      : "memory");
+}
+
 // One epilogue warp's staging ring (see EP_*).  Lane i holds row i of a box.
 template <int SLOTS = EP_SLOTS>
 struct EpRing {
@@ -137,6 +163,20 @@ struct EpRing {
         tma_reduce_add_2d(map, smem_u32(box), x, y);
       else
         tma_store_2d(map, smem_u32(box), x, y);
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+    slot = (slot + 1) & (SLOTS - 1);
+  }
+  // issue() with an L2 cache policy for the written lines
+  __device__ __forceinline__ void issue_hint(uint8_t* box, const CUtensorMap* map, int x, int y, bool reduce,
+                                             uint64_t pol) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+      if (reduce)
+        tma_reduce_add_2d_hint(map, smem_u32(box), x, y, pol);
+      else
+        tma_store_2d_hint(map, smem_u32(box), x, y, pol);
       asm volatile("cp.async.bulk.commit_group;" ::: "memory");
     }
     slot = (slot + 1) & (SLOTS - 1);
