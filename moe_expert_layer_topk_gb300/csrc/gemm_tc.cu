@@ -29,7 +29,7 @@
 //   warp 1      TMEM allocator + MMA issuer (one lane issues)
 //   warps 2..   epilogue: TMEM -> registers -> global (warp w reads TMEM
 //               lanes 32*(w%4)..+31, i.e. accumulator rows); four warps, or
-//               eight (two per lane quadrant, half the columns each) for the
+//               eight (two per lane quadrant, sharing the columns) for the
 //               weight-gradient, SwiGLU-backward and down-projection kinds
 //   last 4      row-gathering kinds only: they and warp 0 copy the A rows
 //               from x by token id with cp.async
@@ -37,8 +37,10 @@
 // row (64 bf16 or 128 e4m3 elements), 4-stage shared-memory ring (3 for the
 // router dX kind, whose epilogue stages its addend), two 256-column
 // accumulators in TMEM so the epilogue of tile i overlaps the MMAs of tile
-// i+1.  GATE_UP_BWD_DX, and GATE_UP_FWD in the dispatch layout (one segment
-// per expert), run as cluster pairs (tcgen05 cta_group::2, 256-row tiles).
+// i+1.  GATE_UP_BWD_DX, and GATE_UP_FWD and DOWN_FWD in the dispatch layout
+// (one segment per expert), run as cluster pairs (tcgen05 cta_group::2,
+// 256-row tiles).  The weight-gradient kind's TMA stores carry an
+// evict-last L2 policy.
 //
 // Every wait on an mbarrier is bounded (globaltimer): on timeout the CTA
 // records MOE_STATUS_TIMEOUT, all roles leave their loops, outstanding MMAs
@@ -171,7 +173,7 @@ struct Cfg {
   // The weight-gradient kind (fp32 output, short reductions), the
   // SwiGLU-backward kind (heavy epilogue) and the down projections (256
   // output columns per tile from a short reduction, K = I) run eight
-  // epilogue warps, two per TMEM lane quadrant, each on half the columns (a
+  // epilogue warps, two per TMEM lane quadrant sharing the columns (a
   // one-box store ring each).
   static constexpr bool EP8 = KIND == DW || KIND == DOWN_BWD_DX || is_down_fwd(KIND);
   static constexpr int EPW = EP8 ? 8 : 4;
