@@ -1010,10 +1010,20 @@ int pick_bn(int n) { return n % 256 == 0 ? 256 : (n % 128 == 0 ? 128 : 64); }
 
 // Cluster pairs (256-row tiles) need at least 128 output columns per tile
 // (64 per CTA).  They are used where they measured faster: the gate/up
-// backward dX GEMM, the bf16 down projection, and the gate/up forward GEMM
-// on permuted rows in the dispatch layout (see swiglu_impl).  Every other
-// kind runs one CTA per 128-row tile.
+// backward dX GEMM, and the bf16 down projection and gate/up forward GEMM
+// on permuted rows in the dispatch layout with enough rows per expert
+// (pair_for_rows).  Every other kind runs one CTA per 128-row tile.
 bool use_pair(int bn) { return bn >= 128; }
+
+// The forward row kinds take pairs only in the dispatch layout (one segment
+// per expert) and with at least 384 rows per segment on average: a pair
+// tile wastes up to 255 rows of a segment's last tile, a single CTA's up to
+// 127.  Measured at T=8192 (512 rows per expert): down 187 -> 181 us as
+// pairs, gate/up equal; at T=4096 (256 rows): single CTAs 1.6-1.7% faster
+// for both.
+bool pair_for_rows(int bn, int R, int num_seg, int E) {
+  return use_pair(bn) && num_seg <= E && (long long)R >= 384LL * num_seg;
+}
 
 bool g_attr[kNumKinds][2][64] = {};
 // SMs the persistent GEMM grids may use, for launches from this thread (0: all)
@@ -1226,11 +1236,10 @@ int swiglu_impl(const void* a_src, const int32_t* gather_rows, int T, const void
   if (int rc = make_out_map(&tgu, gu_save ? gu_save : h, gu_save ? 2 * I : I, R, false)) return rc;
   if (gather_rows) return run<GATE_UP_GATHER>(false, p, ta, tg, tu, th, tgu, s, fn);
   // Cluster pairs (the leader loads the gate rows of B, the peer the up rows)
-  // for the dispatch layout, one segment per expert: measured faster at 256
-  // and 512 rows per expert.  With several segments per expert (the EP
-  // receive layout) each expert's weights stay in L2 across its segments and
-  // the 256-row tiles waste more rows: single CTAs measured faster there.
-  const bool pair = use_pair(p.BN) && num_seg <= E;
+  // by pair_for_rows.  With several segments per expert (the EP receive
+  // layout) each expert's weights stay in L2 across its segments and the
+  // 256-row tiles waste more rows: single CTAs measured faster there.
+  const bool pair = pair_for_rows(p.BN, R, num_seg, E);
   return run<GATE_UP_FWD>(pair, p, ta, tg, tu, th, tgu, s, fn);
 }
 
@@ -1402,8 +1411,7 @@ int moe_grouped_gemm_down(const void* h, const void* Wd, int num_seg, const int3
   p.out0 = y_perm;
   CUtensorMap ta, tb;
   if (int rc = make_tmap(&ta, h, I, R, 64, BM)) return rc;
-  // pairs with one segment per expert, as for the gate/up forward
-  const bool pair = use_pair(p.BN) && num_seg <= E;
+  const bool pair = pair_for_rows(p.BN, R, num_seg, E);
   if (int rc = make_tmap(&tb, Wd, I, (uint64_t)E * H, 64, p.BN / (pair ? 2 : 1))) return rc;
   CUtensorMap to;
   if (int rc = make_out_map(&to, y_perm, H, R, false)) return rc;

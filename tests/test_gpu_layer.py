@@ -3,7 +3,8 @@
 Shapes are chosen so that every kernel runs several tiles with ragged tails:
 128-row GEMM tiles over row counts that are not multiples of 128, both
 gate/up tile widths (I % 128 == 0 -> 128-wide g and u halves, else 64), all
-three down-projection tile widths (H % 256, % 128, % 64), several ranking
+three down-projection tile widths (H % 256, % 128, % 64), cluster-pair
+tiles for the forward GEMMs (enough rows per expert), several ranking
 chunks, and both router variants (E % 8 == 0 vectorised, else scalar).
 Every stored tensor of the layer (routing, permutation, h, g|u, y_perm, y,
 dy_perm, d_w, dgu, dx_perm, dx_acc, dX and the weight gradients) is compared
@@ -33,6 +34,9 @@ CASES = {
     # kernel; E % 4 != 0 takes the scalar Wr loads
     "router_e130": (96, 256, 64, 130, 4, 2, None),
     "router_e256": (64, 320, 64, 256, 8, 8, None),
+    # about 512 rows per expert: the forward gate/up and down GEMMs run as
+    # cluster pairs (256-row tiles, ragged last tiles)
+    "pair_tiles": (1024, 256, 128, 4, 2, 2, None),
 }
 
 
