@@ -236,6 +236,27 @@ int moe_grouped_gemm_down(const void* h, const void* Wd, int num_seg, const int3
                           const int32_t* seg_expert, int R, int H, int I, int E, void* y_perm,
                           void* ws, size_t ws_bytes, void* stream);
 
+/* A5 + A6 fused (the second half of the pages' fused dispatcher,
+ * "FSDPTurbo EP/EFSDP and LlamaFactory FSDP2/CP Design" section 3: the
+ * grouped matmul and the unpermute as one operator): the down GEMM of A5
+ * whose epilogue scales each row r = row_of_slot[t,j] by topk_w[t,j] and
+ * adds it into y_acc[t] (fp32), then y = bf16(y_acc).  y_perm is never
+ * written.  The fp32 additions into a token's row happen in no fixed order
+ * (16-byte reductions in L2), so y may differ from moe_grouped_gemm_down +
+ * moe_combine (which add the k rows in slot order) by the rounding of that
+ * order: results are not bit-reproducible from run to run.
+ * token_of_row int32 [R], row_of_slot int32 [T,k] (moe_dispatch's);
+ * topk_w fp32 [T,k]; y_acc fp32 [T,H] (caller's scratch, zeroed by the call);
+ * y bf16 [T,H].  A row whose token or slot does not match is skipped; a
+ * token none of whose rows lies in a segment gets y = 0.  Forward only:
+ * the combine backward needs the unweighted rows.  It saves the R x H
+ * y_perm buffer; on GB300 it measured slower than moe_grouped_gemm_down +
+ * moe_combine (one 16-byte L2 reduction per 4 outputs). */
+int moe_grouped_gemm_down_combine(const void* h, const void* Wd, int num_seg, const int32_t* seg_offsets,
+                                  const int32_t* seg_expert, int R, int H, int I, int E,
+                                  const int32_t* token_of_row, const int32_t* row_of_slot,
+                                  const float* topk_w, int T, int k, float* y_acc, void* y, void* stream);
+
 /* ------------------------------------------------------------------------
  * FP8 (e4m3) forward GEMMs -- the second "next" step after the path.
  *

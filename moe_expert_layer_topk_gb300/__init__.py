@@ -21,7 +21,7 @@ __all__ = ["lib", "MoEError", "LIB_PATH", "ENTRY_POINTS",
            "moe_route_topk", "moe_route_topk_chunks", "moe_route_topk_chunks_workspace_size",
            "moe_dispatch", "moe_dispatch_chunked", "moe_dispatch_e4m3_chunked", "moe_dispatch_no_alloc",
            "moe_grouped_gemm_swiglu",
-           "moe_grouped_gemm_swiglu_gather", "moe_grouped_gemm_down",
+           "moe_grouped_gemm_swiglu_gather", "moe_grouped_gemm_down", "moe_grouped_gemm_down_combine",
            "moe_quantize_rows_e4m3", "moe_dispatch_e4m3", "moe_grouped_gemm_swiglu_fp8",
            "moe_grouped_gemm_down_fp8",
            "moe_combine", "moe_combine_bwd", "moe_grouped_gemm_down_bwd",
@@ -54,6 +54,7 @@ ENTRY_POINTS = {
     "moe_grouped_gemm_swiglu": ([_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P], _I),
     "moe_grouped_gemm_swiglu_gather": ([_P, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_grouped_gemm_down": ([_P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _P], _I),
+    "moe_grouped_gemm_down_combine": ([_P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _I, _I, _P, _P, _P], _I),
     "moe_quantize_rows_e4m3": ([_P, _I, _I, _P, _P, _P], _I),
     "moe_dispatch_e4m3": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P], _I),
     "moe_grouped_gemm_swiglu_fp8": ([_P, _P, _P, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P], _I),
@@ -217,6 +218,13 @@ def moe_grouped_gemm_down(h, Wd, num_seg, seg_offsets, seg_expert, R, H, I, E, y
                           stream=None):
     _call("moe_grouped_gemm_down", _ptr(h), _ptr(Wd), num_seg, _ptr(seg_offsets),
           _ptr(seg_expert), R, H, I, E, _ptr(y_perm), _ptr(ws), _nbytes(ws), _stream(stream))
+
+
+def moe_grouped_gemm_down_combine(h, Wd, num_seg, seg_offsets, seg_expert, R, H, I, E, token_of_row,
+                                  row_of_slot, topk_w, T, k, y_acc, y, stream=None):
+    _call("moe_grouped_gemm_down_combine", _ptr(h), _ptr(Wd), num_seg, _ptr(seg_offsets),
+          _ptr(seg_expert), R, H, I, E, _ptr(token_of_row), _ptr(row_of_slot), _ptr(topk_w), T, k,
+          _ptr(y_acc), _ptr(y), _stream(stream))
 
 
 def moe_quantize_rows_e4m3(a, rows, cols, q, scale, stream=None):

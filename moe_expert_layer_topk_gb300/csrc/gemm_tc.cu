@@ -19,6 +19,8 @@
 //                  one fp32 scale per A row and per B row (output channel),
 //                  applied to the accumulator in the epilogue
 //   DOWN_FWD       y = A Wd^T                                     A, B K-major
+//   DOWN_COMBINE   the same, each row scaled by its routing weight and
+//                  added into its token's fp32 output row (fused combine)
 //   DOWN_BWD_DX    dh = A Wd; SwiGLU backward in the epilogue     B MN-major
 //   GATE_UP_BWD_DX dx = dg Wg + du Wu (K = 2I, two B tensors)      B MN-major
 //   DW             dW[g] = sum over group g's rows of A^T B (fp32) A, B MN-major
@@ -69,9 +71,10 @@ enum Kind : int {
   GATE_UP_GATHER = 6,
   GATE_UP_FP8 = 7,
   GATE_UP_GATHER_FP8 = 8,
-  DOWN_FP8 = 9
+  DOWN_FP8 = 9,
+  DOWN_COMBINE = 10
 };
-constexpr int kNumKinds = 10;
+constexpr int kNumKinds = 11;
 __host__ __device__ constexpr bool is_fp8(int k) {
   return k == GATE_UP_FP8 || k == GATE_UP_GATHER_FP8 || k == DOWN_FP8;
 }
@@ -81,7 +84,8 @@ __host__ __device__ constexpr bool is_gate_up(int k) {
   return k == GATE_UP_FWD || k == GATE_UP_GATHER || k == GATE_UP_FP8 || k == GATE_UP_GATHER_FP8;
 }
 __host__ __device__ constexpr bool is_gather(int k) { return k == GATE_UP_GATHER || k == GATE_UP_GATHER_FP8; }
-__host__ __device__ constexpr bool is_down_fwd(int k) { return k == DOWN_FWD || k == DOWN_FP8; }
+// the down-projection kinds (same tiles and operands)
+__host__ __device__ constexpr bool is_down_fwd(int k) { return k == DOWN_FWD || k == DOWN_FP8 || k == DOWN_COMBINE; }
 // reduction elements per k-block: one 128-byte row of the operand type
 __host__ __device__ constexpr int kblock_elems(int k) { return is_fp8(k) ? 128 : BK; }
 
@@ -117,6 +121,13 @@ struct Params {
     };
   };
   int* status;
+  // DOWN_COMBINE: the rows' tokens and routing weights, the fp32 output
+  const int32_t* comb_token;   // token_of_row [M]
+  const int32_t* comb_rows;    // row_of_slot [comb_T, comb_k]
+  const float* comb_w;         // topk_w [comb_T, comb_k]
+  float* comb_out;             // [comb_T, ldo]
+  int comb_T;
+  int comb_k;
 };
 
 struct Ctl {
@@ -186,7 +197,7 @@ struct Cfg {
   // without the segment tables
   static constexpr size_t SMEM_FIXED = 1024 + (size_t)STAGES * STAGE_BYTES + EP_TOTAL + sizeof(Ctl);
 };
-// the configurations launched (cluster pairs for GATE_UP_FWD, GATE_UP_BWD_DX and DOWN_FWD)
+// the configurations launched (cluster pairs for GATE_UP_FWD, GATE_UP_BWD_DX, DOWN_FWD and DOWN_COMBINE)
 static_assert(Cfg<GATE_UP_FWD, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<GATE_UP_GATHER, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<GATE_UP_FP8, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
@@ -198,6 +209,8 @@ static_assert(Cfg<GATE_UP_FWD, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<GATE_UP_BWD_DX, 2>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<GATE_UP_FWD, 2>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<DOWN_FWD, 2>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
+                  Cfg<DOWN_COMBINE, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
+                  Cfg<DOWN_COMBINE, 2>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<DENSE_ADD, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax &&
                   Cfg<DW, 1>::SMEM_FIXED + kMaxTableBytes <= kSmemMax,
               "shared memory budget exceeded");
@@ -781,6 +794,37 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
           sc0 = nx0;
           sc1 = nx1;
         }
+      } else if constexpr (KIND == DOWN_COMBINE) {
+        // out[token] += w * (this lane's row): the row's token from
+        // token_of_row, its routing weight from the token's slot whose row
+        // it is; 16-byte fp32 reductions in L2, in no fixed order
+        int tok = -1;
+        float wt = 0.0f;
+        if (any && lane < nvalid) {
+          const int r = rb + lane;
+          const int tt = __ldg(p.comb_token + r);
+          if (tt >= 0 && tt < p.comb_T) {
+            for (int j = 0; j < p.comb_k; ++j) {
+              if (__ldg(p.comb_rows + (size_t)tt * p.comb_k + j) == r) {
+                tok = tt;
+                wt = __ldg(p.comb_w + (size_t)tt * p.comb_k + j);
+                break;
+              }
+            }
+          }
+        }
+        for (int c = cbeg; any && c < cend; c += cstep) {
+          uint32_t a[32];
+          tmem_ld32(taddr + c, a);
+          tmem_wait_ld();
+          if (tok >= 0) {
+            float* dst = p.comb_out + (size_t)tok * p.ldo + t.n0 + c;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              red_add_f32x4(dst + 4 * i, wt * f32(a[4 * i]), wt * f32(a[4 * i + 1]), wt * f32(a[4 * i + 2]),
+                            wt * f32(a[4 * i + 3]));
+          }
+        }
       } else if constexpr (is_down_fwd(KIND) || KIND == GATE_UP_BWD_DX) {
         const size_t pitch = (size_t)p.ldo * 2;
         for (int c = cbeg; any && c < cend; c += cstep) {
@@ -969,6 +1013,19 @@ __global__ void __launch_bounds__(Cfg<KIND, CTAS>::NTHREADS, 1)
 // address is moved to segment s's first row and whose row extent is the
 // segment's length (rows clamped to [0, rows) like the kernel's own table).
 // An empty segment keeps the template unchanged; no k-block ever reads it.
+// y = bf16(acc) (round to nearest even), eight elements per step.
+__global__ void __launch_bounds__(256) f32_to_bf16_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ y,
+                                                          size_t n8) {
+  pdl_wait();
+  pdl_trigger();
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+    reinterpret_cast<uint4*>(y)[i] =
+        make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+  }
+}
+
 __global__ void dw_segment_maps_kernel(const __grid_constant__ CUtensorMap tplA,
                                        const __grid_constant__ CUtensorMap tplB,
                                        const int32_t* seg_offsets, int num_seg, int rows,
@@ -1091,7 +1148,7 @@ int launch(Params p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensor
 template <int KIND>
 int run(bool pair, const Params& p, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
         const CUtensorMap& o0, const CUtensorMap& o1, cudaStream_t s, const char* what) {
-  if constexpr (KIND == GATE_UP_BWD_DX || KIND == GATE_UP_FWD || KIND == DOWN_FWD) {
+  if constexpr (KIND == GATE_UP_BWD_DX || KIND == GATE_UP_FWD || KIND == DOWN_FWD || KIND == DOWN_COMBINE) {
     if (pair) return launch<KIND, 2>(p, a, b0, b1, o0, o1, s, what);
   }
   return launch<KIND, 1>(p, a, b0, b1, o0, o1, s, what);
@@ -1416,6 +1473,53 @@ int moe_grouped_gemm_down(const void* h, const void* Wd, int num_seg, const int3
   CUtensorMap to;
   if (int rc = make_out_map(&to, y_perm, H, R, false)) return rc;
   return run<DOWN_FWD>(pair, p, ta, tb, tb, to, to, static_cast<cudaStream_t>(stream), fn);
+}
+
+int moe_grouped_gemm_down_combine(const void* h, const void* Wd, int num_seg, const int32_t* seg_offsets,
+                                  const int32_t* seg_expert, int R, int H, int I, int E,
+                                  const int32_t* token_of_row, const int32_t* row_of_slot, const float* topk_w,
+                                  int T, int k, float* y_acc, void* y, void* stream) {
+  clear_error();
+  const char* fn = "moe_grouped_gemm_down_combine";
+  if (int rc = check_grouped(fn, num_seg, seg_offsets, R, H, I, E)) return rc;
+  if (T < 0 || k < 1 || k > 32) return fail(MOE_ERR_INVALID_ARG, "%s: need T>=0, 1<=k<=32", fn);
+  const bool rows = R > 0 && num_seg > 0;
+  if ((T > 0 && (!y_acc || !y)) || (rows && (!h || !Wd || !token_of_row || (T > 0 && (!row_of_slot || !topk_w)))))
+    return fail(MOE_ERR_INVALID_ARG, "%s: NULL pointer argument", fn);
+  if ((h && !aligned16(h)) || (Wd && !aligned16(Wd)) || (y_acc && !aligned16(y_acc)) || (y && !aligned16(y)))
+    return fail(MOE_ERR_ALIGNMENT, "%s: tensors must be 16-byte aligned", fn);
+  if (T == 0) return MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(y_acc, 0, sizeof(float) * (size_t)T * H, s);
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+  if (rows) {
+    Params p = base_params(num_seg, seg_offsets, seg_expert, E);
+    p.M = R;
+    p.N = H;
+    p.K = I;
+    p.BN = pick_bn(H);
+    p.n_tiles = H / p.BN;
+    p.b_group_rows = H;
+    p.ldo = H;
+    p.comb_token = token_of_row;
+    p.comb_rows = row_of_slot;
+    p.comb_w = topk_w;
+    p.comb_out = y_acc;
+    p.comb_T = T;
+    p.comb_k = k;
+    CUtensorMap ta, tb;
+    if (int rc = make_tmap(&ta, h, I, R, 64, BM)) return rc;
+    const bool pair = pair_for_rows(p.BN, R, num_seg, E);
+    if (int rc = make_tmap(&tb, Wd, I, (uint64_t)E * H, 64, p.BN / (pair ? 2 : 1))) return rc;
+    // no output map: the epilogue adds straight into y_acc (the A map fills the slots)
+    if (int rc = run<DOWN_COMBINE>(pair, p, ta, tb, tb, ta, ta, s, fn)) return rc;
+  }
+  const size_t n8 = (size_t)T * H / 8;
+  const int sms = sm_count();
+  const size_t blocks = (n8 + 255) / 256, cap = (size_t)(sms > 0 ? sms : 148) * 8;
+  launch_pdl(f32_to_bf16_kernel, (unsigned)(blocks < cap ? blocks : cap), 256, 0, s, static_cast<const float*>(y_acc),
+             static_cast<__nv_bfloat16*>(y), n8);
+  return check_launch(fn);
 }
 
 // B2 and B3 each run as two halves: the dX GEMM (rows x weights, with the

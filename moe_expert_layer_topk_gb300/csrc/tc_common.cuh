@@ -138,6 +138,13 @@ __device__ __forceinline__ void tma_reduce_add_2d_hint(const CUtensorMap* map, u
       : "memory");
 }
 
+// *dst += {a, b, c, d} as one 16-byte reduction in L2 (dst 16-byte aligned).
+__device__ __forceinline__ void red_add_f32x4(float* dst, float a, float b, float c, float d) {
+  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
 // One epilogue warp's staging ring (see EP_*).  Lane i holds row i of a box.
 template <int SLOTS = EP_SLOTS>
 struct EpRing {

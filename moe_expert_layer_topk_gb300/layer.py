@@ -11,7 +11,8 @@ import torch
 
 from . import (moe_combine, moe_combine_bwd, moe_dispatch_bwd, moe_dispatch_chunked,
                moe_dispatch_e4m3_chunked, moe_grouped_gemm_bwd_workspace_size,
-               moe_grouped_gemm_down, moe_grouped_gemm_down_bwd, moe_grouped_gemm_down_fp8,
+               moe_grouped_gemm_down, moe_grouped_gemm_down_bwd, moe_grouped_gemm_down_combine,
+               moe_grouped_gemm_down_fp8,
                moe_grouped_gemm_swiglu, moe_grouped_gemm_swiglu_bwd_dw, moe_grouped_gemm_swiglu_bwd_dx,
                moe_grouped_gemm_swiglu_fp8, moe_set_gemm_sm_limit, sm_count,
                moe_grouped_gemm_swiglu_gather, moe_quantize_rows_e4m3, moe_route_topk_bwd,
@@ -33,19 +34,28 @@ class MoELayer:
     fp8 (forward only): dispatch writes the permuted rows as e4m3 codes with
     one scale per token (moe_dispatch_e4m3), h is quantised per row, and
     both GEMMs run on e4m3 weights prepared once by `quantize_weights` (one
-    scale per output channel)."""
+    scale per output channel).
+
+    fused_combine (forward only, bf16): the down GEMM adds each weighted row
+    into its token's fp32 row and y is rounded from those
+    (moe_grouped_gemm_down_combine), so y_perm is never written; the order
+    of those fp32 additions is not fixed from run to run.  It saves the
+    [T*k, H] y_perm buffer but measured slower than down + combine."""
 
     def __init__(self, T: int, H: int, I: int, E: int, k: int, ep_size: int = 1, *,
                  training: bool = True, fused_dispatch: bool = False, fp8: bool = False,
-                 device: str | torch.device = "cuda"):
+                 fused_combine: bool = False, device: str | torch.device = "cuda"):
         if fp8 and training:
             raise ValueError("the e4m3 path is forward only")
+        if fused_combine and (training or fp8):
+            raise ValueError("fused_combine is a bf16 forward-only path (the combine backward needs y_perm)")
         if fused_dispatch and training:
             raise ValueError("fused_dispatch keeps no x_perm, which the backward pass needs")
         self.T, self.H, self.I, self.E, self.k, self.ep_size = T, H, I, E, k, ep_size
         self.R = R = T * k
         self.training = training
         self.fused_dispatch = fused_dispatch
+        self.fused_combine = fused_combine
         self.fp8 = fp8
         self._x = None
         self._side = None  # side stream of the backward's tail (created on first use)
@@ -65,7 +75,8 @@ class MoELayer:
         self.token_of_row = e(R, dt=i32)
         self.h = e(R, I, dt=bf)
         self.gu = e(R, 2 * I, dt=bf) if training else None
-        self.y_perm = e(R, H, dt=bf)
+        self.y_perm = None if fused_combine else e(R, H, dt=bf)
+        self.y_acc = e(T, H, dt=f32) if fused_combine else None
         self.y = e(T, H, dt=bf)
         if fp8:
             u8 = torch.uint8
@@ -111,9 +122,10 @@ class MoELayer:
         moe_dispatch_chunked(x, self.topk_idx, self.offsets, self.chunk_prefix, self.T, self.H, self.E, self.k,
                              self.x_perm, self.row_of_slot, self.token_of_row, stream)
 
-    def experts(self, Wg, Wu, Wd, stream=None):
+    def experts(self, Wg, Wu, Wd, stream=None, y=None):
         """Wg, Wu, Wd: bf16 expert weights, or (fp8 layers) the dict that
-        `quantize_weights` returns, passed as Wg (Wu and Wd unused)."""
+        `quantize_weights` returns, passed as Wg (Wu and Wd unused).
+        y: the output of a fused_combine layer (default: the layer's own)."""
         if self.fp8:
             w = Wg
             T, H, I, E, R = self.T, self.H, self.I, self.E, self.R
@@ -130,6 +142,11 @@ class MoELayer:
         else:
             moe_grouped_gemm_swiglu(self.x_perm, Wg, Wu, self.E, self.offsets, None, self.R, self.H,
                                     self.I, self.E, self.h, self.gu, None, stream)
+        if self.fused_combine:
+            moe_grouped_gemm_down_combine(self.h, Wd, self.E, self.offsets, None, self.R, self.H, self.I,
+                                          self.E, self.token_of_row, self.row_of_slot, self.topk_w, self.T,
+                                          self.k, self.y_acc, self.y if y is None else y, stream)
+            return
         moe_grouped_gemm_down(self.h, Wd, self.E, self.offsets, None, self.R, self.H, self.I,
                               self.E, self.y_perm, None, stream)
 
@@ -141,8 +158,9 @@ class MoELayer:
         """y: optional bf16 [T,H] output tensor (default: the layer's own)."""
         self.route(x, Wr, bias, stream)
         self.dispatch(x, stream)
-        self.experts(Wg, Wu, Wd, stream)
-        self.combine(stream, y)
+        self.experts(Wg, Wu, Wd, stream, y)
+        if not self.fused_combine:
+            self.combine(stream, y)
         return self.y if y is None else y
 
     def capture_forward(self, x, Wr, bias, Wg, Wu, Wd) -> "torch.cuda.CUDAGraph":
