@@ -440,6 +440,19 @@ def run_ours(args, shape, inp):
     torch.cuda.synchronize(dev)
     fwd_ms = fs.elapsed_time(fe) / args.steps
     del flayer
+    # the same forward with the down GEMM and the combine fused (no y_perm)
+    flayer = m.MoELayer(fshape.T, fshape.H, fshape.I, fshape.E, fshape.k, fshape.ep_size,
+                        training=False, fused_dispatch=True, fused_combine=True, device=dev)
+    for _ in range(args.warmup):
+        flayer.forward(fg["x"], fg["Wr"], fg["bias"], fg["Wg"], fg["Wu"], fg["Wd"])
+    torch.cuda.synchronize(dev)
+    fs.record(stream)
+    for _ in range(args.steps):
+        flayer.forward(fg["x"], fg["Wr"], fg["bias"], fg["Wg"], fg["Wu"], fg["Wd"])
+    fe.record(stream)
+    torch.cuda.synchronize(dev)
+    fused_combine_ms = fs.elapsed_time(fe) / args.steps
+    del flayer
     fp8 = run_fp8_forward(m, fg, fshape, dev, stream, args)
     del fg
     pk, pk_kind = peaks()
@@ -537,6 +550,10 @@ def run_ours(args, shape, inp):
         "fwd_tokens_per_s": fshape.T / (fwd_ms * 1e-3),
         "fwd_ms": fwd_ms, "fwd_config": {"workload": FWD_WORKLOAD, "T": fshape.T,
                        "path": "fused dispatch: rows gathered from x by the gate/up GEMM"},
+        "fused_combine_fwd": {"workload": FWD_WORKLOAD, "T": fshape.T,
+                              "tokens_per_s": fshape.T / (fused_combine_ms * 1e-3), "ms": fused_combine_ms,
+                              "path": "fused dispatch and fused combine (the down GEMM adds its weighted rows "
+                                      "into the tokens' fp32 rows; no y_perm; not the headline path)"},
         "fp8_fwd": fp8,
         **extra,
         "grouped_gemm_tflops": gemm_tflops,
