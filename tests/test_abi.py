@@ -100,6 +100,25 @@ def test_grouped_gemm_rejects_bad_shapes(L):
                                        None) == ALIGN
 
 
+def test_fused_combine_rejects_bad_args(L):
+    # moe_grouped_gemm_down_combine(h, Wd, num_seg, seg_offsets, seg_expert, R, H, I, E,
+    #                               token_of_row, row_of_slot, topk_w, T, k, y_acc, y, stream)
+    P = FAKE
+    assert L.moe_grouped_gemm_down_combine(P, P, 8, P, None, 64, 100, 64, 8, P, P, P, 32, 2, P, P, None) == SHAPE
+    assert L.moe_grouped_gemm_down_combine(P, P, 8, P, None, 64, 128, 64, 8, P, P, P, 32, 0, P, P, None) == INVALID
+    assert L.moe_grouped_gemm_down_combine(P, P, 8, P, None, 64, 128, 64, 8, P, P, P, 32, 33, P, P, None) == INVALID
+    assert L.moe_grouped_gemm_down_combine(P, P, 8, P, None, 64, 128, 64, 8, None, P, P, 32, 2, P, P,
+                                           None) == INVALID
+    assert L.moe_grouped_gemm_down_combine(P, P, 8, P, None, 64, 128, 64, 8, P, P, P, 32, 2, None, P,
+                                           None) == INVALID
+    assert L.moe_grouped_gemm_down_combine(P, P, 8, P, None, 64, 128, 64, 8, P, P, P, 32, 2, P + 8, P,
+                                           None) == ALIGN
+    assert "moe_grouped_gemm_down_combine" in _err(L)
+    # no tokens: nothing to write, no launch
+    assert L.moe_grouped_gemm_down_combine(P, P, 8, P, None, 0, 128, 64, 8, P, P, P, 0, 2, None, None,
+                                           None) == OK
+
+
 def test_rows_ops_reject_bad_args(L):
     P = FAKE
     assert L.moe_combine(P, P, P, 16, 128, 33, P, None) == SHAPE
