@@ -50,7 +50,9 @@
  *     tables) cannot be checked on the host.  Kernels clamp every access
  *     they derive from it, skip what is out of range, and record a device
  *     status word that moe_read_device_status() returns.
- *   - Results are deterministic: no floating-point atomics anywhere.
+ *   - Results are deterministic (no floating-point atomics), except those
+ *     of moe_grouped_gemm_down_combine, which adds with L2 reductions in no
+ *     fixed order.
  *   - Expert weights are read only.  Weight gradients are fp32 and are
  *     overwritten, or added to when `accumulate` != 0.
  */
