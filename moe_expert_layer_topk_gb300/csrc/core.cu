@@ -140,7 +140,7 @@ int moe_probe_fma(int packed, int per_sm, int iters, float* out, long long* fmas
   return moe::check_launch("moe_probe_fma");
 }
 
-int moe_abi_version(void) { return 102; }
+int moe_abi_version(void) { return 103; }
 
 const char* moe_last_error_string(void) { return g_err; }
 

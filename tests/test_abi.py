@@ -25,6 +25,10 @@ def header_decls():
     return {name: args for name, args in DECL.findall(HEADER.read_text())}
 
 
+def test_abi_version(L):
+    assert L.moe_abi_version() == 103  # 1.03: the fused down + combine call
+
+
 def test_header_symbols_exported(L):
     decls = header_decls()
     assert len(decls) >= 16
