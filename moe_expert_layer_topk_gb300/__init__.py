@@ -37,6 +37,9 @@ LIB_PATH: Path = _build_mod.LIB
 _P, _I, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 
 # name -> (argtypes, restype); mirrors include/moe_topk.h
+# the ABI version of include/moe_topk.h these signatures follow
+ABI_VERSION = 103
+
 ENTRY_POINTS = {
     "moe_abi_version": ([], _I),
     "moe_last_error_string": ([], ctypes.c_char_p),
@@ -98,6 +101,9 @@ def lib(path: Path | str | None = None) -> ctypes.CDLL:
             f = getattr(L, name)
             f.argtypes = args
             f.restype = res
+        if L.moe_abi_version() != ABI_VERSION:
+            raise RuntimeError(f"CUDA library {p} has ABI version {L.moe_abi_version()}, this binding "
+                               f"expects {ABI_VERSION}: rebuild it")
         _lib = L
     return _lib
 
