@@ -128,6 +128,8 @@ GEMM_CASES = {
     "ragged_empty": (300, 256, 128, 4, [0, 0, 77, 77, 300], None),
     "three_n_tiles_uncovered_tail": (520, 256, 384, 3, [0, 129, 390, 500], None),
     "segments": (400, 384, 256, 4, [0, 40, 40, 170, 200, 399, 400], [2, 0, 1, 3, 0, 2]),
+    # two long segments whose last 128-row tiles hold 1 and 75 rows
+    "long_segments": (1100, 256, 256, 2, [0, 513, 1100], None),
 }
 
 
@@ -227,7 +229,8 @@ def _oracle_fp8_chain(inp, f):
     return oracle.combine(rne_bf16(yp), f["rt"]["topk_w"], f["dp"]["row_of_slot"]), W
 
 
-@pytest.mark.parametrize("T,H,I,E,k,ep", [(256, 256, 128, 8, 2, 2), (300, 256, 256, 12, 3, 4)])
+@pytest.mark.parametrize("T,H,I,E,k,ep", [(256, 256, 128, 8, 2, 2), (300, 256, 256, 12, 3, 4),
+                                         (1024, 256, 128, 4, 2, 2)])  # the last: ~512 rows per expert
 def test_fp8_layer_forward(T, H, I, E, k, ep):
     inp = inputs(T, H, I, E, k, seed=5, ep=ep)
     g = to_dev(inp)
