@@ -838,6 +838,27 @@ def run_profile_fp8(args):
                       "device_status": m.moe_read_device_status(reset=True)}))
 
 
+def run_profile_fwd(args):
+    """Untimed bf16 forward passes of one layer shape, fused dispatch, with
+    or without the fused combine (for ncu captures)."""
+    import torch
+
+    import moe_expert_layer_topk_gb300 as m
+    from moe_expert_layer_topk_gb300.synth import LayerShape, make_layer_inputs
+    spec, _, mode = args.profile_fwd.partition(":")
+    T, H, I, E, k = (int(v) for v in spec.split(","))
+    shape = LayerShape(T=T, H=H, I=I, E=E, k=k, ep_size=1)
+    inp = make_layer_inputs(shape, 0, with_dy=False)
+    g = {n: (v.cuda() if isinstance(v, torch.Tensor) else v) for n, v in inp.items()}
+    layer = m.MoELayer(T, H, I, E, k, 1, training=False, fused_dispatch=True,
+                       fused_combine=(mode == "fused_combine"))
+    for _ in range(args.steps):
+        layer.forward(g["x"], g["Wr"], None, g["Wg"], g["Wu"], g["Wd"])
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_fwd": [T, H, I, E, k], "fused_combine": mode == "fused_combine",
+                      "passes": args.steps, "device_status": m.moe_read_device_status(reset=True)}))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -851,6 +872,8 @@ def main(argv=None):
                     help="run --steps untimed forward+backward passes of this shape and exit")
     ap.add_argument("--profile-router", default=None, metavar="T,H,E,k",
                     help="run --steps untimed router passes and exit")
+    ap.add_argument("--profile-fwd", default=None, metavar="T,H,I,E,k[:fused_combine]",
+                    help="run --steps untimed bf16 forward passes (fused dispatch) of this shape and exit")
     ap.add_argument("--profile-fp8", default=None, metavar="T,H,I,E,k",
                     help="run --steps untimed fp8 forward passes of this shape and exit")
     args = ap.parse_args(argv)
@@ -860,6 +883,8 @@ def main(argv=None):
         return run_profile_case(args)
     if args.profile_fp8:
         return run_profile_fp8(args)
+    if args.profile_fwd:
+        return run_profile_fwd(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     from moe_expert_layer_topk_gb300.synth import CONFIGS, make_layer_inputs
